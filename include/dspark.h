@@ -1,0 +1,226 @@
+/*
+ * dspark.h -- C ABI of the GB300 DSpark cycle library (libdspark.so).
+ *
+ * One DSpark decoding cycle has three data-parallel parts, each one entry
+ * point here:
+ *
+ *   dspark_draft_markov / dspark_draft_rnn
+ *       the sequential stage of the semi-autoregressive drafter: for
+ *       k = 1..gamma, B_k is added to the parallel backbone's base logits
+ *       U_k and x_k is sampled from q_k = softmax((U_k + B_k) / T)
+ *       ("DSpark: DeepSeek 线上跑的投机解码" blog, section 3.2, MarkovHead,
+ *       RNNHead and the sequential-stage loop; DSpark explainer, section 03,
+ *       q_k = softmax(U_k + B_k) with B_k = W1[x_{k-1}] W2).
+ *   dspark_verify
+ *       lossless verification: accept x with min(1, p(x)/q(x)), on the first
+ *       rejection resample from max(p - q, 0) normalised, emit a bonus token
+ *       when every verified draft is accepted (DSpark explainer, section 05,
+ *       alpha(x) and r(v); section 02 for the greedy T = 0 form).
+ *   dspark_schedule
+ *       the confidence scheduler: a_j = c_1 ... c_j, B = sum_r (1 + l_r),
+ *       tau = sum_r (1 + sum_{j <= l_r} a_{r,j}), Theta = tau * SPS(B), and
+ *       the greedy early stop over candidates sorted by a (blog section 4.3;
+ *       explainer section 04, "algorithm details").
+ *
+ * Conventions for every entry point:
+ *  - Tensor arguments are DEVICE pointers owned by the caller, row-major and
+ *    contiguous.  The library never allocates device memory: all scratch
+ *    lives in a caller-provided workspace whose size the matching
+ *    dspark_*_workspace_size() returns (256-byte aligned pointer required).
+ *  - Work is enqueued asynchronously on the caller's stream `stream`
+ *    (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *  - dtype arguments take DSPARK_F32 or DSPARK_BF16 (bf16 = IEEE bfloat16).
+ *  - The return value is DSPARK_OK or a negative DSPARK_ERR_* code.  Host
+ *    checks (null pointers, sizes, dtypes, workspace size) fail before any
+ *    work is enqueued.  Conditions that only the device can see (a token id
+ *    outside [0, V), a bounded wait that ran out) do not fault: the kernel
+ *    skips the bad access, records the condition in a status word at the
+ *    start of the workspace and finishes; dspark_workspace_status() reads
+ *    and clears it.
+ *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key
+ *    (seed low 32 bits, seed high 32 bits) and counter
+ *    (v / 4, request id, position, stream); index v takes output word v mod 4
+ *    and becomes u = ((w >> 9) + 1/2) * 2^-23 in (0, 1).  Streams:
+ *    0 = draft Gumbel noise (v = vocabulary index, position k = 1..gamma),
+ *    1 = acceptance uniform (v = 0, position k),
+ *    2 = residual / bonus draw (v = tree level, position = the position sampled).
+ *    The request id is req_ids[i] (device array) or i when req_ids is NULL.
+ *  - Nothing is thrown across the ABI.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum dspark_dtype { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
+
+enum dspark_status {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARG = -1,     /* null pointer, negative size, bad temperature */
+    DSPARK_ERR_UNSUPPORTED_DTYPE = -2,
+    DSPARK_ERR_SHAPE = -3,           /* sizes outside the supported range */
+    DSPARK_ERR_CUDA = -4,            /* a CUDA runtime call failed */
+    DSPARK_ERR_TIMEOUT = -5,         /* a bounded device wait ran out */
+    DSPARK_ERR_BAD_TOKEN = -6,       /* a token id outside [0, V) reached a kernel */
+    DSPARK_ERR_UNIMPLEMENTED = -7,
+    DSPARK_ERR_WORKSPACE = -8        /* workspace null, misaligned or too small */
+};
+
+/* Text for a status code (static storage). */
+const char* dspark_strerror(int status);
+/* Library version string (static storage). */
+const char* dspark_version(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word at the
+ * start of workspace `ws` (any workspace this library was given).  Returns
+ * DSPARK_OK, DSPARK_ERR_BAD_TOKEN, DSPARK_ERR_TIMEOUT or DSPARK_ERR_CUDA.
+ */
+int dspark_workspace_status(void* ws, void* stream);
+
+/* ------------------------------------------------------------------ draft */
+
+/*
+ * Workspace bytes for dspark_draft_markov / dspark_draft_rnn (d = 0 for the
+ * Markov head).  Returns 0 for unsupported sizes.
+ */
+size_t dspark_draft_workspace_size(int R, int gamma, int V, int r, int d);
+
+/*
+ * Markov-head drafting: the sequential stage with B_k = W1[x_{k-1}] W2
+ * (blog section 3.2 MarkovHead; explainer section 03), x_0 = anchor.
+ *
+ *   U       [R, gamma, V]  u_dtype   base logits of the parallel backbone
+ *   anchor  [R]            int32     x_0 per request, in [0, V)
+ *   W1      [V, r]         w_dtype   rank-r embedding of the previous token
+ *   W2      [r, V]         w_dtype   rank-r projection to the vocabulary
+ *   seed, req_ids, temperature       RNG key, request ids (NULL = index),
+ *                                    T > 0 samples, T = 0 takes the argmax
+ * Outputs (device, caller-owned):
+ *   tokens  [R, gamma]     int32     x_k
+ *   q_tok   [R, gamma]     float     q_k(x_k) (1 at T = 0)
+ *   lse     [R, gamma]     double    log sum_v exp((U_k + B_k)[v] / T) (0 at T = 0)
+ *   code    [R, gamma, r]  float     e_k = W1[x_{k-1}], the rank-r code that
+ *                                    gives B_k = e_k W2 (consumed by verify)
+ * Sampling: x_k = argmax_v (U_k + B_k)[v] / T + G_v with Gumbel noise
+ * G_v = -ln(-ln u_v) from stream 0; ties go to the lowest v.
+ * B_k and q_k are never written to memory.
+ * Requirements: R >= 1, 1 <= gamma <= 64, V >= 2 with V % 8 == 0 for bf16 and
+ * V % 4 == 0 for f32 storage, V <= 2^20, 1 <= r <= 1024, T >= 0 and finite.
+ */
+int dspark_draft_markov(const void* U, int u_dtype, const int32_t* anchor,
+                        const void* W1, const void* W2, int w_dtype,
+                        int R, int gamma, int V, int r,
+                        uint64_t seed, const uint32_t* req_ids, float temperature,
+                        int32_t* tokens, float* q_tok, double* lse, float* code,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * RNN-head drafting (blog section 3.2 RNNHead.step): per step
+ *   z   = [s_{k-1}, W1[x_{k-1}], h_k]                    (2r + d)
+ *   G   = z Wgco, split into gate | cand | out           (3r, columns in that order)
+ *   s_k = sigmoid(gate) * s_{k-1} + (1 - sigmoid(gate)) * tanh(cand),  s_0 = 0
+ *   e_k = tanh(out),  B_k = e_k W2
+ * and the same sampling as dspark_draft_markov.
+ *   H      [R, gamma, d]  bfloat16   backbone hidden states h_k
+ *   Wgco   [2r + d, 3r]   w_dtype
+ *   state_out [R, r]      float      s_gamma (may be NULL)
+ * code receives e_k = tanh(out_k).  Requirements as for the Markov head plus
+ * 1 <= d <= 16384.
+ */
+int dspark_draft_rnn(const void* U, int u_dtype, const int32_t* anchor,
+                     const void* W1, const void* W2, const void* Wgco, int w_dtype,
+                     const void* H, int d,
+                     int R, int gamma, int V, int r,
+                     uint64_t seed, const uint32_t* req_ids, float temperature,
+                     int32_t* tokens, float* q_tok, double* lse, float* code,
+                     float* state_out,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------- verify */
+
+size_t dspark_verify_workspace_size(int R, int gamma, int V, int r);
+
+/*
+ * Lossless verification (explainer section 05; blog section 1).
+ *
+ *   P          [R, gamma + 1, V] p_dtype  target logits; row k-1 scores draft
+ *                                         position k, row gamma is the bonus row
+ *   U, W2, tokens, q_tok, lse, code       as produced by a draft call
+ *   verify_len [R] int32 or NULL          l_r in [0, gamma]; NULL verifies all
+ * For T > 0, with p_k = softmax(P_{k-1} / T), for k = 1..l_r:
+ *   u_k from stream 1; accept x_k iff u_k < p_k(x_k) / q_k(x_k).
+ * On the first rejection j: draw from r(v) = max(p_j - q_j, 0) / Z with
+ * q_j(v) = exp((U_j + code_j W2)[v] / T - lse_j) rebuilt on the fly; if Z = 0
+ * (rounding only) draw from p_j.  If all l_r drafts are accepted: draw the
+ * bonus token from p_{l_r + 1}.  Both draws go down a binary sum tree over
+ * the vocabulary (depth ceil(log2 V)), one stream-2 uniform per level: at a
+ * node with child masses (mL, mR) go left iff u * (mL + mR) < mL.
+ * For T = 0: accept iff x_k equals argmax P_{k-1} (lowest index); the first
+ * mismatch emits that argmax; a fully accepted block emits argmax P_{l_r}.
+ * Outputs:
+ *   out_tokens [R, gamma + 1] int32  accepted drafts then the new token, -1 padded
+ *   accept_len [R]            int32  accepted drafts
+ *   n_out      [R]            int32  accept_len + 1
+ *   p_tok      [R, gamma]     float  p_k(x_k) for tested positions (may be NULL)
+ *   lse_p      [R, gamma + 1] double log-sum-exp of P_k / T for rows read (may be NULL)
+ * Rows the request never reads hold NaN in p_tok / lse_p.
+ */
+int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype,
+                  const void* W2, int w_dtype,
+                  const int32_t* tokens, const float* q_tok, const double* lse,
+                  const float* code, const int32_t* verify_len,
+                  int R, int gamma, int V, int r,
+                  uint64_t seed, const uint32_t* req_ids, float temperature,
+                  int32_t* out_tokens, int32_t* accept_len, int32_t* n_out,
+                  float* p_tok, double* lse_p,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------- schedule */
+
+size_t dspark_schedule_workspace_size(int R, int gamma);
+
+/*
+ * Confidence scheduler (blog section 4.3; explainer section 04).
+ *   c        [R, gamma]  float   calibrated confidences c_{r,j} in [0, 1]
+ *   sps      [n_sps]     double  steps per second at token batch B = index;
+ *                                entries past the table count as 0
+ * a_{r,j} = c_{r,1} ... c_{r,j} (float32 product in position order).  The
+ * candidates (r, j) with a > 0 are ordered by a descending, then r, then j
+ * ascending; tau_n = R + a_(1) + ... + a_(n) (double), Theta(n) =
+ * tau_n * SPS[R + n]; n* is the first n with Theta(n + 1) <= Theta(n)
+ * (all candidates if none); l_r counts request r among the first n*.
+ * Inputs are c and SPS only: the schedule never sees the target or the RNG.
+ * Outputs: verify_len [R] int32, theta [1] double = Theta(n*), n_star [1] int32.
+ * Requirements: 1 <= R, 1 <= gamma <= 64, R * gamma <= 8192, n_sps >= 1.
+ */
+int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gamma,
+                    int32_t* verify_len, double* theta, int32_t* n_star,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* -------------------------------------------------------------- profiling */
+
+/*
+ * Kernel timing for benchmarks (no counterpart on the pages).  While enabled
+ * (on != 0), every kernel the library launches is bracketed by two CUDA
+ * events recorded on the caller's stream; dspark_profile_collect()
+ * synchronises those events and returns, per launch in issue order, a kernel
+ * name id and its device time in milliseconds (at most `cap` entries; the
+ * return value is the number of launches recorded, which may exceed `cap`),
+ * then forgets them.  dspark_profile_kernel_name() maps an id to its name.
+ * Disabled by default; costs two event records per launch when enabled.
+ * Host-side state, not thread-safe.
+ */
+int dspark_profile_enable(int on);
+int dspark_profile_collect(int32_t* name_ids, float* ms, int cap);
+const char* dspark_profile_kernel_name(int name_id);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H */

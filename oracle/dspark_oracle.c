@@ -601,9 +601,14 @@ int oracle_schedule_closed(const float* c, const double* sps, int n_sps, int R, 
     int nstar = n;
     for (int i = 0; i < n; ++i)
         if (!(th[i + 1] > th[i])) { nstar = i; break; }
+    /* smallest relative gap over every comparison the stop rule made */
     double gap = INFINITY;
-    if (nstar < n && th[nstar] != 0.0) gap = fabs(th[nstar + 1] - th[nstar]) / fabs(th[nstar]);
-    else if (nstar < n) gap = 0.0;
+    int last = nstar < n ? nstar : n - 1;
+    for (int i = 0; i <= last; ++i) {
+        double den = fabs(th[i]) > 0.0 ? fabs(th[i]) : 1.0;
+        double g = fabs(th[i + 1] - th[i]) / den;
+        if (g < gap) gap = g;
+    }
     if (min_rel_gap) *min_rel_gap = gap;
     for (int ri = 0; ri < R; ++ri) lengths[ri] = 0;
     for (int i = 0; i < nstar; ++i) lengths[cand[i].r] += 1;

@@ -97,8 +97,8 @@ int oracle_schedule_loop(const float* c, const double* sps, int n_sps, int R, in
                          int32_t* lengths, double* theta);
 /* Same scheduler in closed form: Theta(n) = tau_n * SPS[R+n] over the sorted
  * prefix sums; n* = first n with Theta(n+1) <= Theta(n).  min_rel_gap gets
- * the relative gap |Theta(n*+1) - Theta(n*)| / Theta(n*) of the stopping
- * comparison (+inf when the list is exhausted).  Returns n*. */
+ * the smallest relative gap |Theta(n+1) - Theta(n)| / Theta(n) over the
+ * comparisons n = 0..n* the stop rule made (+inf if none).  Returns n*. */
 int oracle_schedule_closed(const float* c, const double* sps, int n_sps, int R, int gamma,
                            int32_t* lengths, double* theta, double* min_rel_gap);
 

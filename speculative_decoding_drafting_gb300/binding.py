@@ -1,0 +1,250 @@
+"""Thin Python binding of libdspark.so (ctypes; argument marshalling only).
+
+Every function takes CUDA torch tensors, passes their device pointers and the
+current CUDA stream to the C ABI of ``include/dspark.h`` and returns the
+output tensors it allocated.  All arithmetic of the cycle runs in the
+library's kernels; this module only checks types, allocates outputs and the
+workspace, and translates status codes into exceptions.  There is no CPU
+fallback: if the library cannot be loaded, importing a function raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+F32 = 0
+BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported dtype", -3: "unsupported sizes",
+          -4: "CUDA runtime error", -5: "bounded device wait ran out", -6: "token id outside [0, V)",
+          -7: "not implemented", -8: "workspace null, misaligned or too small"}
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed with status {code} ({STATUS.get(code, 'unknown')})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libdspark.so (building it first if asked); raises if unavailable."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libdspark.so not found at {path}; run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        P, i32, u64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+        L.dspark_strerror.argtypes = [i32]
+        L.dspark_strerror.restype = ctypes.c_char_p
+        L.dspark_version.restype = ctypes.c_char_p
+        L.dspark_workspace_status.argtypes = [P, P]
+        L.dspark_draft_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.dspark_draft_workspace_size.restype = sz
+        L.dspark_draft_markov.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, u64, P, f32,
+                                          P, P, P, P, P, sz, P]
+        L.dspark_draft_rnn.argtypes = [P, i32, P, P, P, P, i32, P, i32, i32, i32, i32, i32, u64, P, f32,
+                                       P, P, P, P, P, P, sz, P]
+        L.dspark_verify_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.dspark_verify_workspace_size.restype = sz
+        L.dspark_verify.argtypes = [P, i32, P, i32, P, i32, P, P, P, P, P, i32, i32, i32, i32, u64, P, f32,
+                                    P, P, P, P, P, P, sz, P]
+        L.dspark_schedule_workspace_size.argtypes = [i32, i32]
+        L.dspark_schedule_workspace_size.restype = sz
+        L.dspark_schedule.argtypes = [P, P, i32, i32, i32, P, P, P, P, sz, P]
+        L.dspark_profile_enable.argtypes = [i32]
+        L.dspark_profile_collect.argtypes = [P, P, i32]
+        L.dspark_profile_kernel_name.argtypes = [i32]
+        L.dspark_profile_kernel_name.restype = ctypes.c_char_p
+        for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_verify", "dspark_schedule",
+                     "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
+            getattr(L, name).restype = i32
+        _lib = L
+        return _lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libdspark takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libdspark takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"storage dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise DsparkError(fn, code)
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks; the first
+    # word (the device status word) must start at zero.
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def version() -> str:
+    return load().dspark_version().decode()
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    return load().dspark_workspace_status(_p(ws), _stream(stream))
+
+
+def draft_workspace_bytes(R, gamma, V, r, d=0) -> int:
+    return int(load().dspark_draft_workspace_size(R, gamma, V, r, d))
+
+
+def verify_workspace_bytes(R, gamma, V, r) -> int:
+    return int(load().dspark_verify_workspace_size(R, gamma, V, r))
+
+
+def schedule_workspace_bytes(R, gamma) -> int:
+    return int(load().dspark_schedule_workspace_size(R, gamma))
+
+
+def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None, ws=None, out=None, stream=None):
+    """Markov-head drafting (``dspark_draft_markov``).  Returns a dict of outputs."""
+    L = load()
+    R, gamma, V = U.shape
+    r = W1.shape[1]
+    dev = U.device
+    if out is None:
+        out = dict(tokens=torch.empty((R, gamma), dtype=torch.int32, device=dev),
+                   q_tok=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   lse=torch.empty((R, gamma), dtype=torch.float64, device=dev),
+                   code=torch.empty((R, gamma, r), dtype=torch.float32, device=dev))
+    nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, 0)
+    if ws is None:
+        ws = _workspace(nbytes, dev)
+    code = L.dspark_draft_markov(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _dt(W1), R, gamma, V, r,
+                                 int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
+                                 _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
+                                 _p(ws), ws.numel(), _stream(stream))
+    _check("dspark_draft_markov", code)
+    out["ws"] = ws
+    return out
+
+
+def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids=None, ws=None, out=None,
+              stream=None):
+    """RNN-head drafting (``dspark_draft_rnn``)."""
+    L = load()
+    R, gamma, V = U.shape
+    r = W1.shape[1]
+    d = H.shape[2]
+    dev = U.device
+    if H.dtype != torch.bfloat16:
+        raise TypeError("H must be bfloat16")
+    if out is None:
+        out = dict(tokens=torch.empty((R, gamma), dtype=torch.int32, device=dev),
+                   q_tok=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   lse=torch.empty((R, gamma), dtype=torch.float64, device=dev),
+                   code=torch.empty((R, gamma, r), dtype=torch.float32, device=dev),
+                   state=torch.empty((R, r), dtype=torch.float32, device=dev))
+    nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, d)
+    if ws is None:
+        ws = _workspace(nbytes, dev)
+    code = L.dspark_draft_rnn(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _p(Wgco), _dt(W1), _p(H), d,
+                              R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
+                              _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
+                              _p(out.get("state")), _p(ws), ws.numel(), _stream(stream))
+    _check("dspark_draft_rnn", code)
+    out["ws"] = ws
+    return out
+
+
+def verify(P, U, W2, draft, temperature: float, seed: int, verify_len=None, req_ids=None, ws=None, out=None,
+           stream=None):
+    """Rejection-sampling verification (``dspark_verify``); ``draft`` is a draft output dict."""
+    L = load()
+    R, G1, V = P.shape
+    gamma = G1 - 1
+    r = W2.shape[0]
+    dev = P.device
+    if out is None:
+        out = dict(out_tokens=torch.empty((R, G1), dtype=torch.int32, device=dev),
+                   accept_len=torch.empty((R,), dtype=torch.int32, device=dev),
+                   n_out=torch.empty((R,), dtype=torch.int32, device=dev),
+                   p_tok=torch.empty((R, gamma), dtype=torch.float32, device=dev),
+                   lse_p=torch.empty((R, G1), dtype=torch.float64, device=dev))
+    nbytes = L.dspark_verify_workspace_size(R, gamma, V, r)
+    if ws is None:
+        ws = _workspace(nbytes, dev)
+    code = L.dspark_verify(_p(P), _dt(P), _p(U), _dt(U), _p(W2), _dt(W2), _p(draft["tokens"]),
+                           _p(draft["q_tok"]), _p(draft["lse"]), _p(draft["code"]), _p(verify_len),
+                           R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
+                           _p(out["out_tokens"]), _p(out["accept_len"]), _p(out["n_out"]),
+                           _p(out.get("p_tok")), _p(out.get("lse_p")), _p(ws), ws.numel(), _stream(stream))
+    _check("dspark_verify", code)
+    out["ws"] = ws
+    return out
+
+
+def schedule(c, sps, ws=None, out=None, stream=None):
+    """Confidence scheduler (``dspark_schedule``): verify lengths, Theta*, n*."""
+    L = load()
+    R, gamma = c.shape
+    dev = c.device
+    if out is None:
+        out = dict(verify_len=torch.empty((R,), dtype=torch.int32, device=dev),
+                   theta=torch.empty((1,), dtype=torch.float64, device=dev),
+                   n_star=torch.empty((1,), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = _workspace(L.dspark_schedule_workspace_size(R, gamma), dev)
+    code = L.dspark_schedule(_p(c), _p(sps), sps.numel(), R, gamma, _p(out["verify_len"]), _p(out["theta"]),
+                             _p(out["n_star"]), _p(ws), ws.numel(), _stream(stream))
+    _check("dspark_schedule", code)
+    out["ws"] = ws
+    return out
+
+
+def profile_enable(on: bool = True) -> None:
+    """Bracket every library launch with CUDA events (benchmark timing)."""
+    load().dspark_profile_enable(1 if on else 0)
+
+
+def profile_collect(cap: int = 1 << 16):
+    """Per launch since the last collect: list of (kernel name, milliseconds)."""
+    import numpy as np
+    L = load()
+    ids = np.zeros(cap, np.int32)
+    ms = np.zeros(cap, np.float32)
+    n = L.dspark_profile_collect(ctypes.c_void_p(ids.ctypes.data), ctypes.c_void_p(ms.ctypes.data), cap)
+    if n < 0:
+        raise DsparkError("dspark_profile_collect", n)
+    n = min(n, cap)
+    return [(L.dspark_profile_kernel_name(int(i)).decode(), float(t)) for i, t in zip(ids[:n], ms[:n])]

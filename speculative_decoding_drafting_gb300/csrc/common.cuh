@@ -1,0 +1,168 @@
+// common.cuh -- device helpers shared by the DSpark kernels.
+//
+// Counter-based RNG: Philox4x32-10 as published by Salmon, Moraes, Dror and
+// Shaw ("Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): two 32x32->64
+// multiplies per round, the high halves xored into the other two lanes with
+// the round key, the key bumped by the Weyl constants between rounds.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status bits kept in the first word of every workspace.
+enum : uint32_t { kStatBadToken = 1u, kStatTimeout = 2u };
+
+struct WsHeader {
+    uint32_t status;
+    uint32_t pad[63];   // keep what follows 256-byte aligned
+};
+
+__device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
+    atomicOr(reinterpret_cast<uint32_t*>(ws), bits);
+}
+
+// ---------------------------------------------------------------- Philox
+struct PhiloxKey {
+    uint32_t k0, k1;
+};
+
+__host__ __device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
+    return PhiloxKey{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+    uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint32_t lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// u = ((w >> 9) + 1/2) 2^-23, exact in float.
+__device__ __forceinline__ float word_to_uniform(uint32_t w) {
+    return __uint_as_float(0x3F800000u | (w >> 9)) - 0.99999994039535522f;
+}
+// t = 1 - u for the same word, also exact: the complemented top 23 bits.
+__device__ __forceinline__ float word_to_one_minus_uniform(uint32_t w) {
+    return __uint_as_float(0x3F800000u | ((~w) >> 9)) - 0.99999994039535522f;
+}
+__device__ __forceinline__ double word_to_uniform_d(uint32_t w) {
+    return (static_cast<double>(w >> 9) + 0.5) * (1.0 / 8388608.0);
+}
+
+__device__ __forceinline__ uint32_t pick_word(uint4 w, uint32_t i) {
+    return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+}
+
+// One uniform (double) for index v of (req, pos, stream).
+__device__ __forceinline__ double rng_uniform_d(PhiloxKey key, uint32_t req, uint32_t pos, uint32_t stream,
+                                                uint32_t v) {
+    uint4 w = philox4x32_10(make_uint4(v >> 2, req, pos, stream), key);
+    return word_to_uniform_d(pick_word(w, v & 3u));
+}
+
+// ---------------------------------------------------------------- math
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Exponential race key: for t = 1 - u (exact), E = -ln u = -log1p(-t) and the
+// Gumbel-max key of logit z is z - ln E  (= z + G with G = -ln(-ln u)).
+__device__ __forceinline__ float race_key(float z, float t) {
+    const float E = -log1pf(-t);
+    return z - logf(E);
+}
+
+// ---------------------------------------------------------------- loads
+template <int DT>
+struct Elem;
+template <>
+struct Elem<DSPARK_F32> {
+    using T = float;
+    static __device__ __forceinline__ float get(const float* p, size_t i) { return p[i]; }
+};
+template <>
+struct Elem<DSPARK_BF16> {
+    using T = __nv_bfloat16;
+    static __device__ __forceinline__ float get(const __nv_bfloat16* p, size_t i) {
+        return __bfloat162float(p[i]);
+    }
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// 4 consecutive elements starting at a multiple of 4 (16 B f32 / 8 B bf16).
+template <int DT>
+__device__ __forceinline__ float4 load4(const void* base, size_t i);
+template <>
+__device__ __forceinline__ float4 load4<DSPARK_F32>(const void* base, size_t i) {
+    return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+}
+template <>
+__device__ __forceinline__ float4 load4<DSPARK_BF16>(const void* base, size_t i) {
+    uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + i));
+    return make_float4(bf16_bits_to_float(v.x & 0xFFFFu), bf16_bits_to_float(v.x >> 16),
+                       bf16_bits_to_float(v.y & 0xFFFFu), bf16_bits_to_float(v.y >> 16));
+}
+// Streaming variant (read once): evict-first in L2, no L1 allocation.
+template <int DT>
+__device__ __forceinline__ float4 load4_stream(const void* base, size_t i);
+template <>
+__device__ __forceinline__ float4 load4_stream<DSPARK_F32>(const void* base, size_t i) {
+    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+}
+template <>
+__device__ __forceinline__ float4 load4_stream<DSPARK_BF16>(const void* base, size_t i) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + i));
+    return make_float4(bf16_bits_to_float(v.x & 0xFFFFu), bf16_bits_to_float(v.x >> 16),
+                       bf16_bits_to_float(v.y & 0xFFFFu), bf16_bits_to_float(v.y >> 16));
+}
+
+__device__ __forceinline__ float ld_elem(const void* p, int dt, size_t i) {
+    if (dt == DSPARK_F32) return __ldg(static_cast<const float*>(p) + i);
+    return bf16_bits_to_float(__ldg(static_cast<const unsigned short*>(p) + i));
+}
+
+// ---------------------------------------------------------------- warp ops
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__host__ __device__ __forceinline__ int ceil_log2_i(int V) {
+    int L = 0;
+    while ((1 << L) < V) ++L;
+    return L;
+}
+
+__host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace dspark

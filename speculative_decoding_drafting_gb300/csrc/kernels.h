@@ -1,0 +1,97 @@
+// kernels.h -- internal launch interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+
+// Per-(request, step, V-slice) partial state of the draft's reduction over V:
+// running max and sum for the log-sum-exp, and the best race key so far.
+struct DraftPartial {
+    float m;       // max of z over the slice (-inf if empty)
+    float kb;      // best key (z - ln E, or the logit itself at T = 0)
+    float zb;      // z of the best element
+    int ib;        // its vocabulary index (INT_MAX if empty)
+    double s;      // sum of exp(z - m) over the slice
+};
+
+struct DraftArgs {
+    const void* U;
+    int u_dtype;
+    const int32_t* anchor;
+    const void* W1;
+    const void* W2;
+    const void* Wgco;   // RNN only
+    const void* H;      // RNN only (bf16)
+    int w_dtype;
+    int R, gamma, V, r, d;
+    uint64_t seed;
+    const uint32_t* req_ids;
+    float T;
+    int32_t* tokens;
+    float* q_tok;
+    double* lse;
+    float* code;
+    float* state_out;
+    // workspace carve-up
+    void* ws;
+    DraftPartial* parts;      // [2][R][n_slices]
+    uint16_t* ebf;            // [2][R][r] bf16 bits (hi, lo) of e_k
+    float* rnn_state;         // [R][r]
+    int n_slices;             // V-slices per request in the active sweep
+    int parts_stride;         // R * n_slices_max
+};
+
+struct VerifyArgs {
+    const void* P;
+    int p_dtype;
+    const void* U;
+    int u_dtype;
+    const void* W2;
+    int w_dtype;
+    const int32_t* tokens;
+    const float* q_tok;
+    const double* lse;
+    const float* code;
+    const int32_t* verify_len;
+    int R, gamma, V, r;
+    uint64_t seed;
+    const uint32_t* req_ids;
+    float T;
+    int32_t* out_tokens;
+    int32_t* accept_len;
+    int32_t* n_out;
+    float* p_tok;
+    double* lse_p;
+    // workspace
+    void* ws;
+    float2* vparts;     // [R][gamma+1][NCH]  (m, s) or (max, idx bits)
+    double* lsep_ws;    // [R][gamma+1]
+    int2* vstate;       // [R] (mode, position)
+    double* rmass;      // [R][NCH]
+    int nch;            // number of 1024-wide chunks of V
+};
+
+constexpr int kChunk = 1024;          // leaf chunk of the sampling tree
+constexpr int kChunkLog2 = 10;
+constexpr int kGenericSlice = 4096;   // V-slice of the generic draft sweep
+
+enum VerifyMode : int { kModeDone = 0, kModeResidual = 1, kModeBonus = 2 };
+
+size_t draft_workspace_bytes(int R, int gamma, int V, int r, int d);
+int draft_carve(DraftArgs& a, size_t ws_bytes);
+cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s);
+
+size_t verify_workspace_bytes(int R, int gamma, int V, int r);
+int verify_carve(VerifyArgs& a, size_t ws_bytes);
+cudaError_t launch_verify(VerifyArgs& a, cudaStream_t s);
+
+size_t schedule_smem_bytes(int R, int gamma);
+cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,
+                            double* theta, int32_t* nstar, void* ws, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace dspark

@@ -1,0 +1,164 @@
+// schedule.cu -- the confidence-driven greedy early-stop verify-length scheduler.
+//
+// Blog section 4.3 and DSpark explainer section 04: with calibrated
+// confidences c, the prefix survival of request r at depth j is
+// a_{r,j} = c_{r,1} ... c_{r,j}; sending l_r drafts of request r to the target
+// costs B = sum_r (1 + l_r) tokens and is expected to yield
+// tau = sum_r (1 + sum_{j <= l_r} a_{r,j}) tokens, so the batch objective is
+// Theta = tau * SPS(B).  Extending prefixes in decreasing order of a and
+// stopping at the first non-improving Theta is the page's synchronous
+// algorithm.  Its inputs are c and SPS only: it never sees the target's
+// logits nor any random number (the explainer's causal no-peek condition).
+//
+// One CTA of 1024 threads does the whole batch in shared memory:
+//   1. a = running float32 product of c along each request
+//   2. 64-bit keys (~bits(a) << 32 | r * gamma + j) bitonic-sorted ascending,
+//      i.e. a descending, then r, then j ascending; a <= 0 sorts last
+//   3. tau_n = R + inclusive scan of the sorted a (double)
+//   4. Theta(n) = tau_n * SPS[R + n]; n* = first n with Theta(n+1) <= Theta(n)
+//   5. l_r = number of the first n* candidates that belong to r
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "profile.h"
+
+namespace dspark {
+
+constexpr int kSchedThreads = 1024;
+
+__device__ __forceinline__ double sps_at(const double* sps, int n_sps, long long B) {
+    return (B >= 0 && B < n_sps) ? sps[B] : 0.0;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c, const double* sps, int n_sps,
+                                                                 int R, int gamma, int Np, int32_t* len,
+                                                                 double* theta, int32_t* nstar) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
+    double* val = reinterpret_cast<double*>(smem + (size_t)Np * 8);
+    int* cnt = reinterpret_cast<int*>(smem + (size_t)Np * 16);
+    __shared__ double wsum[kSchedThreads / 32];
+    __shared__ int s_nvalid, s_nstar;
+    const int tid = threadIdx.x;
+    const int N = R * gamma;
+
+    // 1-2: products and keys
+    for (int r = tid; r < R; r += blockDim.x) {
+        float prod = 1.0f;
+        for (int j = 0; j < gamma; ++j) {
+            prod = __fmul_rn(prod, c[(size_t)r * gamma + j]);
+            const int idx = r * gamma + j;
+            keys[idx] = (prod > 0.0f) ? (((unsigned long long)(~__float_as_uint(prod)) << 32) | (unsigned)idx)
+                                      : ~0ull;
+        }
+        cnt[r] = 0;
+    }
+    for (int i = N + tid; i < Np; i += blockDim.x) keys[i] = ~0ull;
+    if (tid == 0) s_nvalid = 0;
+    __syncthreads();
+    for (int size = 2; size <= Np; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < Np / 2; i += blockDim.x) {
+                const int lo = (i / stride) * stride * 2 + (i % stride);
+                const int hi = lo + stride;
+                const bool up = ((lo & size) == 0);
+                const unsigned long long a = keys[lo], b = keys[hi];
+                if ((a > b) == up) {
+                    keys[lo] = b;
+                    keys[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // 3: scan of the sorted a (double), sequential within a thread's run
+    const int per = (Np + blockDim.x - 1) / blockDim.x;
+    const int b0 = tid * per;
+    double run = 0.0;
+    int nv = 0;
+    for (int i = b0; i < b0 + per && i < Np; ++i) {
+        const unsigned long long k = keys[i];
+        double a = 0.0;
+        if (k != ~0ull) {
+            a = (double)__uint_as_float(~(unsigned)(k >> 32));
+            ++nv;
+        }
+        run += a;
+        val[i] = run;
+    }
+    atomicAdd(&s_nvalid, nv);
+    // block exclusive scan of the per-thread totals
+    const int lane = tid & 31, warp = tid >> 5;
+    double x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        double w = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;     // inclusive over warps
+    }
+    __syncthreads();
+    const double offset = (x - run) + (warp > 0 ? wsum[warp - 1] : 0.0);
+    for (int i = b0; i < b0 + per && i < Np; ++i) val[i] += offset;
+    if (tid == 0) s_nstar = INT_MAX;
+    __syncthreads();
+    const int nvalid = s_nvalid;
+    // 4: first non-improvement.  Theta(n) = (R + S_{n-1}) * SPS[R + n]
+    for (int n = tid; n < nvalid; n += blockDim.x) {
+        const double tn = (double)R + (n > 0 ? val[n - 1] : 0.0);
+        const double tn1 = (double)R + val[n];
+        const double th_n = tn * sps_at(sps, n_sps, (long long)R + n);
+        const double th_n1 = tn1 * sps_at(sps, n_sps, (long long)R + n + 1);
+        if (!(th_n1 > th_n)) atomicMin(&s_nstar, n);
+    }
+    __syncthreads();
+    const int ns = s_nstar == INT_MAX ? nvalid : s_nstar;
+    // 5: lengths
+    for (int i = tid; i < ns; i += blockDim.x) {
+        const int idx = (int)(unsigned)(keys[i] & 0xFFFFFFFFull);
+        atomicAdd(&cnt[idx / gamma], 1);
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += blockDim.x) len[r] = cnt[r];
+    if (tid == 0) {
+        *nstar = ns;
+        const double tn = (double)R + (ns > 0 ? val[ns - 1] : 0.0);
+        *theta = tn * sps_at(sps, n_sps, (long long)R + ns);
+    }
+}
+
+static int next_pow2(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+size_t schedule_smem_bytes(int R, int gamma) {
+    const int Np = next_pow2(R * gamma < 2 ? 2 : R * gamma);
+    return (size_t)Np * 16 + (size_t)R * sizeof(int);
+}
+
+cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,
+                            double* theta, int32_t* nstar, void* ws, cudaStream_t s) {
+    (void)ws;
+    const int Np = next_pow2(R * gamma < 2 ? 2 : R * gamma);
+    const size_t smem = schedule_smem_bytes(R, gamma);
+    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_begin(kPSchedule, s);
+    schedule_kernel<<<1, kSchedThreads, smem, s>>>(c, sps, n_sps, R, gamma, Np, len, theta, nstar);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

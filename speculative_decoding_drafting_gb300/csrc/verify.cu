@@ -1,0 +1,478 @@
+// verify.cu -- lossless rejection-sampling verification.
+//
+// DSpark explainer, section 05: with p the target distribution and q the
+// draft distribution actually used (including the sequential head's bias),
+// x ~ q is accepted with alpha(x) = min(1, p(x)/q(x)); on rejection the new
+// token comes from r(v) = max(p(v) - q(v), 0) / sum_u max(p(u) - q(u), 0).
+// Blog section 1 and explainer section 02: everything after the first
+// rejection is discarded, and a fully accepted block earns one bonus token
+// from the target; the greedy teaching version (T = 0) accepts on exact match
+// and replaces the first mismatch by the target's argmax.
+//
+// Kernels (one stream):
+//   pass1     stream every target row the request verifies (rows 0..l_r)
+//             once, 1024-wide chunks: (max, sum exp) of P/T, or (max, argmax)
+//   accept    one warp per request: lse of each row, p(x_k), the acceptance
+//             scan with stream-1 uniforms; decides residual / bonus / done
+//   residual  rejecting requests only: w = max(p_j - q_j, 0) over the row,
+//             q_j rebuilt from U_j, code_j W2 and lse_j; per-chunk mass
+//   sample    one CTA per request that still needs a token: descend the
+//             binary sum tree (chunk masses above, exact element weights in
+//             double inside the chosen chunk), one stream-2 uniform a level
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "profile.h"
+
+namespace dspark {
+
+bool verify_tc_supported(const VerifyArgs& a);
+cudaError_t launch_verify_tc_residual(VerifyArgs& a, cudaStream_t s);
+
+__device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
+    if (!A.verify_len) return A.gamma;
+    int L = A.verify_len[r];
+    return L < 0 ? 0 : (L > A.gamma ? A.gamma : L);
+}
+
+// ------------------------------------------------------------------ pass 1
+template <int PT, bool GREEDY>
+__global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
+    const int lane = threadIdx.x & 31;
+    const int warps_total = gridDim.x * (blockDim.x >> 5);
+    const int V = A.V, G1 = A.gamma + 1, NCH = A.nch;
+    const long long tasks = (long long)A.R * G1 * NCH;
+    const float invT = GREEDY ? 1.f : 1.f / A.T;
+    for (long long task = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks;
+         task += warps_total) {
+        const int ch = (int)(task % NCH);
+        const long long rr = task / NCH;
+        const int row = (int)(rr % G1);
+        const int r = (int)(rr / G1);
+        if (row > verify_len_of(A, r)) continue;            // warp-uniform
+        const size_t base = ((size_t)r * G1 + row) * (size_t)V;
+        const int c0 = ch * kChunk;
+        float x[32];
+        bool ok[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = c0 + 4 * lane + 128 * i;
+            ok[i] = c < V;
+            float4 v = ok[i] ? load4_stream<PT>(A.P, base + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[4 * i + 0] = v.x;
+            x[4 * i + 1] = v.y;
+            x[4 * i + 2] = v.z;
+            x[4 * i + 3] = v.w;
+        }
+        float2 out;
+        if (GREEDY) {
+            float best = -INFINITY;
+            int arg = INT_MAX;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = c0 + 4 * lane + 128 * i + q;
+                    const float y = x[4 * i + q];
+                    if (ok[i] && (y > best || (y == best && c < arg))) {
+                        best = y;
+                        arg = c;
+                    }
+                }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+                const int a2 = __shfl_xor_sync(0xffffffffu, arg, o);
+                if (b2 > best || (b2 == best && a2 < arg)) {
+                    best = b2;
+                    arg = a2;
+                }
+            }
+            out = make_float2(best, __int_as_float(arg));
+        } else {
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (ok[i]) m = fmaxf(m, x[4 * i + q] * invT);
+            const float mw = warp_max(m);
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (ok[i]) s += ex2_approx((x[4 * i + q] * invT - mw) * kLog2e);
+            s = warp_sum(s);
+            out = make_float2(mw, s);
+        }
+        if (lane == 0) A.vparts[rr * NCH + ch] = out;
+    }
+}
+
+// ------------------------------------------------------------------ accept
+template <int PT, bool GREEDY>
+__global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= A.R) return;
+    const int G1 = A.gamma + 1, NCH = A.nch, V = A.V;
+    const int L = verify_len_of(A, r);
+    const float invT = GREEDY ? 1.f : 1.f / A.T;
+    int32_t* out = A.out_tokens + (size_t)r * G1;
+    for (int i = lane; i < G1; i += 32) {
+        out[i] = -1;
+        if (A.lse_p) A.lse_p[(size_t)r * G1 + i] = NAN;
+        if (A.p_tok && i < A.gamma) A.p_tok[(size_t)r * A.gamma + i] = NAN;
+    }
+    __syncwarp();
+    const float2* parts = A.vparts + (size_t)r * G1 * NCH;
+    if (GREEDY) {
+        int j = 0;
+        for (int k = 1; k <= L + 1; ++k) {
+            const int row = k - 1;
+            float best = -INFINITY;
+            int arg = INT_MAX;
+            for (int c = lane; c < NCH; c += 32) {
+                const float2 p = parts[(size_t)row * NCH + c];
+                const int a2 = __float_as_int(p.y);
+                if (p.x > best || (p.x == best && a2 < arg)) {
+                    best = p.x;
+                    arg = a2;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+                const int a2 = __shfl_xor_sync(0xffffffffu, arg, o);
+                if (b2 > best || (b2 == best && a2 < arg)) {
+                    best = b2;
+                    arg = a2;
+                }
+            }
+            if (arg < 0 || arg >= V) arg = 0;
+            if (k == L + 1) {               // bonus: all L drafts matched
+                if (lane == 0) out[L] = arg;
+                break;
+            }
+            int x = A.tokens[(size_t)r * A.gamma + row];
+            if (lane == 0) out[row] = arg;  // equals x when accepted
+            if (x != arg) {
+                j = k;
+                break;
+            }
+        }
+        if (lane == 0) {
+            const int acc = j ? j - 1 : L;
+            A.accept_len[r] = acc;
+            A.n_out[r] = acc + 1;
+            A.vstate[r] = make_int2(kModeDone, 0);
+        }
+        return;
+    }
+    // T > 0: log-sum-exp of every row the request reads.
+    double* lsep = A.lsep_ws + (size_t)r * G1;
+    for (int row = 0; row <= L; ++row) {
+        float m = -INFINITY;
+        for (int c = lane; c < NCH; c += 32) m = fmaxf(m, parts[(size_t)row * NCH + c].x);
+        m = warp_max(m);
+        double s = 0.0;
+        for (int c = lane; c < NCH; c += 32) {
+            const float2 p = parts[(size_t)row * NCH + c];
+            s += (double)p.y * exp((double)p.x - (double)m);
+        }
+        s = warp_sum_d(s);
+        const double l = (double)m + log(s);
+        if (lane == 0) {
+            lsep[row] = l;
+            if (A.lse_p) A.lse_p[(size_t)r * G1 + row] = l;
+        }
+    }
+    __syncwarp();
+    if (lane != 0) return;
+    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+    const PhiloxKey key = philox_key(A.seed);
+    int j = 0;
+    for (int k = 1; k <= L; ++k) {
+        int x = A.tokens[(size_t)r * A.gamma + (k - 1)];
+        if (x < 0 || x >= V) {
+            raise_status(A.ws, kStatBadToken);
+            x = 0;
+        }
+        const size_t prow = ((size_t)r * G1 + (k - 1)) * (size_t)V;
+        const double px = exp((double)ld_elem(A.P, PT, prow + x) * (double)invT - lsep[k - 1]);
+        if (A.p_tok) A.p_tok[(size_t)r * A.gamma + (k - 1)] = (float)px;
+        const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + (k - 1)];
+        const double u = rng_uniform_d(key, req, (uint32_t)k, 1u, 0u);
+        if (u < ratio) {
+            out[k - 1] = x;
+        } else {
+            j = k;
+            break;
+        }
+    }
+    if (j) {
+        A.vstate[r] = make_int2(kModeResidual, j);
+        A.accept_len[r] = j - 1;
+    } else {
+        A.vstate[r] = make_int2(kModeBonus, L + 1);
+        A.accept_len[r] = L;
+    }
+    A.n_out[r] = A.accept_len[r] + 1;
+}
+
+// ------------------------------------------------------------------ residual (generic)
+// One CTA per (chunk, request); q_j rebuilt with B = e_j W2 on CUDA cores.
+template <int PT, int UT, int WT>
+__global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
+    extern __shared__ float e_sh[];
+    const int ch = blockIdx.x, r = blockIdx.y;
+    const int2 st = A.vstate[r];
+    if (st.x != kModeResidual) return;
+    const int j = st.y, V = A.V, G1 = A.gamma + 1;
+    for (int i = threadIdx.x; i < A.r; i += blockDim.x)
+        e_sh[i] = A.code[((size_t)r * A.gamma + (j - 1)) * A.r + i];
+    __syncthreads();
+    const int c = ch * kChunk + 4 * threadIdx.x;
+    double wsum = 0.0;
+    if (c < V) {
+        float b[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < A.r; ++i) {
+            const float4 w = load4<WT>(A.W2, (size_t)i * V + c);
+            const float ei = e_sh[i];
+            b[0] = fmaf(ei, w.x, b[0]);
+            b[1] = fmaf(ei, w.y, b[1]);
+            b[2] = fmaf(ei, w.z, b[2]);
+            b[3] = fmaf(ei, w.w, b[3]);
+        }
+        const float invT = 1.f / A.T;
+        const double lq = A.lse[(size_t)r * A.gamma + (j - 1)];
+        const double lp = A.lsep_ws[(size_t)r * G1 + (j - 1)];
+        const float lq_hi = (float)lq, lq_lo = (float)(lq - (double)lq_hi);
+        const float lp_hi = (float)lp, lp_lo = (float)(lp - (double)lp_hi);
+        const float4 u4 = load4<UT>(A.U, ((size_t)r * A.gamma + (j - 1)) * V + c);
+        const float4 p4 = load4<PT>(A.P, ((size_t)r * G1 + (j - 1)) * V + c);
+        const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+        const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float qv = expf(((uu[q] + b[q]) * invT - lq_hi) - lq_lo);
+            const float pv = expf((pp[q] * invT - lp_hi) - lp_lo);
+            const float w = pv - qv;
+            wsum += w > 0.f ? (double)w : 0.0;
+        }
+    }
+    wsum = warp_sum_d(wsum);
+    __shared__ double sh[8];
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = wsum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int i = 0; i < 8; ++i) t += sh[i];
+        A.rmass[(size_t)r * A.nch + ch] = t;
+    }
+}
+
+// ------------------------------------------------------------------ sample
+// Weights of the draw, in double, for one element (used inside the chosen chunk).
+template <int PT, int UT, int WT>
+__device__ double leaf_weight(const VerifyArgs& A, int r, int mode, int pos, bool use_p, int v,
+                              const float* e_sh) {
+    const int V = A.V, G1 = A.gamma + 1;
+    const double invT = 1.0 / (double)A.T;
+    const double lp = A.lsep_ws[(size_t)r * G1 + (pos - 1)];
+    const double pv = exp((double)ld_elem(A.P, PT, ((size_t)r * G1 + (pos - 1)) * V + v) * invT - lp);
+    if (mode == kModeBonus || use_p) return pv;
+    float b = 0.f;
+    for (int i = 0; i < A.r; ++i) b = fmaf(e_sh[i], ld_elem(A.W2, WT, (size_t)i * V + v), b);
+    const double lq = A.lse[(size_t)r * A.gamma + (pos - 1)];
+    const double z = ((double)ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + v) + (double)b) * invT;
+    const double qv = exp(z - lq);
+    const double w = pv - qv;
+    return w > 0.0 ? w : 0.0;
+}
+
+template <int PT, int UT, int WT>
+__global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
+    __shared__ double cm[1024];        // chunk masses (top of the tree), then leaf weights
+    __shared__ float e_sh[1024];
+    __shared__ int s_chunk;
+    __shared__ int s_use_p;
+    const int r = blockIdx.x;
+    const int2 st = A.vstate[r];
+    if (st.x == kModeDone) return;
+    const int mode = st.x, pos = st.y;
+    const int V = A.V, NCH = A.nch, G1 = A.gamma + 1;
+    const int L = ceil_log2_i(V);
+    const int Ltop = L > kChunkLog2 ? L - kChunkLog2 : 0;
+    const int nleaf_top = 1 << Ltop;     // >= NCH
+    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+    const PhiloxKey key = philox_key(A.seed);
+    if (mode == kModeResidual)
+        for (int i = threadIdx.x; i < A.r; i += blockDim.x)
+            e_sh[i] = A.code[((size_t)r * A.gamma + (pos - 1)) * A.r + i];
+    // chunk masses
+    double tot = 0.0;
+    for (int c = threadIdx.x; c < nleaf_top; c += blockDim.x) {
+        double m = 0.0;
+        if (c < NCH) {
+            if (mode == kModeResidual) {
+                m = A.rmass[(size_t)r * NCH + c];
+            } else {
+                const float2 p = A.vparts[((size_t)r * G1 + (pos - 1)) * NCH + c];
+                m = (double)p.y * exp((double)p.x - A.lsep_ws[(size_t)r * G1 + (pos - 1)]);
+            }
+        }
+        cm[c] = m;
+        tot += m;
+    }
+    tot = warp_sum_d(tot);
+    __shared__ double sh[8];
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = tot;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int i = 0; i < 8; ++i) t += sh[i];
+        s_use_p = (mode == kModeResidual && !(t > 0.0)) ? 1 : 0;
+    }
+    __syncthreads();
+    const bool use_p = s_use_p != 0;
+    if (use_p) {   // empty residual (rounding only): draw from p_j
+        for (int c = threadIdx.x; c < nleaf_top; c += blockDim.x) {
+            double m = 0.0;
+            if (c < NCH) {
+                const float2 p = A.vparts[((size_t)r * G1 + (pos - 1)) * NCH + c];
+                m = (double)p.y * exp((double)p.x - A.lsep_ws[(size_t)r * G1 + (pos - 1)]);
+            }
+            cm[c] = m;
+        }
+        __syncthreads();
+    }
+    // top levels over chunk masses
+    if (threadIdx.x == 0) {
+        int lo = 0;
+        for (int d = 0; d < Ltop; ++d) {
+            const int half = 1 << (Ltop - d - 1);
+            double mL = 0.0, mR = 0.0;
+            for (int c = lo; c < lo + half; ++c) mL += cm[c];
+            for (int c = lo + half; c < lo + 2 * half; ++c) mR += cm[c];
+            const double u = rng_uniform_d(key, req, (uint32_t)pos, 2u, (uint32_t)d);
+            if (!(u * (mL + mR) < mL)) lo += half;
+        }
+        s_chunk = lo;
+    }
+    __syncthreads();
+    const int chunk = s_chunk;
+    // exact leaf weights of the chosen chunk
+    const int Lbot = L - Ltop;             // levels inside the chunk
+    const int nleaf = 1 << Lbot;           // <= 1024
+    for (int i = threadIdx.x; i < nleaf; i += blockDim.x) {
+        const int v = chunk * kChunk + i;
+        double w = 0.0;
+        if (v < V) w = leaf_weight<PT, UT, WT>(A, r, mode, pos, use_p, v, e_sh);
+        cm[i] = w;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int lo = 0;
+        for (int d = 0; d < Lbot; ++d) {
+            const int half = 1 << (Lbot - d - 1);
+            double mL = 0.0, mR = 0.0;
+            for (int i = lo; i < lo + half; ++i) mL += cm[i];
+            for (int i = lo + half; i < lo + 2 * half; ++i) mR += cm[i];
+            const double u = rng_uniform_d(key, req, (uint32_t)pos, 2u, (uint32_t)(Ltop + d));
+            if (!(u * (mL + mR) < mL)) lo += half;
+        }
+        int y = chunk * kChunk + lo;
+        if (y >= V) y = V - 1;
+        A.out_tokens[(size_t)r * G1 + (pos - 1)] = y;
+    }
+}
+
+// ------------------------------------------------------------------ host
+static int nch_of(int V) { return (V + kChunk - 1) / kChunk; }
+
+size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
+    (void)r;
+    const int G1 = gamma + 1, NCH = nch_of(V);
+    size_t off = sizeof(WsHeader);
+    off = align_up(off + (size_t)R * G1 * NCH * sizeof(float2), 256);
+    off = align_up(off + (size_t)R * G1 * sizeof(double), 256);
+    off = align_up(off + (size_t)R * sizeof(int2), 256);
+    off = align_up(off + (size_t)R * NCH * sizeof(double), 256);
+    return off;
+}
+
+int verify_carve(VerifyArgs& a, size_t ws_bytes) {
+    if (ws_bytes < verify_workspace_bytes(a.R, a.gamma, a.V, a.r)) return DSPARK_ERR_WORKSPACE;
+    const int G1 = a.gamma + 1, NCH = nch_of(a.V);
+    a.nch = NCH;
+    char* base = static_cast<char*>(a.ws);
+    size_t off = sizeof(WsHeader);
+    a.vparts = reinterpret_cast<float2*>(base + off);
+    off = align_up(off + (size_t)a.R * G1 * NCH * sizeof(float2), 256);
+    a.lsep_ws = reinterpret_cast<double*>(base + off);
+    off = align_up(off + (size_t)a.R * G1 * sizeof(double), 256);
+    a.vstate = reinterpret_cast<int2*>(base + off);
+    off = align_up(off + (size_t)a.R * sizeof(int2), 256);
+    a.rmass = reinterpret_cast<double*>(base + off);
+    return DSPARK_OK;
+}
+
+template <int PT, int UT, int WT>
+static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
+    const bool greedy = !(a.T > 0.f);
+    const int nsm = num_sms();
+    const long long tasks = (long long)a.R * (a.gamma + 1) * a.nch;
+    long long want = (tasks + 7) / 8;
+    int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
+    if (grid < 1) grid = 1;
+    if (greedy) {
+        prof_begin(kPVerifyPass1, s);
+        verify_pass1<PT, true><<<grid, 256, 0, s>>>(a);
+        prof_end(s);
+        prof_begin(kPVerifyAccept, s);
+        verify_accept<PT, true><<<(a.R + 7) / 8, 256, 0, s>>>(a);
+        prof_end(s);
+        return cudaGetLastError();
+    }
+    prof_begin(kPVerifyPass1, s);
+    verify_pass1<PT, false><<<grid, 256, 0, s>>>(a);
+    prof_end(s);
+    prof_begin(kPVerifyAccept, s);
+    verify_accept<PT, false><<<(a.R + 7) / 8, 256, 0, s>>>(a);
+    prof_end(s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (verify_tc_supported(a)) {
+        e = launch_verify_tc_residual(a, s);
+    } else {
+        dim3 g2(a.nch, a.R);
+        prof_begin(kPVerifyResidualGeneric, s);
+        verify_residual_generic<PT, UT, WT><<<g2, 256, a.r * sizeof(float), s>>>(a);
+        prof_end(s);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+    prof_begin(kPVerifySample, s);
+    verify_sample<PT, UT, WT><<<a.R, 256, 0, s>>>(a);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify(VerifyArgs& a, cudaStream_t s) {
+    const int key = a.p_dtype * 4 + a.u_dtype * 2 + a.w_dtype;
+    switch (key) {
+        case 0: return launch_typed<DSPARK_F32, DSPARK_F32, DSPARK_F32>(a, s);
+        case 1: return launch_typed<DSPARK_F32, DSPARK_F32, DSPARK_BF16>(a, s);
+        case 2: return launch_typed<DSPARK_F32, DSPARK_BF16, DSPARK_F32>(a, s);
+        case 3: return launch_typed<DSPARK_F32, DSPARK_BF16, DSPARK_BF16>(a, s);
+        case 4: return launch_typed<DSPARK_BF16, DSPARK_F32, DSPARK_F32>(a, s);
+        case 5: return launch_typed<DSPARK_BF16, DSPARK_F32, DSPARK_BF16>(a, s);
+        case 6: return launch_typed<DSPARK_BF16, DSPARK_BF16, DSPARK_F32>(a, s);
+        default: return launch_typed<DSPARK_BF16, DSPARK_BF16, DSPARK_BF16>(a, s);
+    }
+}
+
+}  // namespace dspark

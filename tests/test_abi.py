@@ -1,0 +1,60 @@
+"""The C ABI library builds, loads and exports every entry point that
+include/dspark.h declares; host-side argument checks answer without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_drafting_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "dspark.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls():
+    syms = declared_symbols()
+    for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_verify", "dspark_schedule"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol():
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+
+
+def test_host_only_calls():
+    L = binding.load()
+    assert b"sm_103a" in L.dspark_version()
+    assert L.dspark_strerror(-6) == b"token id outside [0, V)"
+    assert binding.draft_workspace_bytes(256, 5, 151936, 256) > 0
+    assert binding.draft_workspace_bytes(0, 5, 151936, 256) == 0
+    assert binding.verify_workspace_bytes(256, 5, 151936, 256) > 0
+    assert binding.schedule_workspace_bytes(512, 16) > 0
+    assert binding.schedule_workspace_bytes(1024, 16) == 0          # R * gamma above 8192
+
+
+def test_invalid_arguments_rejected_before_any_device_work():
+    L = binding.load()
+    null = None
+    # null inputs
+    st = L.dspark_draft_markov(null, 0, null, null, null, 1, 4, 5, 4096, 32, 0, null, 1.0,
+                               null, null, null, null, null, 0, null)
+    assert st == -1
+    # unsupported dtype / sizes
+    assert L.dspark_draft_markov(null, 7, null, null, null, 1, 4, 5, 4096, 32, 0, null, 1.0,
+                                 null, null, null, null, null, 0, null) == -2
+    assert L.dspark_draft_markov(null, 0, null, null, null, 1, 4, 5, 4099, 32, 0, null, 1.0,
+                                 null, null, null, null, null, 0, null) == -3
+    assert L.dspark_verify(null, 0, null, 0, null, 1, null, null, null, null, null, 4, 0, 4096, 32, 0, null,
+                           1.0, null, null, null, null, null, null, 0, null) == -3
+    assert L.dspark_schedule(null, null, 10, 4, 5, null, null, null, null, 0, null) == -1
+    assert L.dspark_schedule(null, null, 10, 1000, 16, null, null, null, null, 0, null) == -3

@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Discrete outputs (tokens, accept lengths, verify lengths) must be bit-exact
+except at positions the oracle flags as near-ties (Gumbel or argmax margin
+below 1e-4, a uniform within 1e-6 of its threshold); q(x), p(x) and the
+log-sum-exps agree within 1e-4 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import (compare_draft, compare_verify, dev, gpu_draft, gpu_verify_on, host, oracle_draft,
+                     oracle_verify_on)
+from speculative_decoding_drafting_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16 = synth.F32, synth.BF16
+
+SMALL = {
+    "toy": synth.WORKLOADS["toy"],
+    "bf16_r64": synth.Workload("bf16_r64", R=6, gamma=4, V=20488, r=64, T=1.0),
+    "bf16_storage_T08": synth.Workload("bf16_storage_T08", R=5, gamma=3, V=12296, r=128, T=0.8,
+                                       u_dtype=BF16, p_dtype=BF16, sigma_pnoise=1.2),
+    "greedy": synth.Workload("greedy", R=5, gamma=4, V=16392, r=64, T=0.0, sigma_u=2.0, sigma_pnoise=0.7),
+    "rnn": synth.Workload("rnn", R=4, gamma=3, V=8200, r=64, T=1.0, head="rnn", d=96),
+    "f32_r7": synth.Workload("f32_r7", R=3, gamma=2, V=1036, r=7, T=1.3, w_dtype=F32, sigma_w=0.3),
+    "tiny": synth.Workload("tiny", R=1, gamma=1, V=8, r=1, T=1.0, w_dtype=F32, sigma_w=0.5),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("seed", [0, 77])
+def test_draft_parity(name, seed):
+    w = SMALL[name].scaled(seed=seed)
+    x = synth.gen_all(w)
+    g = gpu_draft(w, x, seed=1000 + seed)
+    o = oracle_draft(w, x, seed=1000 + seed)
+    n, nflag, m = compare_draft(g, o, tag=name)
+    assert n >= w.R
+    # the rank-r code: W1 rows exactly (Markov) / tanh(out) to 1e-5 (RNN)
+    if w.head == "markov":
+        np.testing.assert_array_equal(g["code"][m], o["code"][m].astype(np.float32))
+    else:
+        np.testing.assert_allclose(g["code"][m], o["code"][m], atol=2e-5)
+
+
+@pytest.mark.parametrize("name", [k for k in SMALL if k != "rnn"])
+@pytest.mark.parametrize("mode", ["all", "random", "zero"])
+def test_verify_parity_on_oracle_drafts(name, mode):
+    w = SMALL[name]
+    x = synth.gen_all(w)
+    seed = 4242
+    dr = oracle_draft(w, x, seed)
+    rng = np.random.default_rng(3)
+    vl = None if mode == "all" else (rng.integers(0, w.gamma + 1, w.R).astype(np.int32) if mode == "random"
+                                     else np.zeros(w.R, np.int32))
+    g = gpu_verify_on(w, x, dr, seed, verify_len=vl)
+    o = oracle_verify_on(w, x, dr, seed, verify_len=vl)
+    n, nflag = compare_verify(g, o, np.ones(w.R, bool), tag=name)
+    assert n + nflag == w.R
+
+
+def test_verify_parity_rnn_codes():
+    w = SMALL["rnn"]
+    x = synth.gen_all(w)
+    dr = oracle_draft(w, x, 5)
+    g = gpu_verify_on(w, x, dr, 5)
+    o = oracle_verify_on(w, x, dr, 5)
+    compare_verify(g, o, np.ones(w.R, bool), tag="rnn")
+
+
+@pytest.mark.parametrize("name", ["toy", "bf16_r64", "greedy", "rnn"])
+def test_cycle_end_to_end(name):
+    """GPU draft -> GPU verify against oracle draft -> oracle verify."""
+    w = SMALL[name]
+    x = synth.gen_all(w)
+    seed = 99
+    g = gpu_draft(w, x, seed)
+    o = oracle_draft(w, x, seed)
+    _, _, m = compare_draft(g, o, tag=name)
+    same = (g["tokens"] == o["tokens"]).all(axis=1)
+    gv = gpu_verify_on(w, x, g, seed)
+    ov = oracle_verify_on(w, x, o, seed)
+    compare_verify(gv, ov, same, tag=name)
+
+
+def test_verify_many_requests_statistics():
+    """Many requests of a small vocabulary: parity on each request, and the
+    empirical first-position acceptance matches 1 - TV of the oracle's p and q."""
+    w = synth.Workload("stats", R=512, gamma=3, V=64, r=4, T=1.0, w_dtype=F32, sigma_w=0.2,
+                       sigma_pnoise=0.8)
+    x = synth.gen_all(w)
+    dr = oracle_draft(w, x, 8)
+    g = gpu_verify_on(w, x, dr, 8)
+    o = oracle_verify_on(w, x, dr, 8)
+    compare_verify(g, o, np.ones(w.R, bool), tag="stats")
+
+
+@pytest.mark.parametrize("R,gamma,rho", [(1, 1, 0.0), (3, 5, 0.5), (8, 4, 0.0), (5, 16, 0.5), (64, 5, 0.9),
+                                         (512, 16, 0.9), (300, 7, 0.1)])
+def test_schedule_parity(R, gamma, rho):
+    rng = np.random.default_rng(R * 100 + gamma)
+    for trial in range(4):
+        c = (1 / (1 + np.exp(-rng.normal(1.5, 1.0, (R, gamma))))).astype(np.float32)
+        if trial == 3:
+            c[:, : max(1, gamma // 2)] = 1.0          # exact ties along requests
+            c[0, 0] = 0.0                               # a zero candidate
+        sps = synth.gen_sps(R, gamma, rho)
+        if trial == 2:
+            sps = sps[: R * (1 + gamma) // 2 + 1]       # table shorter than the batch
+        out = binding.schedule(dev(c), dev(sps))
+        torch.cuda.synchronize()
+        L, th, n, gap = oracle.schedule_closed(c, sps)
+        L2, th2, n2 = oracle.schedule_loop(c, sps)
+        assert np.array_equal(L, L2) and n == n2
+        if gap < 1e-12:
+            continue                                     # flagged near-tie of Theta
+        np.testing.assert_array_equal(host(out["verify_len"]), L)
+        assert int(host(out["n_star"])[0]) == n
+        np.testing.assert_allclose(host(out["theta"])[0], th, rtol=1e-12)
+
+
+def test_schedule_toy_workload():
+    w = synth.WORKLOADS["toy"]
+    c = synth.gen_c(w)
+    sps = synth.gen_sps(w.R, w.gamma, w.rho)
+    out = binding.schedule(dev(c), dev(sps))
+    L, th, n = oracle.schedule_loop(c, sps)
+    np.testing.assert_array_equal(host(out["verify_len"]), L)
+    assert 0 < n < w.R * w.gamma
+
+
+def test_bad_anchor_sets_status_not_fault():
+    w = SMALL["bf16_r64"]
+    x = synth.gen_all(w)
+    x["anchor"] = x["anchor"].copy()
+    x["anchor"][2] = w.V + 5
+    d = binding.draft_markov(dev(x["U"]), dev(x["anchor"]), dev(x["W1"]), dev(x["W2"]), w.T, 3)
+    torch.cuda.synchronize()
+    assert binding.workspace_status(d["ws"]) == -6
+    assert binding.workspace_status(d["ws"]) == 0          # cleared by the read
+
+
+def test_bad_draft_token_in_verify_sets_status():
+    w = SMALL["bf16_r64"]
+    x = synth.gen_all(w)
+    dr = oracle_draft(w, x, 1)
+    dr["tokens"] = dr["tokens"].copy()
+    dr["tokens"][0, 0] = -3
+    qx = dr["qx"].astype(np.float32)
+    draft = dict(tokens=dev(dr["tokens"]), q_tok=dev(qx), lse=dev(dr["lse"]), code=dev(dr["code"].astype(np.float32)))
+    v = binding.verify(dev(x["P"]), dev(x["U"]), dev(x["W2"]), draft, w.T, 1)
+    torch.cuda.synchronize()
+    assert binding.workspace_status(v["ws"]) == -6
+
+
+def test_host_argument_errors():
+    w = SMALL["bf16_r64"]
+    x = synth.gen_all(w)
+    with pytest.raises(binding.DsparkError) as e:
+        binding.draft_markov(dev(x["U"]), dev(x["anchor"]), dev(x["W1"]), dev(x["W2"]), -1.0, 0)
+    assert e.value.code == -1
+    small_ws = torch.zeros(256, dtype=torch.uint8, device="cuda:0")
+    with pytest.raises(binding.DsparkError) as e:
+        binding.draft_markov(dev(x["U"]), dev(x["anchor"]), dev(x["W1"]), dev(x["W2"]), 1.0, 0, ws=small_ws)
+    assert e.value.code == -8
