@@ -121,32 +121,25 @@ def algorithmic_bytes(w, n_rej: float, verify_rows: int):
                 residual_per_launch=resid)
 
 
-def cpu_oracle_sample(w, x, target_s: float = 12.0, max_req: int = 64):
-    """Time the CPU oracle (draft + schedule + verify) on a bounded sample of
-    requests of the same workload; returns positions/s and the sample size."""
+def cpu_oracle_sample(w, x, target_s: float = 10.0):
+    """Time the CPU oracle (draft + schedule + verify) on the workload itself:
+    whole cycles over all R requests, repeated with fresh seeds until about
+    target_s of CPU work; returns positions/s."""
     import oracle
     cores = oracle.default_threads()
-
-    def run(n):
-        idx = np.arange(n)
-        sub = {k: (v[idx] if k in ("U", "P", "anchor", "c") else v) for k, v in x.items()}
+    idx = np.arange(w.R).astype(np.uint32)
+    t_tot, cycles = 0.0, 0
+    while t_tot < target_s and cycles < 8:
         t0 = time.perf_counter()
-        d = oracle.draft_markov(sub["U"], sub["anchor"], sub["W1"], sub["W2"], w.T, 7, req_ids=idx.astype(np.uint32))
+        d = oracle.draft_markov(x["U"], x["anchor"], x["W1"], x["W2"], w.T, 7 + cycles, req_ids=idx)
         oracle.schedule_loop(x["c"], x["sps"])
-        oracle.verify(sub["P"], sub["U"], sub["W2"], d["tokens"], d["qx"], d["lse"], d["code"], w.T, 7,
-                      req_ids=idx.astype(np.uint32))
-        return time.perf_counter() - t0
-
-    n = min(cores, w.R)
-    t = run(n)
-    if t < target_s / 3 and n < max_req:
-        n2 = int(min(max_req, w.R, max(n + 1, n * target_s / max(t, 1e-3))))
-        n2 = max(n, (n2 // cores) * cores) if n2 >= cores else n2
-        if n2 > n:
-            n, t = n2, run(n2)
-    return dict(value=n * w.gamma / t, unit="positions/s", cores=cores, kind="oracle",
-                sample=f"{n} of {w.R} requests (all {w.gamma} positions, V={w.V}), draft+schedule+verify, "
-                       f"{t:.2f} s")
+        oracle.verify(x["P"], x["U"], x["W2"], d["tokens"], d["qx"], d["lse"], d["code"], w.T, 7 + cycles,
+                      req_ids=idx)
+        t_tot += time.perf_counter() - t0
+        cycles += 1
+    return dict(value=cycles * w.R * w.gamma / t_tot, unit="positions/s", cores=cores, kind="oracle",
+                sample=f"{cycles} full cycle(s) of the workload (all {w.R} requests x {w.gamma} positions, "
+                       f"V={w.V}): draft+schedule+verify, {t_tot:.2f} s on {cores} threads")
 
 
 def run_reference(args):

@@ -304,6 +304,7 @@ static cudaError_t launch_sweep(DraftArgs& a, int k, bool use_tc, cudaStream_t s
 }
 
 cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
+    a.rnn = rnn ? 1 : 0;
     const bool use_tc = draft_tc_supported(a);
     a.n_slices = use_tc ? draft_tc_slices(a) : (a.V + kGenericSlice - 1) / kGenericSlice;
     const size_t rnn_smem = (size_t)(2 * a.r + a.d) * sizeof(float);

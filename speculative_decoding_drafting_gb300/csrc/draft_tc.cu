@@ -1,22 +1,395 @@
-// draft_tc.cu -- tensor-core (tcgen05) V sweep of the drafter.
+// draft_tc.cu -- tensor-core V sweep of one draft step (sm_103a, tcgen05 + TMA).
+//
+// For step k the Markov head's bias is B_k = e_k W2 with e_k = W1[x_{k-1}]
+// ("DSpark: DeepSeek 线上跑的投机解码" blog, section 3.2 MarkovHead; DSpark
+// explainer, section 03, q_k = softmax(U_k + B_k)).  One CTA owns 128
+// requests (an M-group) and a contiguous slice of 64-wide vocabulary tiles:
+//
+//   warp 0  TMA producer: e_k rows (A, once), then per tile the W2 tile
+//           (B, r x 64 bf16, kept in L2 with evict-last) and the U_k tile
+//           (128 x 64, streamed with evict-first) into a ring of stages
+//   warp 1  MMA issuer: r/16 tcgen05.mma (M=128, N=64, K=16, bf16 -> f32)
+//           into one of two TMEM accumulators, committed to mbarriers
+//   warps 2-5  epilogue: thread = one request row; tcgen05.ld its 64
+//           accumulator columns, add U_k from shared memory, z = (U+B)/T,
+//           online log-sum-exp and the Gumbel race (row_acc.cuh); at the end
+//           one partial per (row, slice) goes to the workspace
+//
+// B_k and q_k never leave the SM.  Every wait is bounded (mbar_wait); a CTA
+// that gives up records DSPARK_ERR_TIMEOUT in the workspace status word,
+// lets the other roles wind down, and still frees its tensor memory.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "profile.h"
+#include "row_acc.cuh"
+#include "sm100.cuh"
 
 namespace dspark {
 
+namespace {
+
+constexpr int kBM = 128;           // requests per CTA (one M-group)
+constexpr int kBN = 64;            // vocabulary columns per tile
+constexpr int kNB = 2;             // W2 stages
+constexpr int kNU = 3;             // U stages
+constexpr int kNACC = 2;           // TMEM accumulators
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 128;
+constexpr int kUStageBytes = kBM * kBN * 4;   // 32 KB (f32); bf16 uses half
+
+struct TcParams {
+    DraftPartial* parts;     // this step's partial buffer [R][n_slices]
+    const uint32_t* req_ids;
+    void* ws;
+    int R, V, r, k;          // k = 1-based step
+    int ntiles, nslices;
+    float invT;
+    uint64_t seed;
+};
+
+struct Smem {
+    uint8_t* A;
+    uint8_t* B;
+    uint8_t* U;
+    uint64_t* a_full;
+    uint64_t* b_full;
+    uint64_t* b_empty;
+    uint64_t* u_full;
+    uint64_t* u_empty;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint32_t* tmem_holder;
+    int* abort_flag;
+};
+
+__host__ __device__ constexpr size_t smem_bytes_for(int r) {
+    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * r * 128 + (size_t)kNU * kUStageBytes + 256;
+}
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
+    Smem s;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.A = base;
+    s.B = s.A + (size_t)(r / 64) * 16384;
+    s.U = s.B + (size_t)kNB * r * 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.U + (size_t)kNU * kUStageBytes);
+    s.a_full = bars;
+    s.b_full = bars + 1;
+    s.b_empty = s.b_full + kNB;
+    s.u_full = s.b_empty + kNB;
+    s.u_empty = s.u_full + kNU;
+    s.acc_full = s.u_empty + kNU;
+    s.acc_empty = s.acc_full + kNACC;
+    s.tmem_holder = reinterpret_cast<uint32_t*>(s.acc_empty + kNACC);
+    s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
+    return s;
+}
+
+template <int UT, bool GREEDY>
+__global__ void __launch_bounds__(kThreads, 1)
+    draft_sweep_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmU, TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem S = carve(smem_raw, p.r);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slice = blockIdx.x, mg = blockIdx.y;
+    const int t_begin = (int)((long long)slice * p.ntiles / p.nslices);
+    const int t_end = (int)((long long)(slice + 1) * p.ntiles / p.nslices);
+    const int nt = t_end - t_begin;
+    const int kblocks = p.r / 64;
+    volatile int* abort_flag = S.abort_flag;
+
+    if (threadIdx.x == 0) {
+        mbar_init(S.a_full, 1);
+        for (int i = 0; i < kNB; ++i) {
+            mbar_init(&S.b_full[i], 1);
+            mbar_init(&S.b_empty[i], 1);
+        }
+        for (int i = 0; i < kNU; ++i) {
+            mbar_init(&S.u_full[i], 1);
+            mbar_init(&S.u_empty[i], 128);
+        }
+        for (int i = 0; i < kNACC; ++i) {
+            mbar_init(&S.acc_full[i], 1);
+            mbar_init(&S.acc_empty[i], 128);
+        }
+        *S.abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmU);
+    }
+    if (warp == 1) tmem_alloc(S.tmem_holder, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *S.tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer
+            const uint64_t pol_first = policy_evict_first();
+            const uint64_t pol_last = policy_evict_last();
+            mbar_expect_tx(S.a_full, (uint32_t)kblocks * 16384u);
+            for (int kb = 0; kb < kblocks; ++kb)
+                tma_load_2d(S.A + kb * 16384, &tmA, S.a_full, kb * 64, mg * kBM, pol_last);
+            const uint32_t ubytes = UT == DSPARK_F32 ? (uint32_t)kUStageBytes : (uint32_t)(kUStageBytes / 2);
+            int issued = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int v0 = (t_begin + t) * kBN;
+                const int bs = t % kNB;
+                const uint32_t bph = (uint32_t)(t / kNB) & 1u;
+                if (!mbar_wait(&S.b_empty[bs], bph ^ 1u, abort_flag)) break;
+                mbar_expect_tx(&S.b_full[bs], (uint32_t)p.r * 128u);
+                tma_load_2d(S.B + (size_t)bs * p.r * 128, &tmB, &S.b_full[bs], v0, 0, pol_last);
+                const int us = t % kNU;
+                const uint32_t uph = (uint32_t)(t / kNU) & 1u;
+                if (!mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag)) break;
+                mbar_expect_tx(&S.u_full[us], ubytes);
+                uint8_t* dst = S.U + (size_t)us * kUStageBytes;
+                if (UT == DSPARK_F32) {
+                    tma_load_3d(dst, &tmU, &S.u_full[us], v0, p.k - 1, mg * kBM, pol_first);
+                    tma_load_3d(dst + kUStageBytes / 2, &tmU, &S.u_full[us], v0 + 32, p.k - 1, mg * kBM, pol_first);
+                } else {
+                    tma_load_3d(dst, &tmU, &S.u_full[us], v0, p.k - 1, mg * kBM, pol_first);
+                }
+                issued = t + 1;
+            }
+            if (*abort_flag) {
+                // wind down: let the copies this thread issued land before exit
+                mbar_wait_for(S.a_full, 0, kWaitLimitNs);
+                for (int t = (issued > kNU ? issued - kNU : 0); t < issued; ++t) {
+                    mbar_wait_for(&S.b_full[t % kNB], (uint32_t)(t / kNB) & 1u, kWaitLimitNs);
+                    mbar_wait_for(&S.u_full[t % kNU], (uint32_t)(t / kNU) & 1u, kWaitLimitNs);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
+            bool ok = mbar_wait(S.a_full, 0, abort_flag);
+            tc_fence_after();
+            for (int t = 0; ok && t < nt; ++t) {
+                const int bs = t % kNB;
+                const uint32_t bph = (uint32_t)(t / kNB) & 1u;
+                const int buf = t % kNACC;
+                const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
+                if (!mbar_wait(&S.acc_empty[buf], aph ^ 1u, abort_flag)) break;
+                if (!mbar_wait(&S.b_full[bs], bph, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * kBN);
+                const uint8_t* bstage = S.B + (size_t)bs * p.r * 128;
+                for (int kk = 0; kk < p.r / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(S.A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
+                    umma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&S.b_empty[bs]);
+                umma_commit(&S.acc_full[buf]);
+            }
+        }
+    } else {
+        // ---------------- epilogue: one request row per thread
+        const int q = warp & 3;                      // TMEM lane quarter of this warp
+        const int rit = q * 32 + lane;               // row inside the tile
+        const int row = mg * kBM + rit;
+        const bool row_ok = row < p.R;
+        const uint32_t req = row_ok ? (p.req_ids ? p.req_ids[row] : (uint32_t)row) : 0u;
+        const PhiloxKey key = philox_key(p.seed);
+        RowAcc acc;
+        acc_init(acc);
+        for (int t = 0; t < nt; ++t) {
+            const int v0 = (t_begin + t) * kBN;
+            const int buf = t % kNACC;
+            const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
+            const int us = t % kNU;
+            const uint32_t uph = (uint32_t)(t / kNU) & 1u;
+            bool ready = mbar_wait(&S.acc_full[buf], aph, abort_flag);
+            ready = ready && mbar_wait(&S.u_full[us], uph, abort_flag);
+            if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
+            tc_fence_after();
+            const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float a[32];
+                __syncwarp();
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + h * 32), a);
+                float u[32];
+                if (UT == DSPARK_F32) {
+                    const uint8_t* rowp = ust + h * (kUStageBytes / 2) + rit * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 f = *reinterpret_cast<const float4*>(rowp + ((c ^ (rit & 7)) << 4));
+                        u[4 * c + 0] = f.x;
+                        u[4 * c + 1] = f.y;
+                        u[4 * c + 2] = f.z;
+                        u[4 * c + 3] = f.w;
+                    }
+                } else {
+                    const uint8_t* rowp = ust + rit * 128;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 f = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (rit & 7)) << 4));
+                        const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            u[8 * c + 2 * e + 0] = bf16_bits_to_float(w4[e] & 0xFFFFu);
+                            u[8 * c + 2 * e + 1] = bf16_bits_to_float(w4[e] >> 16);
+                        }
+                    }
+                }
+                float z[32];
+                int col[32];
+                bool ok[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    col[i] = v0 + h * 32 + i;
+                    ok[i] = row_ok && col[i] < p.V;
+                    z[i] = GREEDY ? (a[i] + u[i]) : (a[i] + u[i]) * p.invT;
+                }
+                if (GREEDY) {
+                    acc_update_greedy<32>(acc, z, col, ok);
+                } else {
+                    float tt[32];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint4 w = philox4x32_10(
+                            make_uint4((uint32_t)(v0 + h * 32 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), key);
+                        tt[4 * g + 0] = word_to_one_minus_uniform(w.x);
+                        tt[4 * g + 1] = word_to_one_minus_uniform(w.y);
+                        tt[4 * g + 2] = word_to_one_minus_uniform(w.z);
+                        tt[4 * g + 3] = word_to_one_minus_uniform(w.w);
+                    }
+                    acc_update_sample<32>(acc, z, tt, col, ok);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&S.acc_empty[buf]);
+            mbar_arrive(&S.u_empty[us]);
+        }
+        if (row_ok && !*abort_flag) p.parts[(size_t)row * p.nslices + slice] = acc_to_partial(acc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) raise_status(p.ws, kStatTimeout);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, (cuuint32_t)rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int slices_for(const DraftArgs& a) {
+    const int n_mg = (a.R + kBM - 1) / kBM;
+    const int ntiles = (a.V + kBN - 1) / kBN;
+    int ns = num_sms() / n_mg;
+    if (ns < 1) ns = 1;
+    if (ns > ntiles) ns = ntiles;
+    if (ns > 1024) ns = 1024;
+    return ns;
+}
+
+template <int UT, bool GREEDY>
+cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
+    CUtensorMap tmA, tmB, tmU;
+    // A: the bf16 codes e_k, [R rows x r], boxes of 64 x 128 rows
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.r, (cuuint64_t)a.R};
+        cuuint64_t str[1] = {(cuuint64_t)a.r * 2};
+        cuuint32_t box[2] = {64, kBM};
+        if (!make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ebf, dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    // B: W2 [r rows x V], boxes of 64 columns x r rows
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
+        cuuint64_t str[1] = {(cuuint64_t)a.V * 2};
+        cuuint32_t box[2] = {kBN, (cuuint32_t)a.r};
+        if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    // U: [R, gamma, V] as a 3-d tensor (V, gamma, R); box 128 B x 1 x 128 rows
+    {
+        const size_t es = UT == DSPARK_F32 ? 4 : 2;
+        cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
+        cuuint64_t str[2] = {(cuuint64_t)a.V * es, (cuuint64_t)a.gamma * a.V * es};
+        cuuint32_t box[3] = {UT == DSPARK_F32 ? 32u : 64u, 1u, (cuuint32_t)kBM};
+        if (!make_map(&tmU, UT == DSPARK_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      3, const_cast<void*>(a.U), dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    TcParams p;
+    p.parts = a.parts + (size_t)(k & 1) * a.parts_stride;
+    p.req_ids = a.req_ids;
+    p.ws = a.ws;
+    p.R = a.R;
+    p.V = a.V;
+    p.r = a.r;
+    p.k = k;
+    p.ntiles = (a.V + kBN - 1) / kBN;
+    p.nslices = a.n_slices;
+    p.invT = a.T > 0.f ? 1.f / a.T : 1.f;
+    p.seed = a.seed;
+    const size_t smem = smem_bytes_for(a.r);
+    auto kern = draft_sweep_tc<UT, GREEDY>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.n_slices, (a.R + kBM - 1) / kBM);
+    prof_begin(kPDraftSweepTc, s);
+    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmU, p);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 bool draft_tc_supported(const DraftArgs& a) {
-    (void)a;
-    return false;
+    if (a.rnn) return false;                       // e_k = tanh(out) is not bf16-exact
+    if (a.w_dtype != DSPARK_BF16) return false;
+    if (a.r % 64 != 0 || a.r > 256) return false;
+    if (a.V % 8 != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(a.U) & 15) || (reinterpret_cast<uintptr_t>(a.W2) & 15)) return false;
+    if (smem_bytes_for(a.r) > 232448) return false;
+    return encode_fn() != nullptr;
 }
-int draft_tc_slices(const DraftArgs& a) {
-    (void)a;
-    return 1;
-}
+
+int draft_tc_slices(const DraftArgs& a) { return slices_for(a); }
+
 cudaError_t launch_draft_tc_sweep(DraftArgs& a, int k, cudaStream_t s) {
-    (void)a;
-    (void)k;
-    (void)s;
-    return cudaErrorNotSupported;
+    const bool greedy = !(a.T > 0.f);
+    if (a.u_dtype == DSPARK_F32)
+        return greedy ? launch_typed<DSPARK_F32, true>(a, k, s) : launch_typed<DSPARK_F32, false>(a, k, s);
+    return greedy ? launch_typed<DSPARK_BF16, true>(a, k, s) : launch_typed<DSPARK_BF16, false>(a, k, s);
 }
 
 }  // namespace dspark
