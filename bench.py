@@ -288,38 +288,42 @@ def main(argv=None):
     cycle_gbs = ab["total"] / (tot_ms / args.steps / 1000.0) / 1e9 if world == 1 else None
 
     # end to end through the C ABI with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    hU, hP, hA, hC = pin(x["U"]), pin(x["P"]), pin(x["anchor"]), pin(x["c"])
-    if x["U"].dtype == np.uint16:
-        hU = hU.view(torch.bfloat16)
-    if x["P"].dtype == np.uint16:
-        hP = hP.view(torch.bfloat16)
-    h_out = torch.empty((w.R, w.gamma + 1), dtype=torch.int32).pin_memory()
-    h_n = torch.empty((w.R,), dtype=torch.int32).pin_memory()
-    e2e_ms = []
-    for i in range(args.e2e_steps + 1):
-        flush.zero_()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        U.copy_(hU, non_blocking=True)
-        P.copy_(hP, non_blocking=True)
-        anchor.copy_(hA, non_blocking=True)
-        c.copy_(hC, non_blocking=True)
-        d, s, v = step(5000 + i, wss)
-        h_out.copy_(v["out_tokens"], non_blocking=True)
-        h_n.copy_(v["n_out"], non_blocking=True)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        if i > 0:
-            e2e_ms.append(a0.elapsed_time(a1))
-    h2d = int(hU.numel() * hU.element_size() + hP.numel() * hP.element_size() + hA.numel() * 4 + hC.numel() * 4)
-    d2h = int(h_out.numel() * 4 + h_n.numel() * 4)
-    e2e_tot = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_tot], device=devc, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_tot = float(t.item())
-    e2e_value = w.R * w.gamma * world * len(e2e_ms) / (e2e_tot / 1000.0)
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        hU, hP, hA, hC = pin(x["U"]), pin(x["P"]), pin(x["anchor"]), pin(x["c"])
+        if x["U"].dtype == np.uint16:
+            hU = hU.view(torch.bfloat16)
+        if x["P"].dtype == np.uint16:
+            hP = hP.view(torch.bfloat16)
+        h_out = torch.empty((w.R, w.gamma + 1), dtype=torch.int32).pin_memory()
+        h_n = torch.empty((w.R,), dtype=torch.int32).pin_memory()
+        e2e_ms = []
+        for i in range(args.e2e_steps + 1):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            U.copy_(hU, non_blocking=True)
+            P.copy_(hP, non_blocking=True)
+            anchor.copy_(hA, non_blocking=True)
+            c.copy_(hC, non_blocking=True)
+            d, s, v = step(5000 + i, wss)
+            h_out.copy_(v["out_tokens"], non_blocking=True)
+            h_n.copy_(v["n_out"], non_blocking=True)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            if i > 0:
+                e2e_ms.append(a0.elapsed_time(a1))
+        h2d = int(hU.numel() * hU.element_size() + hP.numel() * hP.element_size() + hA.numel() * 4 + hC.numel() * 4)
+        d2h = int(h_out.numel() * 4 + h_n.numel() * 4)
+        e2e_tot = sum(e2e_ms)
+        if world > 1:
+            t = torch.tensor([e2e_tot], device=devc, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_tot = float(t.item())
+        e2e_value = w.R * w.gamma * world * len(e2e_ms) / (e2e_tot / 1000.0)
+        e2e = {"value": round(e2e_value, 1), "unit": "positions/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / len(e2e_ms), 3)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -346,8 +350,7 @@ def main(argv=None):
             "gpu_launches": len(launches),
             "clocks": clk,
             "wall_s_timed": round(t_wall, 3),
-            "e2e": {"value": round(e2e_value, 1), "unit": "positions/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / len(e2e_ms), 3)},
+            "e2e": e2e,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -40,7 +40,7 @@
  *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key
  *    (seed low 32 bits, seed high 32 bits) and counter
  *    (v / 4, request id, position, stream); index v takes output word v mod 4
- *    and becomes u = ((w >> 9) + 1/2) * 2^-23 in (0, 1).  Streams:
+ *    and becomes u = (w + 1/2) * 2^-32 in (0, 1).  Streams:
  *    0 = draft Gumbel noise (v = vocabulary index, position k = 1..gamma),
  *    1 = acceptance uniform (v = 0, position k),
  *    2 = residual / bonus draw (v = tree level, position = the position sampled).

@@ -51,7 +51,7 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
 }
 
 double oracle_uniform(uint32_t w) {
-    return ((double)(w >> 9) + 0.5) * (1.0 / 8388608.0);   /* 2^-23 */
+    return ((double)w + 0.5) * (1.0 / 4294967296.0);   /* (w + 1/2) 2^-32 */
 }
 
 /* Counter (v/4, request, position, stream), key (seed lo, seed hi); the

@@ -32,7 +32,7 @@ enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
 
 /* Philox4x32-10 block function. */
 void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
-/* Uniform in (0,1) from one 32-bit word: ((w >> 9) + 1/2) * 2^-23. */
+/* Uniform in (0,1) from one 32-bit word: (w + 1/2) * 2^-32 (exact in double). */
 double oracle_uniform(uint32_t w);
 /* The uniform for (seed, request id, position, stream, index v). */
 double oracle_rng_uniform(uint64_t seed, uint32_t req, uint32_t pos, uint32_t stream, uint32_t v);

@@ -38,14 +38,21 @@ __host__ __device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
     return PhiloxKey{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
 }
 
+// 32 x 32 -> 64-bit product as one wide multiply.
+__device__ __forceinline__ uint64_t mul_wide_u32(uint32_t a, uint32_t b) {
+    uint64_t r;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
     uint32_t k0 = key.k0, k1 = key.k1;
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        const uint32_t lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+        const uint64_t p0 = mul_wide_u32(0xD2511F53u, c.x);
+        const uint64_t p1 = mul_wide_u32(0xCD9E8D57u, c.z);
+        const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
+        const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
         c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
@@ -53,16 +60,17 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
     return c;
 }
 
-// u = ((w >> 9) + 1/2) 2^-23, exact in float.
-__device__ __forceinline__ float word_to_uniform(uint32_t w) {
-    return __uint_as_float(0x3F800000u | (w >> 9)) - 0.99999994039535522f;
-}
-// t = 1 - u for the same word, also exact: the complemented top 23 bits.
-__device__ __forceinline__ float word_to_one_minus_uniform(uint32_t w) {
-    return __uint_as_float(0x3F800000u | ((~w) >> 9)) - 0.99999994039535522f;
-}
+// u = (w + 1/2) 2^-32 in (0, 1), exact in double.
 __device__ __forceinline__ double word_to_uniform_d(uint32_t w) {
-    return (static_cast<double>(w >> 9) + 0.5) * (1.0 / 8388608.0);
+    return ((double)w + 0.5) * (1.0 / 4294967296.0);
+}
+// t = 1 - u = (~w + 1/2) 2^-32 in float (relative error below 2^-24).
+__device__ __forceinline__ float word_to_t(uint32_t w) {
+    return fmaf(__uint2float_rn(~w), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
+}
+// A lower bound on t from the top 23 bits of ~w: floor(~w / 2^9) 2^-23 <= t.
+__device__ __forceinline__ float word_to_t_lower(uint32_t w) {
+    return __uint_as_float(0x3F800000u | ((~w) >> 9)) - 1.0f;
 }
 
 __device__ __forceinline__ uint32_t pick_word(uint4 w, uint32_t i) {
@@ -83,11 +91,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Exponential race key: for t = 1 - u (exact), E = -ln u = -log1p(-t) and the
-// Gumbel-max key of logit z is z - ln E  (= z + G with G = -ln(-ln u)).
-__device__ __forceinline__ float race_key(float z, float t) {
+// Gumbel-max key in base-2 units.  With y = z log2(e) the tempered logit in
+// bits and t = 1 - u, E = -ln u = -log1p(-t) is an Exp(1) variate and
+// z + G = z - ln E (G = -ln(-ln u)); in bits the key is y - log2(E).
+__device__ __forceinline__ float race_key2(float y, uint32_t word) {
+    const float t = word_to_t(word);
     const float E = -log1pf(-t);
-    return z - logf(E);
+    return y - log2f(E);
 }
 
 // ---------------------------------------------------------------- loads

@@ -66,9 +66,9 @@ __device__ int finish_step(const DraftArgs& A, int r, int kprev, const DraftPart
         }
         A.tokens[o] = x;
         if (A.T > 0.f) {
-            // q(x) = exp(z_x - m) / s;  lse = m + ln s
-            A.q_tok[o] = (float)(exp((double)a.zb - (double)a.m) / a.s);
-            A.lse[o] = (double)a.m + log(a.s);
+            // base-2 state: q(x) = 2^(y_x - m) / s;  lse = ln2 (m + log2 s)
+            A.q_tok[o] = (float)((double)exp2f(a.zb - a.m) / a.s);
+            A.lse[o] = 0.69314718055994531 * ((double)a.m + log2(a.s));
         } else {
             A.q_tok[o] = 1.f;
             A.lse[o] = 0.0;
@@ -204,33 +204,30 @@ __global__ void __launch_bounds__(256) draft_sweep_generic(DraftArgs A, int k) {
     }
     const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
     const PhiloxKey key = philox_key(A.seed);
-    const float invT = GREEDY ? 1.f : 1.f / A.T;
+    const float c2 = GREEDY ? 1.f : kLog2e / A.T;     // tempered logits in bits
     const size_t urow = ((size_t)r * A.gamma + (k - 1)) * (size_t)V;
     RowAcc a;
     acc_init(a);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        float z[4], t[4];
+        float y[4];
         int c4[4];
         bool v4[4];
         float4 u = ok[g] ? load4<UT>(A.U, urow + col[g]) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            z[q] = GREEDY ? (uu[q] + acc[g][q]) : (uu[q] + acc[g][q]) * invT;
+            y[q] = GREEDY ? (uu[q] + acc[g][q]) : (uu[q] + acc[g][q]) * c2;
             c4[q] = col[g] + q;
             v4[q] = ok[g];
         }
         if (GREEDY) {
-            acc_update_greedy<4>(a, z, c4, v4);
+            acc_update_greedy<4>(a, y, c4, v4);
         } else {
             uint4 w = ok[g] ? philox4x32_10(make_uint4((uint32_t)col[g] >> 2, req, (uint32_t)k, 0u), key)
                             : make_uint4(0, 0, 0, 0);
-            t[0] = word_to_one_minus_uniform(w.x);
-            t[1] = word_to_one_minus_uniform(w.y);
-            t[2] = word_to_one_minus_uniform(w.z);
-            t[3] = word_to_one_minus_uniform(w.w);
-            acc_update_sample<4>(a, z, t, c4, v4);
+            const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+            acc_update_exact<4>(a, y, wd, c4, v4);
         }
     }
     // block reduce -> partial of this slice

@@ -35,9 +35,23 @@ constexpr int kBN = 64;            // vocabulary columns per tile
 constexpr int kNB = 2;             // W2 stages
 constexpr int kNU = 3;             // U stages
 constexpr int kNACC = 2;           // TMEM accumulators
-constexpr int kThreads = 192;
+constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 16 of a tile's 64 columns
+constexpr int kEpiWarps = 4 * kEpiWG;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 128;
 constexpr int kUStageBytes = kBM * kBN * 4;   // 32 KB (f32); bf16 uses half
+// Margin on the candidate test; the exact key decides, the test only has to
+// stay conservative against the rounding of w and 2^(m_t - kthr).
+constexpr float kRaceSafety = 1.0009765625f;   // 1 + 2^-10
+
+// Order-preserving map of float keys to unsigned (for atomicMax in shared memory).
+__device__ __forceinline__ uint32_t key_order(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_from_order(uint32_t e) {
+    return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
+}
 
 struct TcParams {
     DraftPartial* parts;     // this step's partial buffer [R][n_slices]
@@ -45,7 +59,7 @@ struct TcParams {
     void* ws;
     int R, V, r, k;          // k = 1-based step
     int ntiles, nslices;
-    float invT;
+    float c2;                // log2(e) / T
     uint64_t seed;
 };
 
@@ -62,10 +76,11 @@ struct Smem {
     uint64_t* acc_empty;
     uint32_t* tmem_holder;
     int* abort_flag;
+    uint32_t* best;          // [128] best race key seen so far per row (order-preserving bits)
 };
 
 __host__ __device__ constexpr size_t smem_bytes_for(int r) {
-    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * r * 128 + (size_t)kNU * kUStageBytes + 256;
+    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * r * 128 + (size_t)kNU * kUStageBytes + 256 + 512;
 }
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
@@ -84,6 +99,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
     s.acc_empty = s.acc_full + kNACC;
     s.tmem_holder = reinterpret_cast<uint32_t*>(s.acc_empty + kNACC);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
+    s.best = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) + 256);
     return s;
 }
 
@@ -109,13 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kNU; ++i) {
             mbar_init(&S.u_full[i], 1);
-            mbar_init(&S.u_empty[i], 128);
+            mbar_init(&S.u_empty[i], kEpiWarps);
         }
         for (int i = 0; i < kNACC; ++i) {
             mbar_init(&S.acc_full[i], 1);
-            mbar_init(&S.acc_empty[i], 128);
+            mbar_init(&S.acc_empty[i], kEpiWarps);
         }
         *S.abort_flag = 0;
+        for (int i = 0; i < kBM; ++i) S.best[i] = key_order(-INFINITY);
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -192,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue: one request row per thread
+        // ---------------- epilogue: thread = (request row, 16-column quarter of each tile)
+        const int wg = (warp - 2) >> 2;              // column quarter
         const int q = warp & 3;                      // TMEM lane quarter of this warp
         const int rit = q * 32 + lane;               // row inside the tile
         const int row = mg * kBM + rit;
@@ -202,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         RowAcc acc;
         acc_init(acc);
         for (int t = 0; t < nt; ++t) {
-            const int v0 = (t_begin + t) * kBN;
+            const int v0 = (t_begin + t) * kBN + wg * 16;
             const int buf = t % kNACC;
             const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
             const int us = t % kNU;
@@ -211,66 +229,127 @@ __global__ void __launch_bounds__(kThreads, 1)
             ready = ready && mbar_wait(&S.u_full[us], uph, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
             tc_fence_after();
+            __syncwarp();
+            float a[16];
+            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), a);
+            float y[16];
             const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float a[32];
-                __syncwarp();
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + h * 32), a);
-                float u[32];
-                if (UT == DSPARK_F32) {
-                    const uint8_t* rowp = ust + h * (kUStageBytes / 2) + rit * 128;
+            if (UT == DSPARK_F32) {
+                const uint8_t* rowp = ust + (wg >> 1) * (kUStageBytes / 2) + rit * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 f = *reinterpret_cast<const float4*>(rowp + ((c ^ (rit & 7)) << 4));
-                        u[4 * c + 0] = f.x;
-                        u[4 * c + 1] = f.y;
-                        u[4 * c + 2] = f.z;
-                        u[4 * c + 3] = f.w;
-                    }
-                } else {
-                    const uint8_t* rowp = ust + rit * 128;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 f = *reinterpret_cast<const uint4*>(rowp + (((4 * h + c) ^ (rit & 7)) << 4));
-                        const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            u[8 * c + 2 * e + 0] = bf16_bits_to_float(w4[e] & 0xFFFFu);
-                            u[8 * c + 2 * e + 1] = bf16_bits_to_float(w4[e] >> 16);
-                        }
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    const float4 f =
+                        *reinterpret_cast<const float4*>(rowp + ((((wg & 1) * 4 + c) ^ (rit & 7)) << 4));
+                    y[4 * c + 0] = a[4 * c + 0] + f.x;
+                    y[4 * c + 1] = a[4 * c + 1] + f.y;
+                    y[4 * c + 2] = a[4 * c + 2] + f.z;
+                    y[4 * c + 3] = a[4 * c + 3] + f.w;
                 }
-                float z[32];
-                int col[32];
-                bool ok[32];
+            } else {
+                const uint8_t* rowp = ust + rit * 128;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    col[i] = v0 + h * 32 + i;
-                    ok[i] = row_ok && col[i] < p.V;
-                    z[i] = GREEDY ? (a[i] + u[i]) : (a[i] + u[i]) * p.invT;
-                }
-                if (GREEDY) {
-                    acc_update_greedy<32>(acc, z, col, ok);
-                } else {
-                    float tt[32];
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 f = *reinterpret_cast<const uint4*>(rowp + (((2 * wg + c) ^ (rit & 7)) << 4));
+                    const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const uint4 w = philox4x32_10(
-                            make_uint4((uint32_t)(v0 + h * 32 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), key);
-                        tt[4 * g + 0] = word_to_one_minus_uniform(w.x);
-                        tt[4 * g + 1] = word_to_one_minus_uniform(w.y);
-                        tt[4 * g + 2] = word_to_one_minus_uniform(w.z);
-                        tt[4 * g + 3] = word_to_one_minus_uniform(w.w);
+                    for (int e = 0; e < 4; ++e) {
+                        y[8 * c + 2 * e + 0] = a[8 * c + 2 * e + 0] + bf16_bits_to_float(w4[e] & 0xFFFFu);
+                        y[8 * c + 2 * e + 1] = a[8 * c + 2 * e + 1] + bf16_bits_to_float(w4[e] >> 16);
                     }
-                    acc_update_sample<32>(acc, z, tt, col, ok);
                 }
             }
+            // the tile's data is in registers: hand the buffers back early
             tc_fence_before();
-            mbar_arrive(&S.acc_empty[buf]);
-            mbar_arrive(&S.u_empty[us]);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&S.acc_empty[buf]);
+                mbar_arrive(&S.u_empty[us]);
+            }
+            if (GREEDY) {
+                int col[16];
+                bool ok[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    col[i] = v0 + i;
+                    ok[i] = row_ok && col[i] < p.V;
+                }
+                acc_update_greedy<16>(acc, y, col, ok);
+                continue;
+            }
+            uint32_t vmask = 0;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                y[i] *= p.c2;                                   // tempered logit in bits
+                const bool ok = row_ok && (v0 + i) < p.V;
+                vmask |= ok ? (1u << i) : 0u;
+                if (ok) mt = fmaxf(mt, y[i]);
+            }
+            if (!__any_sync(0xffffffffu, vmask)) continue;
+            uint32_t word[16];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(v0 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), key);
+                word[4 * g + 0] = w4.x;
+                word[4 * g + 1] = w4.y;
+                word[4 * g + 2] = w4.z;
+                word[4 * g + 3] = w4.w;
+            }
+            uint32_t cand = 0;
+            if (vmask) {
+                float w[16];
+                float st = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    w[i] = (vmask >> i & 1u) ? ex2_approx(y[i] - mt) : 0.f;
+                    st += w[i];
+                }
+                acc_add_mass(acc, mt, st);
+                float kthr = fmaxf(acc.kb, key_from_order(S.best[rit]));
+                if (kthr == -INFINITY) {
+                    // first chunk of the row: seed the race with the largest logit
+                    int istar = 0;
+                    uint32_t wstar = word[0];
+#pragma unroll
+                    for (int i = 15; i >= 0; --i)
+                        if ((vmask >> i & 1u) && y[i] == mt) {
+                            istar = i;
+                            wstar = word[i];
+                        }
+                    acc_take(acc, race_key2(mt, wstar), mt, v0 + istar);
+                    atomicMax(&S.best[rit], key_order(acc.kb));
+                    kthr = acc.kb;
+                }
+                // candidate iff its key can exceed kthr: key <= y - log2(t), t >= t_lower
+                const float cthr = ex2_approx(mt - kthr) * kRaceSafety;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    cand |= ((vmask >> i & 1u) && word_to_t_lower(word[i]) < w[i] * cthr) ? (1u << i) : 0u;
+            }
+            // exact keys of the candidates; lanes without any wait
+            while (__any_sync(0xffffffffu, cand)) {
+                if (cand) {
+                    const int i = __ffs(cand) - 1;
+                    cand &= cand - 1;
+                    float yi = y[0];
+                    uint32_t wi = word[0];
+#pragma unroll
+                    for (int j = 1; j < 16; ++j) {
+                        yi = (i == j) ? y[j] : yi;
+                        wi = (i == j) ? word[j] : wi;
+                    }
+                    const float kk = race_key2(yi, wi);
+                    if (key_better(kk, v0 + i, acc.kb, acc.ib)) {
+                        acc.kb = kk;
+                        acc.zb = yi;
+                        acc.ib = v0 + i;
+                        atomicMax(&S.best[rit], key_order(kk));
+                    }
+                }
+            }
         }
-        if (row_ok && !*abort_flag) p.parts[(size_t)row * p.nslices + slice] = acc_to_partial(acc);
+        if (row_ok && !*abort_flag)
+            p.parts[((size_t)row * p.nslices + slice) * kEpiWG + wg] = acc_to_partial(acc);
     }
     tc_fence_before();
     __syncthreads();
@@ -357,14 +436,14 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.r = a.r;
     p.k = k;
     p.ntiles = (a.V + kBN - 1) / kBN;
-    p.nslices = a.n_slices;
-    p.invT = a.T > 0.f ? 1.f / a.T : 1.f;
+    p.nslices = a.n_slices / kEpiWG;
+    p.c2 = a.T > 0.f ? kLog2e / a.T : 1.f;
     p.seed = a.seed;
     const size_t smem = smem_bytes_for(a.r);
     auto kern = draft_sweep_tc<UT, GREEDY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_slices, (a.R + kBM - 1) / kBM);
+    dim3 grid(a.n_slices / kEpiWG, (a.R + kBM - 1) / kBM);
     prof_begin(kPDraftSweepTc, s);
     kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmU, p);
     prof_end(s);
@@ -383,7 +462,7 @@ bool draft_tc_supported(const DraftArgs& a) {
     return encode_fn() != nullptr;
 }
 
-int draft_tc_slices(const DraftArgs& a) { return slices_for(a); }
+int draft_tc_slices(const DraftArgs& a) { return slices_for(a) * kEpiWG; }
 
 cudaError_t launch_draft_tc_sweep(DraftArgs& a, int k, cudaStream_t s) {
     const bool greedy = !(a.T > 0.f);

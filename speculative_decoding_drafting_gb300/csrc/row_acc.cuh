@@ -1,15 +1,12 @@
 // row_acc.cuh -- per-row running state of the draft's sweep over the vocabulary.
 //
+// Everything is kept in base-2 units: y = z log2(e) with z = (U_k + B_k) / T.
 // For one (request, position) row the sweep keeps
-//   m, s   the log-sum-exp of z = (U_k + B_k) / T in online form, and
-//   kb, ib the Gumbel-max winner so far.
-// Gumbel-max (x = argmax z_v + G_v, G_v = -ln(-ln u_v)) is evaluated as an
-// exponential race: the key of v is z_v - ln E_v with E_v = -ln u_v.  Since
-// E_v >= t_v = 1 - u_v, the key is at most z_v - ln t_v, so an element can
-// only beat the current best kb if t_v < exp(z_v - kb).  That test costs one
-// multiply per element (exp(z_v - kb) = w_v exp(m_t - kb) reuses the
-// log-sum-exp term w_v = exp(z_v - m_t)); only the few elements that pass it
-// pay for the two logarithms of the exact key.
+//   m, s    the log-sum-exp in online form: s = sum_v 2^(y_v - m)
+//   kb, ib  the Gumbel-max winner so far: key2_v = y_v - log2(E_v), with
+//           E_v = -ln u_v an Exp(1) variate (Gumbel-max as an exponential race)
+// so that log-sum-exp = ln2 (m + log2 s) and q(x) = 2^(y_x - m) / s.
+// At T = 0 the key is the raw logit U + B and only (kb, ib) are used.
 #pragma once
 
 #include <float.h>
@@ -19,10 +16,6 @@
 #include "kernels.h"
 
 namespace dspark {
-
-// Margin on the cheap test; the exact key decides, this only has to be
-// conservative against the rounding of w_v and exp(m_t - kb).
-constexpr float kRaceSafety = 1.0009765625f;   // 1 + 2^-10
 
 struct RowAcc {
     float m;
@@ -44,21 +37,35 @@ __device__ __forceinline__ bool key_better(float k1, int i1, float k2, int i2) {
     return k1 > k2 || (k1 == k2 && i1 < i2);
 }
 
-// Merge b into a (log-sum-exp part and race part).
+// Fold a chunk's (max mt, sum st of 2^(y - mt)) into the running (m, s).
+__device__ __forceinline__ void acc_add_mass(RowAcc& a, float mt, float st) {
+    if (mt > a.m) {
+        a.s = a.s * (double)ex2_approx(a.m - mt) + (double)st;
+        a.m = mt;
+    } else {
+        a.s += (double)st * (double)ex2_approx(mt - a.m);
+    }
+}
+
+__device__ __forceinline__ void acc_take(RowAcc& a, float key, float y, int col) {
+    if (key_better(key, col, a.kb, a.ib)) {
+        a.kb = key;
+        a.zb = y;
+        a.ib = col;
+    }
+}
+
+// Merge b into a.
 __device__ __forceinline__ void acc_merge(RowAcc& a, const RowAcc& b) {
     if (b.m != -INFINITY) {
         if (b.m > a.m) {
-            a.s = a.s * (double)ex2_approx((a.m - b.m) * kLog2e) + b.s;
+            a.s = a.s * (double)ex2_approx(a.m - b.m) + b.s;
             a.m = b.m;
         } else {
-            a.s += b.s * (double)ex2_approx((b.m - a.m) * kLog2e);
+            a.s += b.s * (double)ex2_approx(b.m - a.m);
         }
     }
-    if (key_better(b.kb, b.ib, a.kb, a.ib)) {
-        a.kb = b.kb;
-        a.zb = b.zb;
-        a.ib = b.ib;
-    }
+    acc_take(a, b.kb, b.zb, b.ib);
 }
 
 __device__ __forceinline__ RowAcc acc_shfl_xor(const RowAcc& a, int o) {
@@ -98,43 +105,25 @@ __device__ __forceinline__ RowAcc partial_to_acc(const DraftPartial& p) {
     return a;
 }
 
-// Sampling update with N consecutive-in-register values of one row.
-// z[i]: tempered logits, t[i] = 1 - u_i (exact), col[i]: vocabulary index,
-// valid[i]: column inside [0, V).
+// Straightforward sampling update: log-sum-exp mass and the exact race key of
+// every element (the generic path; the tensor-core sweep has its own filtered
+// version of the same arithmetic).
 template <int N>
-__device__ __forceinline__ void acc_update_sample(RowAcc& a, const float (&z)[N], const float (&t)[N],
-                                                  const int (&col)[N], const bool (&valid)[N]) {
+__device__ __forceinline__ void acc_update_exact(RowAcc& a, const float (&y)[N], const uint32_t (&word)[N],
+                                                 const int (&col)[N], const bool (&valid)[N]) {
     float mt = -INFINITY;
 #pragma unroll
     for (int i = 0; i < N; ++i)
-        if (valid[i]) mt = fmaxf(mt, z[i]);
+        if (valid[i]) mt = fmaxf(mt, y[i]);
     if (mt == -INFINITY) return;
-    float w[N];
     float st = 0.f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        w[i] = valid[i] ? ex2_approx((z[i] - mt) * kLog2e) : 0.f;
-        st += w[i];
-    }
-    if (mt > a.m) {
-        a.s = a.s * (double)ex2_approx((a.m - mt) * kLog2e) + (double)st;
-        a.m = mt;
-    } else {
-        a.s += (double)st * (double)ex2_approx((mt - a.m) * kLog2e);
-    }
-    float c = (a.kb == -INFINITY) ? INFINITY : ex2_approx((mt - a.kb) * kLog2e) * kRaceSafety;
+    for (int i = 0; i < N; ++i)
+        if (valid[i]) st += ex2_approx(y[i] - mt);
+    acc_add_mass(a, mt, st);
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        if (valid[i] && (a.kb == -INFINITY || t[i] < w[i] * c)) {
-            const float key = race_key(z[i], t[i]);
-            if (key_better(key, col[i], a.kb, a.ib)) {
-                a.kb = key;
-                a.zb = z[i];
-                a.ib = col[i];
-                c = ex2_approx((mt - a.kb) * kLog2e) * kRaceSafety;
-            }
-        }
-    }
+    for (int i = 0; i < N; ++i)
+        if (valid[i]) acc_take(a, race_key2(y[i], word[i]), y[i], col[i]);
 }
 
 // Greedy update (T = 0): the key is the logit itself.
@@ -143,11 +132,7 @@ __device__ __forceinline__ void acc_update_greedy(RowAcc& a, const float (&y)[N]
                                                   const bool (&valid)[N]) {
 #pragma unroll
     for (int i = 0; i < N; ++i)
-        if (valid[i] && key_better(y[i], col[i], a.kb, a.ib)) {
-            a.kb = y[i];
-            a.zb = y[i];
-            a.ib = col[i];
-        }
+        if (valid[i]) acc_take(a, y[i], y[i], col[i]);
 }
 
 }  // namespace dspark

@@ -31,15 +31,16 @@ def test_philox_known_answers():
     assert n == 3
 
 
-def test_uniform_range_exact_in_float32():
+def test_uniform_range_and_resolution():
+    """u = (w + 1/2) 2^-32: strictly inside (0, 1), symmetric, exact in double."""
     lo = oracle.uniform(0)
     hi = oracle.uniform(0xFFFFFFFF)
-    assert lo == 2.0 ** -24 and hi == 1.0 - 2.0 ** -24
+    assert lo == 2.0 ** -33 and hi == 1.0 - 2.0 ** -33
     rng = np.random.default_rng(1)
     for w in rng.integers(0, 2 ** 32, size=2000, dtype=np.uint64):
         u = oracle.uniform(int(w))
         assert 0.0 < u < 1.0
-        assert float(np.float32(u)) == u      # exactly representable in fp32
+        assert u + oracle.uniform(int(w) ^ 0xFFFFFFFF) == 1.0      # 1 - u is the complement word
 
 
 def test_rng_stream_layout():
