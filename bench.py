@@ -271,6 +271,8 @@ def main(argv=None):
         e[0] += 1
         e[1] += ms
     n_rej = float(np.mean([int((o[0] < w.gamma).sum().item()) for o in outs]))
+    sweeps = [ms for name, ms in launches if name.startswith("draft_sweep")]
+    sweep_by_k = [round(float(np.mean(sweeps[k::w.gamma])), 4) for k in range(w.gamma)] if sweeps else None
     ab = algorithmic_bytes(w, n_rej, w.R * (w.gamma + 1))
     hbm_peak, bf16_peak, peak_src = _peaks()
     dom = max(table.items(), key=lambda kv: kv[1][1])
@@ -347,6 +349,7 @@ def main(argv=None):
                       "hbm_frac": round(cycle_gbs / hbm_peak, 4) if cycle_gbs else None,
                       "rejecting_requests_per_step": n_rej},
             "kernels": kernels,
+            "draft_sweep_ms_by_position": sweep_by_k,
             "gpu_launches": len(launches),
             "clocks": clk,
             "wall_s_timed": round(t_wall, 3),

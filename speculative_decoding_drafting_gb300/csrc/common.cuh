@@ -60,6 +60,35 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
     return c;
 }
 
+// Philox4x32-10 with the ten round keys precomputed (kernel parameters live in
+// the constant bank, so the rounds need no key arithmetic).
+struct PhiloxSchedule {
+    uint32_t k[20];   // (k0, k1) of rounds 0..9
+};
+
+__host__ __device__ __forceinline__ PhiloxSchedule philox_schedule(uint64_t seed) {
+    PhiloxSchedule s;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int i = 0; i < 10; ++i) {
+        s.k[2 * i] = k0;
+        s.k[2 * i + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return s;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxSchedule& ks) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint64_t p0 = mul_wide_u32(0xD2511F53u, c.x);
+        const uint64_t p1 = mul_wide_u32(0xCD9E8D57u, c.z);
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ ks.k[2 * i], (uint32_t)p1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ ks.k[2 * i + 1], (uint32_t)p0);
+    }
+    return c;
+}
+
 // u = (w + 1/2) 2^-32 in (0, 1), exact in double.
 __device__ __forceinline__ double word_to_uniform_d(uint32_t w) {
     return ((double)w + 0.5) * (1.0 / 4294967296.0);
@@ -91,13 +120,37 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// E = -ln(1 - t) for t in (0, 1) with small relative error everywhere: the
+// Maclaurin series t + t^2/2 + ... + t^9/9 below t = 1/4 (truncation below
+// t^9/10 < 4e-7 relative), the hardware base-2 logarithm of 1 - t above it
+// (|log2(1 - t)| >= 0.41 there, so its absolute error stays relative-small).
+__device__ __forceinline__ float neg_log1m(float t) {
+    if (t < 0.25f) {
+        float p = 1.f / 9.f;
+        p = fmaf(p, t, 1.f / 8.f);
+        p = fmaf(p, t, 1.f / 7.f);
+        p = fmaf(p, t, 1.f / 6.f);
+        p = fmaf(p, t, 1.f / 5.f);
+        p = fmaf(p, t, 1.f / 4.f);
+        p = fmaf(p, t, 1.f / 3.f);
+        p = fmaf(p, t, 1.f / 2.f);
+        p = fmaf(p, t, 1.f);
+        return p * t;
+    }
+    return -kLn2 * lg2_approx(1.f - t);
+}
+
 // Gumbel-max key in base-2 units.  With y = z log2(e) the tempered logit in
-// bits and t = 1 - u, E = -ln u = -log1p(-t) is an Exp(1) variate and
+// bits and t = 1 - u, E = -ln u = -ln(1 - t) is an Exp(1) variate and
 // z + G = z - ln E (G = -ln(-ln u)); in bits the key is y - log2(E).
 __device__ __forceinline__ float race_key2(float y, uint32_t word) {
-    const float t = word_to_t(word);
-    const float E = -log1pf(-t);
-    return y - log2f(E);
+    return y - lg2_approx(neg_log1m(word_to_t(word)));
 }
 
 // ---------------------------------------------------------------- loads

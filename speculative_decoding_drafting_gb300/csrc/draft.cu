@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(256) draft_prep_markov(DraftArgs A, int k) {
         x = finish_step(A, r, k - 1, p);
     }
     if (k > A.gamma) return;
+    if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
     for (int i = threadIdx.x; i < A.r; i += blockDim.x)
         store_code(A, r, k, i, ld_elem(A.W1, A.w_dtype, (size_t)x * A.r + i));
 }
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(256) draft_prep_rnn(DraftArgs A, int k) {
             for (int i = threadIdx.x; i < rr; i += blockDim.x) A.state_out[(size_t)r * rr + i] = srow[i];
         return;
     }
+    if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
     const int Kin = 2 * rr + A.d;
     for (int i = threadIdx.x; i < rr; i += blockDim.x) {
         zin[i] = (k == 1) ? 0.f : srow[i];
@@ -256,6 +258,7 @@ size_t draft_workspace_bytes(int R, int gamma, int V, int r, int d) {
     off = align_up(off + 2ull * R * ns_max * sizeof(DraftPartial), 256);
     off = align_up(off + 2ull * R * r * sizeof(uint16_t), 256);
     off = align_up(off + (size_t)R * r * sizeof(float), 256);
+    off = align_up(off + (size_t)R * sizeof(uint32_t), 256);
     return off;
 }
 
@@ -272,6 +275,8 @@ int draft_carve(DraftArgs& a, size_t ws_bytes) {
     a.ebf = reinterpret_cast<uint16_t*>(base + off);
     off = align_up(off + 2ull * a.R * a.r * sizeof(uint16_t), 256);
     a.rnn_state = reinterpret_cast<float*>(base + off);
+    off = align_up(off + (size_t)a.R * a.r * sizeof(float), 256);
+    a.best = reinterpret_cast<uint32_t*>(base + off);
     return DSPARK_OK;
 }
 

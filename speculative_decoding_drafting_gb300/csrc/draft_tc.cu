@@ -32,35 +32,38 @@ namespace {
 
 constexpr int kBM = 128;           // requests per CTA (one M-group)
 constexpr int kBN = 64;            // vocabulary columns per tile
-constexpr int kNB = 2;             // W2 stages
+constexpr int kNB = 8;             // W2 stages, each 64 columns x 64 rows of r (8 KB)
 constexpr int kNU = 3;             // U stages
 constexpr int kNACC = 2;           // TMEM accumulators
 constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 16 of a tile's 64 columns
 constexpr int kEpiWarps = 4 * kEpiWG;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarp0 = 3;       // warps 0..2: U producer, MMA issuer, W2 producer
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr uint32_t kTmemCols = 128;
 constexpr int kUStageBytes = kBM * kBN * 4;   // 32 KB (f32); bf16 uses half
+constexpr int kPfTiles = 4;        // tiles covered by one L2 prefetch box (256 columns)
 // Margin on the candidate test; the exact key decides, the test only has to
 // stay conservative against the rounding of w and 2^(m_t - kthr).
 constexpr float kRaceSafety = 1.0009765625f;   // 1 + 2^-10
 
-// Order-preserving map of float keys to unsigned (for atomicMax in shared memory).
-__device__ __forceinline__ uint32_t key_order(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_from_order(uint32_t e) {
-    return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
+__device__ __forceinline__ void acc_take_inline(float& kb, float& zb, int& ib, float key, float y, int col) {
+    if (key_better(key, col, kb, ib)) {
+        kb = key;
+        zb = y;
+        ib = col;
+    }
 }
 
 struct TcParams {
     DraftPartial* parts;     // this step's partial buffer [R][n_slices]
+    uint32_t* best;          // [R] best race key so far in this step, shared by every CTA
     const uint32_t* req_ids;
     void* ws;
     int R, V, r, k;          // k = 1-based step
     int ntiles, nslices;
     float c2;                // log2(e) / T
-    uint64_t seed;
+    int pf_dist;             // L2 prefetch distance in tiles (0 = off)
+    PhiloxSchedule ks;
 };
 
 struct Smem {
@@ -76,11 +79,10 @@ struct Smem {
     uint64_t* acc_empty;
     uint32_t* tmem_holder;
     int* abort_flag;
-    uint32_t* best;          // [128] best race key seen so far per row (order-preserving bits)
 };
 
 __host__ __device__ constexpr size_t smem_bytes_for(int r) {
-    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * r * 128 + (size_t)kNU * kUStageBytes + 256 + 512;
+    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * 8192 + (size_t)kNU * kUStageBytes + 256;
 }
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
@@ -88,7 +90,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.A = base;
     s.B = s.A + (size_t)(r / 64) * 16384;
-    s.U = s.B + (size_t)kNB * r * 128;
+    s.U = s.B + (size_t)kNB * 8192;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.U + (size_t)kNU * kUStageBytes);
     s.a_full = bars;
     s.b_full = bars + 1;
@@ -99,14 +101,13 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
     s.acc_empty = s.acc_full + kNACC;
     s.tmem_holder = reinterpret_cast<uint32_t*>(s.acc_empty + kNACC);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
-    s.best = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) + 256);
     return s;
 }
 
 template <int UT, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_sweep_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmU, TcParams p) {
+                   const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmUP, TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw, p.r);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.acc_empty[i], kEpiWarps);
         }
         *S.abort_flag = 0;
-        for (int i = 0; i < kBM; ++i) S.best[i] = key_order(-INFINITY);
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -146,23 +146,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- producer
+            // ---------------- U producer: runs up to kNU tiles ahead
             const uint64_t pol_first = policy_evict_first();
-            const uint64_t pol_last = policy_evict_last();
-            mbar_expect_tx(S.a_full, (uint32_t)kblocks * 16384u);
-            for (int kb = 0; kb < kblocks; ++kb)
-                tma_load_2d(S.A + kb * 16384, &tmA, S.a_full, kb * 64, mg * kBM, pol_last);
             const uint32_t ubytes = UT == DSPARK_F32 ? (uint32_t)kUStageBytes : (uint32_t)(kUStageBytes / 2);
             int issued = 0;
+            if (p.pf_dist > 0)   // warm L2 with the first rows of the slice in 1 KB runs
+                for (int t = 0; t < p.pf_dist && t < nt; t += kPfTiles)
+                    tma_prefetch_3d(&tmUP, (t_begin + t) * kBN, p.k - 1, mg * kBM);
             for (int t = 0; t < nt; ++t) {
                 const int v0 = (t_begin + t) * kBN;
-                const int bs = t % kNB;
-                const uint32_t bph = (uint32_t)(t / kNB) & 1u;
-                if (!mbar_wait(&S.b_empty[bs], bph ^ 1u, abort_flag)) break;
-                mbar_expect_tx(&S.b_full[bs], (uint32_t)p.r * 128u);
-                tma_load_2d(S.B + (size_t)bs * p.r * 128, &tmB, &S.b_full[bs], v0, 0, pol_last);
                 const int us = t % kNU;
                 const uint32_t uph = (uint32_t)(t / kNU) & 1u;
+                if (p.pf_dist > 0 && (t % kPfTiles) == 0 && t + p.pf_dist < nt)
+                    tma_prefetch_3d(&tmUP, (t_begin + t + p.pf_dist) * kBN, p.k - 1, mg * kBM);
                 if (!mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&S.u_full[us], ubytes);
                 uint8_t* dst = S.U + (size_t)us * kUStageBytes;
@@ -174,13 +170,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 issued = t + 1;
             }
-            if (*abort_flag) {
-                // wind down: let the copies this thread issued land before exit
-                mbar_wait_for(S.a_full, 0, kWaitLimitNs);
-                for (int t = (issued > kNU ? issued - kNU : 0); t < issued; ++t) {
-                    mbar_wait_for(&S.b_full[t % kNB], (uint32_t)(t / kNB) & 1u, kWaitLimitNs);
+            if (*abort_flag)   // wind down: let the copies this thread issued land
+                for (int t = (issued > kNU ? issued - kNU : 0); t < issued; ++t)
                     mbar_wait_for(&S.u_full[t % kNU], (uint32_t)(t / kNU) & 1u, kWaitLimitNs);
-                }
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ---------------- A and W2 producer
+            const uint64_t pol_last = policy_evict_last();
+            mbar_expect_tx(S.a_full, (uint32_t)kblocks * 16384u);
+            for (int kb = 0; kb < kblocks; ++kb)
+                tma_load_2d(S.A + kb * 16384, &tmA, S.a_full, kb * 64, mg * kBM, pol_last);
+            int issued = 0;
+            for (int g = 0; g < nt * kblocks; ++g) {
+                const int t = g / kblocks, kb = g - t * kblocks;
+                const int bs = g % kNB;
+                const uint32_t bph = (uint32_t)(g / kNB) & 1u;
+                if (!mbar_wait(&S.b_empty[bs], bph ^ 1u, abort_flag)) break;
+                mbar_expect_tx(&S.b_full[bs], 8192u);
+                tma_load_2d(S.B + (size_t)bs * 8192, &tmB, &S.b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
+                issued = g + 1;
+            }
+            if (*abort_flag) {
+                mbar_wait_for(S.a_full, 0, kWaitLimitNs);
+                for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
+                    mbar_wait_for(&S.b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
@@ -190,49 +204,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(S.a_full, 0, abort_flag);
             tc_fence_after();
             for (int t = 0; ok && t < nt; ++t) {
-                const int bs = t % kNB;
-                const uint32_t bph = (uint32_t)(t / kNB) & 1u;
                 const int buf = t % kNACC;
                 const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
                 if (!mbar_wait(&S.acc_empty[buf], aph ^ 1u, abort_flag)) break;
-                if (!mbar_wait(&S.b_full[bs], bph, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
-                const uint8_t* bstage = S.B + (size_t)bs * p.r * 128;
-                for (int kk = 0; kk < p.r / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(S.A + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
-                    umma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                for (int kb = 0; ok && kb < kblocks; ++kb) {
+                    const int g = t * kblocks + kb;
+                    const int bs = g % kNB;
+                    const uint32_t bph = (uint32_t)(g / kNB) & 1u;
+                    if (!mbar_wait(&S.b_full[bs], bph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* bstage = S.B + (size_t)bs * 8192;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(S.A + kb * 16384 + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
+                        umma_bf16(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                    }
+                    umma_commit(&S.b_empty[bs]);
                 }
-                umma_commit(&S.b_empty[bs]);
+                if (!ok) break;
                 umma_commit(&S.acc_full[buf]);
             }
         }
     } else {
         // ---------------- epilogue: thread = (request row, 16-column quarter of each tile)
-        const int wg = (warp - 2) >> 2;              // column quarter
+        const int wg = (warp - kEpiWarp0) >> 2;      // column quarter
         const int q = warp & 3;                      // TMEM lane quarter of this warp
         const int rit = q * 32 + lane;               // row inside the tile
         const int row = mg * kBM + rit;
         const bool row_ok = row < p.R;
         const uint32_t req = row_ok ? (p.req_ids ? p.req_ids[row] : (uint32_t)row) : 0u;
-        const PhiloxKey key = philox_key(p.seed);
-        RowAcc acc;
-        acc_init(acc);
+        const uint32_t* gbest = p.best + (row_ok ? row : 0);
+        // running state: log-sum-exp mass in float against a reference max
+        // (folded into double at the end), race winner
+        float m = -INFINITY, s32 = 0.f;
+        float kb = -INFINITY, zb = 0.f;
+        int ib = INT_MAX;
+        // the best key any CTA has found for this row (a lower bound on the
+        // winner's), read one tile ahead so the L2 round trip stays hidden
+        uint32_t gnext = GREEDY ? kOrderNegInf : ld_relaxed_gpu(gbest);
         for (int t = 0; t < nt; ++t) {
             const int v0 = (t_begin + t) * kBN + wg * 16;
             const int buf = t % kNACC;
             const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
             const int us = t % kNU;
             const uint32_t uph = (uint32_t)(t / kNU) & 1u;
+            const uint32_t gcur = gnext;
+            if (!GREEDY && t + 1 < nt) gnext = ld_relaxed_gpu(gbest);
+            const float kglob = key_from_order(gcur);
             bool ready = mbar_wait(&S.acc_full[buf], aph, abort_flag);
             ready = ready && mbar_wait(&S.u_full[us], uph, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
             tc_fence_after();
             __syncwarp();
-            float a[16];
-            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), a);
             float y[16];
+            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), y);
             const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
             if (UT == DSPARK_F32) {
                 const uint8_t* rowp = ust + (wg >> 1) * (kUStageBytes / 2) + rit * 128;
@@ -240,10 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) {
                     const float4 f =
                         *reinterpret_cast<const float4*>(rowp + ((((wg & 1) * 4 + c) ^ (rit & 7)) << 4));
-                    y[4 * c + 0] = a[4 * c + 0] + f.x;
-                    y[4 * c + 1] = a[4 * c + 1] + f.y;
-                    y[4 * c + 2] = a[4 * c + 2] + f.z;
-                    y[4 * c + 3] = a[4 * c + 3] + f.w;
+                    y[4 * c + 0] += f.x;
+                    y[4 * c + 1] += f.y;
+                    y[4 * c + 2] += f.z;
+                    y[4 * c + 3] += f.w;
                 }
             } else {
                 const uint8_t* rowp = ust + rit * 128;
@@ -253,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        y[8 * c + 2 * e + 0] = a[8 * c + 2 * e + 0] + bf16_bits_to_float(w4[e] & 0xFFFFu);
-                        y[8 * c + 2 * e + 1] = a[8 * c + 2 * e + 1] + bf16_bits_to_float(w4[e] >> 16);
+                        y[8 * c + 2 * e + 0] += bf16_bits_to_float(w4[e] & 0xFFFFu);
+                        y[8 * c + 2 * e + 1] += bf16_bits_to_float(w4[e] >> 16);
                     }
                 }
             }
@@ -265,91 +296,126 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&S.acc_empty[buf]);
                 mbar_arrive(&S.u_empty[us]);
             }
-            if (GREEDY) {
-                int col[16];
-                bool ok[16];
+            if (!(row_ok && v0 + 16 <= p.V)) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    col[i] = v0 + i;
-                    ok[i] = row_ok && col[i] < p.V;
-                }
-                acc_update_greedy<16>(acc, y, col, ok);
+                for (int i = 0; i < 16; ++i)
+                    if (!(row_ok && v0 + i < p.V)) y[i] = -INFINITY;     // edge of the vocabulary
+            }
+            if (GREEDY) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (y[i] > kb) {          // columns rise along the thread: first max wins ties
+                        kb = y[i];
+                        ib = v0 + i;
+                    }
                 continue;
             }
-            uint32_t vmask = 0;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                y[i] *= p.c2;                                   // tempered logit in bits
-                const bool ok = row_ok && (v0 + i) < p.V;
-                vmask |= ok ? (1u << i) : 0u;
-                if (ok) mt = fmaxf(mt, y[i]);
-            }
-            if (!__any_sync(0xffffffffu, vmask)) continue;
+            // y holds z = U + B here; the race and the mass work in bits (y c2).
+            // The mass is summed against a per-row reference m (the first chunk's
+            // maximum), so the common path needs no per-chunk maximum.
+            if (!__any_sync(0xffffffffu, row_ok && v0 < p.V)) continue;
             uint32_t word[16];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(v0 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), key);
+                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(v0 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), p.ks);
                 word[4 * g + 0] = w4.x;
                 word[4 * g + 1] = w4.y;
                 word[4 * g + 2] = w4.z;
                 word[4 * g + 3] = w4.w;
             }
-            uint32_t cand = 0;
-            if (vmask) {
-                float w[16];
+            if (m == -INFINITY) {
+                // first chunk of this thread: reference = the chunk's maximum (if any column is valid)
+                float zt = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
+                m = zt * p.c2;
+            }
+            float kthr = fmaxf(kb, kglob);
+            bool any = false;
+            if (m != -INFINITY) {
+                const float nm = -m;
+                if (kthr == -INFINITY) {
+                    // nothing known for this row yet (every lane is in its first chunk):
+                    // exact keys for the whole chunk give a strong starting threshold
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (y[i] != -INFINITY) acc_take_inline(kb, zb, ib, race_key2(y[i] * p.c2, word[i]), y[i] * p.c2, v0 + i);
+                    if (kb != -INFINITY) atomicMax(p.best + row, key_order(kb));
+                    float st = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, nm));
+                    s32 += st;
+                    continue;
+                }
+                // an element can beat kthr only if t < 2^(y - kthr) (its key is at most
+                // y - log2 t); with f = 1 + t_lower in [1, 2): candidate iff
+                // f < 1 + 2^(y - m) 2^(m - kthr)
+                const float cthr = ex2_approx(m - kthr) * kRaceSafety;
                 float st = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    w[i] = (vmask >> i & 1u) ? ex2_approx(y[i] - mt) : 0.f;
-                    st += w[i];
+                    const float w = ex2_approx(fmaf(y[i], p.c2, nm));
+                    st += w;
+                    const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
+                    any = (f < fmaf(w, cthr, 1.f)) | any;
                 }
-                acc_add_mass(acc, mt, st);
-                float kthr = fmaxf(acc.kb, key_from_order(S.best[rit]));
-                if (kthr == -INFINITY) {
-                    // first chunk of the row: seed the race with the largest logit
-                    int istar = 0;
-                    uint32_t wstar = word[0];
+                if (!(st <= 1.0e30f)) {
+                    // a column far above the reference: move the reference up and redo the sums
+                    float zt = -INFINITY;
 #pragma unroll
-                    for (int i = 15; i >= 0; --i)
-                        if ((vmask >> i & 1u) && y[i] == mt) {
-                            istar = i;
-                            wstar = word[i];
-                        }
-                    acc_take(acc, race_key2(mt, wstar), mt, v0 + istar);
-                    atomicMax(&S.best[rit], key_order(acc.kb));
-                    kthr = acc.kb;
+                    for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
+                    const float mt = zt * p.c2;
+                    st = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, -mt));
+                    s32 = fmaf(s32, ex2_approx(m - mt), st);
+                    m = mt;
+                    any = true;
+                } else {
+                    s32 += st;
                 }
-                // candidate iff its key can exceed kthr: key <= y - log2(t), t >= t_lower
-                const float cthr = ex2_approx(mt - kthr) * kRaceSafety;
+                if (any) {
+                    // exact keys of the candidates, one per round
+                    const float nm2 = -m;
+                    const float cthr2 = ex2_approx(m - kthr) * kRaceSafety;
+                    uint32_t cand = 0;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    cand |= ((vmask >> i & 1u) && word_to_t_lower(word[i]) < w[i] * cthr) ? (1u << i) : 0u;
-            }
-            // exact keys of the candidates; lanes without any wait
-            while (__any_sync(0xffffffffu, cand)) {
-                if (cand) {
-                    const int i = __ffs(cand) - 1;
-                    cand &= cand - 1;
-                    float yi = y[0];
-                    uint32_t wi = word[0];
-#pragma unroll
-                    for (int j = 1; j < 16; ++j) {
-                        yi = (i == j) ? y[j] : yi;
-                        wi = (i == j) ? word[j] : wi;
+                    for (int i = 0; i < 16; ++i) {
+                        const float w = ex2_approx(fmaf(y[i], p.c2, nm2));
+                        const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
+                        cand |= (f < fmaf(w, cthr2, 1.f)) ? (1u << i) : 0u;
                     }
-                    const float kk = race_key2(yi, wi);
-                    if (key_better(kk, v0 + i, acc.kb, acc.ib)) {
-                        acc.kb = kk;
-                        acc.zb = yi;
-                        acc.ib = v0 + i;
-                        atomicMax(&S.best[rit], key_order(kk));
+                    while (cand) {
+                        const int i = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        float zi = y[0];
+                        uint32_t wi = word[0];
+#pragma unroll
+                        for (int j = 1; j < 16; ++j) {
+                            zi = (i == j) ? y[j] : zi;
+                            wi = (i == j) ? word[j] : wi;
+                        }
+                        const float yi = zi * p.c2;
+                        const float kk = race_key2(yi, wi);
+                        if (key_better(kk, v0 + i, kb, ib)) {
+                            kb = kk;
+                            zb = yi;
+                            ib = v0 + i;
+                            if (kk > kglob) atomicMax(p.best + row, key_order(kk));
+                        }
                     }
                 }
             }
         }
-        if (row_ok && !*abort_flag)
-            p.parts[((size_t)row * p.nslices + slice) * kEpiWG + wg] = acc_to_partial(acc);
+        if (row_ok && !*abort_flag) {
+            DraftPartial part;
+            part.m = m;
+            part.s = (double)s32;
+            part.kb = kb;
+            part.zb = GREEDY ? kb : zb;
+            part.ib = ib;
+            p.parts[((size_t)row * p.nslices + slice) * kEpiWG + wg] = part;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -379,12 +445,13 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const cuuint64_t* dims,
-              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+              const cuuint64_t* strides_bytes, const cuuint32_t* box,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt, (cuuint32_t)rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -413,7 +480,7 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
         cuuint64_t str[1] = {(cuuint64_t)a.V * 2};
-        cuuint32_t box[2] = {kBN, (cuuint32_t)a.r};
+        cuuint32_t box[2] = {kBN, 64};
         if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
             return cudaErrorInvalidValue;
     }
@@ -427,8 +494,21 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
                       3, const_cast<void*>(a.U), dims, str, box))
             return cudaErrorInvalidValue;
     }
+    // U again, as 256-column boxes, for L2 prefetches in long row runs
+    CUtensorMap tmUP;
+    {
+        const size_t es = UT == DSPARK_F32 ? 4 : 2;
+        cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
+        cuuint64_t str[2] = {(cuuint64_t)a.V * es, (cuuint64_t)a.gamma * a.V * es};
+        cuuint32_t box[3] = {(cuuint32_t)(kPfTiles * kBN), 1u, (cuuint32_t)kBM};
+        if (!make_map(&tmUP, UT == DSPARK_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      3, const_cast<void*>(a.U), dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     TcParams p;
+    p.pf_dist = 8;
     p.parts = a.parts + (size_t)(k & 1) * a.parts_stride;
+    p.best = a.best;
     p.req_ids = a.req_ids;
     p.ws = a.ws;
     p.R = a.R;
@@ -438,14 +518,14 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.ntiles = (a.V + kBN - 1) / kBN;
     p.nslices = a.n_slices / kEpiWG;
     p.c2 = a.T > 0.f ? kLog2e / a.T : 1.f;
-    p.seed = a.seed;
+    p.ks = philox_schedule(a.seed);
     const size_t smem = smem_bytes_for(a.r);
     auto kern = draft_sweep_tc<UT, GREEDY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_slices / kEpiWG, (a.R + kBM - 1) / kBM);
     prof_begin(kPDraftSweepTc, s);
-    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmU, p);
+    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmU, tmUP, p);
     prof_end(s);
     return cudaGetLastError();
 }

@@ -40,6 +40,7 @@ struct DraftArgs {
     DraftPartial* parts;      // [2][R][n_slices]
     uint16_t* ebf;            // [2][R][r] bf16 bits (hi, lo) of e_k
     float* rnn_state;         // [R][r]
+    uint32_t* best;           // [R] best race key of the current step (order-preserving bits)
     int rnn;                  // 1 for the RNN head
     int n_slices;             // V-slices per request in the active sweep
     int parts_stride;         // R * n_slices_max

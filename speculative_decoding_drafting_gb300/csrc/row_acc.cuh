@@ -17,6 +17,16 @@
 
 namespace dspark {
 
+// Order-preserving map of float keys to unsigned (atomicMax on keys).
+__device__ __forceinline__ uint32_t key_order(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_from_order(uint32_t e) {
+    return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
+}
+constexpr uint32_t kOrderNegInf = 0x007FFFFFu;   // key_order(-inf)
+
 struct RowAcc {
     float m;
     float kb;
