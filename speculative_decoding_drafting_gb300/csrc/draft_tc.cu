@@ -532,6 +532,13 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
 
 }  // namespace
 
+bool draft_tc_encode_available() { return encode_fn() != nullptr; }
+
+bool draft_tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const cuuint64_t* dims,
+                       const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    return make_map(m, dt, rank, base, dims, strides_bytes, box);
+}
+
 bool draft_tc_supported(const DraftArgs& a) {
     if (a.rnn) return false;                       // e_k = tanh(out) is not bf16-exact
     if (a.w_dtype != DSPARK_BF16) return false;

@@ -72,12 +72,20 @@ struct VerifyArgs {
     float2* vparts;     // [R][gamma+1][NCH]  (m, s) or (max, idx bits)
     double* lsep_ws;    // [R][gamma+1]
     int2* vstate;       // [R] (mode, position)
-    double* rmass;      // [R][NCH]
-    int nch;            // number of 1024-wide chunks of V
+    int nch;            // number of 1024-wide chunks of V (target-row partials)
+    int nch256;         // number of 256-wide chunks of V (residual masses)
+    float* rpart;       // [R][nch256][4] partial residual masses
+    int* rej_count;     // number of requests that rejected a draft
+    int* rej_list;      // [R] those requests, in arrival order
+    uint16_t* a_res;    // [R][r] bf16 codes e_j of the rejecting requests (compact order)
+    uint32_t* vflags;   // bit 0: some rejecting code is not bf16-exact
+    int tc;             // 1 if the tensor-core residual pass is launched
 };
 
-constexpr int kChunk = 1024;          // leaf chunk of the sampling tree
+constexpr int kChunk = 1024;          // chunk of the target-row partials (bonus draws)
 constexpr int kChunkLog2 = 10;
+constexpr int kRChunk = 256;          // chunk of the residual masses
+constexpr int kRChunkLog2 = 8;
 constexpr int kGenericSlice = 4096;   // V-slice of the generic draft sweep
 
 enum VerifyMode : int { kModeDone = 0, kModeResidual = 1, kModeBonus = 2 };

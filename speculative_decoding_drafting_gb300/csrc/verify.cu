@@ -30,6 +30,14 @@ namespace dspark {
 bool verify_tc_supported(const VerifyArgs& a);
 cudaError_t launch_verify_tc_residual(VerifyArgs& a, cudaStream_t s);
 
+// exp(a) for a double argument without double-precision transcendentals:
+// exp(a_hi) in float times the first-order correction for a - a_hi
+// (relative error about 1e-7 for |a| < 80).
+__device__ __forceinline__ double exp_from_double(double a) {
+    const float ah = (float)a;
+    return (double)expf(ah) * (1.0 + (a - (double)ah));
+}
+
 __device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
     if (!A.verify_len) return A.gamma;
     int L = A.verify_len[r];
@@ -39,6 +47,10 @@ __device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
 // ------------------------------------------------------------------ pass 1
 template <int PT, bool GREEDY>
 __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {   // the accept pass appends to these
+        *A.rej_count = 0;
+        *A.vflags = 0u;
+    }
     const int lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (blockDim.x >> 5);
     const int V = A.V, G1 = A.gamma + 1, NCH = A.nch;
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
         double s = 0.0;
         for (int c = lane; c < NCH; c += 32) {
             const float2 p = parts[(size_t)row * NCH + c];
-            s += (double)p.y * exp((double)p.x - (double)m);
+            s += (double)p.y * (double)expf(p.x - m);      // exact difference: both are float maxima
         }
         s = warp_sum_d(s);
         const double l = (double)m + log(s);
@@ -190,87 +202,119 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
         }
     }
     __syncwarp();
-    if (lane != 0) return;
-    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
-    const PhiloxKey key = philox_key(A.seed);
     int j = 0;
-    for (int k = 1; k <= L; ++k) {
-        int x = A.tokens[(size_t)r * A.gamma + (k - 1)];
-        if (x < 0 || x >= V) {
-            raise_status(A.ws, kStatBadToken);
-            x = 0;
+    if (lane == 0) {
+        const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+        const PhiloxKey key = philox_key(A.seed);
+        for (int k = 1; k <= L; ++k) {
+            int x = A.tokens[(size_t)r * A.gamma + (k - 1)];
+            if (x < 0 || x >= V) {
+                raise_status(A.ws, kStatBadToken);
+                x = 0;
+            }
+            const size_t prow = ((size_t)r * G1 + (k - 1)) * (size_t)V;
+            // p(x) = exp(P_x / T - lse_P), with the difference formed in double
+            const double px = exp_from_double((double)ld_elem(A.P, PT, prow + x) * (double)invT - lsep[k - 1]);
+            if (A.p_tok) A.p_tok[(size_t)r * A.gamma + (k - 1)] = (float)px;
+            const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + (k - 1)];
+            const double u = rng_uniform_d(key, req, (uint32_t)k, 1u, 0u);
+            if (u < ratio) {
+                out[k - 1] = x;
+            } else {
+                j = k;
+                break;
+            }
         }
-        const size_t prow = ((size_t)r * G1 + (k - 1)) * (size_t)V;
-        const double px = exp((double)ld_elem(A.P, PT, prow + x) * (double)invT - lsep[k - 1]);
-        if (A.p_tok) A.p_tok[(size_t)r * A.gamma + (k - 1)] = (float)px;
-        const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + (k - 1)];
-        const double u = rng_uniform_d(key, req, (uint32_t)k, 1u, 0u);
-        if (u < ratio) {
-            out[k - 1] = x;
+        if (j) {
+            A.vstate[r] = make_int2(kModeResidual, j);
+            A.accept_len[r] = j - 1;
         } else {
-            j = k;
-            break;
+            A.vstate[r] = make_int2(kModeBonus, L + 1);
+            A.accept_len[r] = L;
         }
+        A.n_out[r] = A.accept_len[r] + 1;
     }
-    if (j) {
-        A.vstate[r] = make_int2(kModeResidual, j);
-        A.accept_len[r] = j - 1;
-    } else {
-        A.vstate[r] = make_int2(kModeBonus, L + 1);
-        A.accept_len[r] = L;
+    j = __shfl_sync(0xffffffffu, j, 0);
+    if (!j) return;
+    // queue the rejecting request for the residual pass with its code e_j in bf16
+    int slot = 0;
+    if (lane == 0) {
+        slot = atomicAdd(A.rej_count, 1);
+        A.rej_list[slot] = r;
     }
-    A.n_out[r] = A.accept_len[r] + 1;
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    const float* e = A.code + ((size_t)r * A.gamma + (j - 1)) * A.r;
+    bool inexact = false;
+    for (int i = lane; i < A.r; i += 32) {
+        const float v = e[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        A.a_res[(size_t)slot * A.r + i] = __bfloat16_as_ushort(h);
+        inexact |= __bfloat162float(h) != v;
+    }
+    if (__any_sync(0xffffffffu, inexact) && lane == 0) atomicOr(A.vflags, 1u);
 }
 
 // ------------------------------------------------------------------ residual (generic)
-// One CTA per (chunk, request); q_j rebuilt with B = e_j W2 on CUDA cores.
+// Rejecting requests only: w = max(p_j - q_j, 0) over the row, with
+// B = e_j W2 on CUDA cores.  One CTA task = (1024 columns, request); the mass
+// of each 256-column chunk goes to rpart[r][c][0].  When the tensor-core pass
+// ran and every code was bf16-exact, this kernel has nothing to do.
 template <int PT, int UT, int WT>
 __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
+    if (A.tc && !(*A.vflags & 1u)) return;
     extern __shared__ float e_sh[];
-    const int ch = blockIdx.x, r = blockIdx.y;
-    const int2 st = A.vstate[r];
-    if (st.x != kModeResidual) return;
-    const int j = st.y, V = A.V, G1 = A.gamma + 1;
-    for (int i = threadIdx.x; i < A.r; i += blockDim.x)
-        e_sh[i] = A.code[((size_t)r * A.gamma + (j - 1)) * A.r + i];
-    __syncthreads();
-    const int c = ch * kChunk + 4 * threadIdx.x;
-    double wsum = 0.0;
-    if (c < V) {
-        float b[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = 0; i < A.r; ++i) {
-            const float4 w = load4<WT>(A.W2, (size_t)i * V + c);
-            const float ei = e_sh[i];
-            b[0] = fmaf(ei, w.x, b[0]);
-            b[1] = fmaf(ei, w.y, b[1]);
-            b[2] = fmaf(ei, w.z, b[2]);
-            b[3] = fmaf(ei, w.w, b[3]);
-        }
-        const float invT = 1.f / A.T;
-        const double lq = A.lse[(size_t)r * A.gamma + (j - 1)];
-        const double lp = A.lsep_ws[(size_t)r * G1 + (j - 1)];
-        const float lq_hi = (float)lq, lq_lo = (float)(lq - (double)lq_hi);
-        const float lp_hi = (float)lp, lp_lo = (float)(lp - (double)lp_hi);
-        const float4 u4 = load4<UT>(A.U, ((size_t)r * A.gamma + (j - 1)) * V + c);
-        const float4 p4 = load4<PT>(A.P, ((size_t)r * G1 + (j - 1)) * V + c);
-        const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
-        const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float qv = expf(((uu[q] + b[q]) * invT - lq_hi) - lq_lo);
-            const float pv = expf((pp[q] * invT - lp_hi) - lp_lo);
-            const float w = pv - qv;
-            wsum += w > 0.f ? (double)w : 0.0;
-        }
-    }
-    wsum = warp_sum_d(wsum);
     __shared__ double sh[8];
-    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = wsum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int i = 0; i < 8; ++i) t += sh[i];
-        A.rmass[(size_t)r * A.nch + ch] = t;
+    const int V = A.V, G1 = A.gamma + 1;
+    const float invT = 1.f / A.T;
+    const long long tasks = (long long)A.nch * A.R;
+    for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {
+        const int ch = (int)(task % A.nch), r = (int)(task / A.nch);
+        const int2 st = A.vstate[r];
+        if (st.x != kModeResidual) continue;                     // block-uniform
+        const int j = st.y;
+        __syncthreads();
+        for (int i = threadIdx.x; i < A.r; i += blockDim.x)
+            e_sh[i] = A.code[((size_t)r * A.gamma + (j - 1)) * A.r + i];
+        __syncthreads();
+        const int c = ch * kChunk + 4 * threadIdx.x;
+        double wsum = 0.0;
+        if (c < V) {
+            float b[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < A.r; ++i) {
+                const float4 w = load4<WT>(A.W2, (size_t)i * V + c);
+                const float ei = e_sh[i];
+                b[0] = fmaf(ei, w.x, b[0]);
+                b[1] = fmaf(ei, w.y, b[1]);
+                b[2] = fmaf(ei, w.z, b[2]);
+                b[3] = fmaf(ei, w.w, b[3]);
+            }
+            const double lq = A.lse[(size_t)r * A.gamma + (j - 1)];
+            const double lp = A.lsep_ws[(size_t)r * G1 + (j - 1)];
+            const float lq_hi = (float)lq, lq_lo = (float)(lq - (double)lq_hi);
+            const float lp_hi = (float)lp, lp_lo = (float)(lp - (double)lp_hi);
+            const float4 u4 = load4<UT>(A.U, ((size_t)r * A.gamma + (j - 1)) * V + c);
+            const float4 p4 = load4<PT>(A.P, ((size_t)r * G1 + (j - 1)) * V + c);
+            const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float qv = expf(((uu[q] + b[q]) * invT - lq_hi) - lq_lo);
+                const float pv = expf((pp[q] * invT - lp_hi) - lp_lo);
+                const float w = pv - qv;
+                wsum += w > 0.f ? (double)w : 0.0;
+            }
+        }
+        // 64 threads cover one 256-column chunk: two warps each
+        wsum = warp_sum_d(wsum);
+        if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = wsum;
+        __syncthreads();
+        if (threadIdx.x < 4) {
+            const int c256 = ch * 4 + threadIdx.x;
+            if (c256 < A.nch256) {
+                float4* dst = reinterpret_cast<float4*>(A.rpart + ((size_t)r * A.nch256 + c256) * 4);
+                *dst = make_float4((float)(sh[2 * threadIdx.x] + sh[2 * threadIdx.x + 1]), 0.f, 0.f, 0.f);
+            }
+        }
     }
 }
 
@@ -295,61 +339,61 @@ __device__ double leaf_weight(const VerifyArgs& A, int r, int mode, int pos, boo
 
 template <int PT, int UT, int WT>
 __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
-    __shared__ double cm[1024];        // chunk masses (top of the tree), then leaf weights
+    __shared__ double cm[1024];        // node masses: chunk masses first, then leaf weights
     __shared__ float e_sh[1024];
+    __shared__ double sh[8];
     __shared__ int s_chunk;
     __shared__ int s_use_p;
     const int r = blockIdx.x;
     const int2 st = A.vstate[r];
     if (st.x == kModeDone) return;
     const int mode = st.x, pos = st.y;
-    const int V = A.V, NCH = A.nch, G1 = A.gamma + 1;
+    const int V = A.V, G1 = A.gamma + 1;
     const int L = ceil_log2_i(V);
-    const int Ltop = L > kChunkLog2 ? L - kChunkLog2 : 0;
-    const int nleaf_top = 1 << Ltop;     // >= NCH
     const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
     const PhiloxKey key = philox_key(A.seed);
+    const double lp = A.lsep_ws[(size_t)r * G1 + (pos - 1)];
     if (mode == kModeResidual)
         for (int i = threadIdx.x; i < A.r; i += blockDim.x)
             e_sh[i] = A.code[((size_t)r * A.gamma + (pos - 1)) * A.r + i];
-    // chunk masses
-    double tot = 0.0;
+    // chunk masses: 256-wide residual masses, or 1024-wide masses of p
+    bool use_p = mode != kModeResidual;
+    if (!use_p) {
+        double tot = 0.0;
+        for (int c = threadIdx.x; c < A.nch256; c += blockDim.x) {
+            const float4 q4 = *reinterpret_cast<const float4*>(A.rpart + ((size_t)r * A.nch256 + c) * 4);
+            tot += (((double)q4.x + (double)q4.y) + (double)q4.z) + (double)q4.w;
+        }
+        tot = warp_sum_d(tot);
+        if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = tot;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+            for (int i = 0; i < 8; ++i) t += sh[i];
+            s_use_p = t > 0.0 ? 0 : 1;        // empty residual (rounding only): draw from p_j
+        }
+        __syncthreads();
+        use_p = s_use_p != 0;
+    }
+    const int clog = use_p ? kChunkLog2 : kRChunkLog2;
+    const int nch = use_p ? A.nch : A.nch256;
+    const int Ltop = L > clog ? L - clog : 0;
+    const int nleaf_top = 1 << Ltop;      // <= 1024 for V <= 2^20 and 256-wide chunks up to 2^18
     for (int c = threadIdx.x; c < nleaf_top; c += blockDim.x) {
         double m = 0.0;
-        if (c < NCH) {
-            if (mode == kModeResidual) {
-                m = A.rmass[(size_t)r * NCH + c];
+        if (c < nch) {
+            if (!use_p) {
+                const float4 q4 = *reinterpret_cast<const float4*>(A.rpart + ((size_t)r * A.nch256 + c) * 4);
+                m = (((double)q4.x + (double)q4.y) + (double)q4.z) + (double)q4.w;
             } else {
-                const float2 p = A.vparts[((size_t)r * G1 + (pos - 1)) * NCH + c];
-                m = (double)p.y * exp((double)p.x - A.lsep_ws[(size_t)r * G1 + (pos - 1)]);
+                const float2 p2 = A.vparts[((size_t)r * G1 + (pos - 1)) * A.nch + c];
+                m = (double)p2.y * exp_from_double((double)p2.x - lp);
             }
         }
         cm[c] = m;
-        tot += m;
-    }
-    tot = warp_sum_d(tot);
-    __shared__ double sh[8];
-    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = tot;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int i = 0; i < 8; ++i) t += sh[i];
-        s_use_p = (mode == kModeResidual && !(t > 0.0)) ? 1 : 0;
     }
     __syncthreads();
-    const bool use_p = s_use_p != 0;
-    if (use_p) {   // empty residual (rounding only): draw from p_j
-        for (int c = threadIdx.x; c < nleaf_top; c += blockDim.x) {
-            double m = 0.0;
-            if (c < NCH) {
-                const float2 p = A.vparts[((size_t)r * G1 + (pos - 1)) * NCH + c];
-                m = (double)p.y * exp((double)p.x - A.lsep_ws[(size_t)r * G1 + (pos - 1)]);
-            }
-            cm[c] = m;
-        }
-        __syncthreads();
-    }
-    // top levels over chunk masses
+    // top levels over the chunk masses: build sums bottom-up, then descend
     if (threadIdx.x == 0) {
         int lo = 0;
         for (int d = 0; d < Ltop; ++d) {
@@ -364,13 +408,27 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     }
     __syncthreads();
     const int chunk = s_chunk;
-    // exact leaf weights of the chosen chunk
-    const int Lbot = L - Ltop;             // levels inside the chunk
-    const int nleaf = 1 << Lbot;           // <= 1024
+    // exact leaf weights of the chosen chunk, in double
+    const int Lbot = L - Ltop;
+    const int nleaf = 1 << Lbot;
+    const double invT = 1.0 / (double)A.T;
+    const double lq = (mode == kModeResidual) ? A.lse[(size_t)r * A.gamma + (pos - 1)] : 0.0;
     for (int i = threadIdx.x; i < nleaf; i += blockDim.x) {
-        const int v = chunk * kChunk + i;
+        const int v = (chunk << clog) + i;
         double w = 0.0;
-        if (v < V) w = leaf_weight<PT, UT, WT>(A, r, mode, pos, use_p, v, e_sh);
+        if (v < V) {
+            const double pv =
+                exp_from_double((double)ld_elem(A.P, PT, ((size_t)r * G1 + (pos - 1)) * V + v) * invT - lp);
+            if (use_p) {
+                w = pv;
+            } else {
+                float b = 0.f;
+                for (int k = 0; k < A.r; ++k) b = fmaf(e_sh[k], ld_elem(A.W2, WT, (size_t)k * V + v), b);
+                const double z = ((double)ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + v) + (double)b) * invT;
+                const double qv = exp_from_double(z - lq);
+                w = pv > qv ? pv - qv : 0.0;
+            }
+        }
         cm[i] = w;
     }
     __syncthreads();
@@ -384,7 +442,7 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
             const double u = rng_uniform_d(key, req, (uint32_t)pos, 2u, (uint32_t)(Ltop + d));
             if (!(u * (mL + mR) < mL)) lo += half;
         }
-        int y = chunk * kChunk + lo;
+        int y = (chunk << clog) + lo;
         if (y >= V) y = V - 1;
         A.out_tokens[(size_t)r * G1 + (pos - 1)] = y;
     }
@@ -392,22 +450,27 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
 
 // ------------------------------------------------------------------ host
 static int nch_of(int V) { return (V + kChunk - 1) / kChunk; }
+static int nch256_of(int V) { return (V + kRChunk - 1) / kRChunk; }
 
 size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
-    (void)r;
-    const int G1 = gamma + 1, NCH = nch_of(V);
+    const int G1 = gamma + 1, NCH = nch_of(V), N2 = nch256_of(V);
     size_t off = sizeof(WsHeader);
-    off = align_up(off + (size_t)R * G1 * NCH * sizeof(float2), 256);
-    off = align_up(off + (size_t)R * G1 * sizeof(double), 256);
-    off = align_up(off + (size_t)R * sizeof(int2), 256);
-    off = align_up(off + (size_t)R * NCH * sizeof(double), 256);
+    off = align_up(off + (size_t)R * G1 * NCH * sizeof(float2), 256);   // vparts
+    off = align_up(off + (size_t)R * G1 * sizeof(double), 256);         // lse of P rows
+    off = align_up(off + (size_t)R * sizeof(int2), 256);                // vstate
+    off = align_up(off + (size_t)R * N2 * 4 * sizeof(float), 256);      // rpart
+    off = align_up(off + 256, 256);                                      // counters, flags
+    off = align_up(off + (size_t)R * sizeof(int), 256);                 // rej_list
+    const size_t rpad = (size_t)((R + 127) / 128) * 128;
+    off = align_up(off + rpad * r * sizeof(uint16_t), 256);              // a_res
     return off;
 }
 
 int verify_carve(VerifyArgs& a, size_t ws_bytes) {
     if (ws_bytes < verify_workspace_bytes(a.R, a.gamma, a.V, a.r)) return DSPARK_ERR_WORKSPACE;
-    const int G1 = a.gamma + 1, NCH = nch_of(a.V);
+    const int G1 = a.gamma + 1, NCH = nch_of(a.V), N2 = nch256_of(a.V);
     a.nch = NCH;
+    a.nch256 = N2;
     char* base = static_cast<char*>(a.ws);
     size_t off = sizeof(WsHeader);
     a.vparts = reinterpret_cast<float2*>(base + off);
@@ -416,7 +479,14 @@ int verify_carve(VerifyArgs& a, size_t ws_bytes) {
     off = align_up(off + (size_t)a.R * G1 * sizeof(double), 256);
     a.vstate = reinterpret_cast<int2*>(base + off);
     off = align_up(off + (size_t)a.R * sizeof(int2), 256);
-    a.rmass = reinterpret_cast<double*>(base + off);
+    a.rpart = reinterpret_cast<float*>(base + off);
+    off = align_up(off + (size_t)a.R * N2 * 4 * sizeof(float), 256);
+    a.rej_count = reinterpret_cast<int*>(base + off);
+    a.vflags = reinterpret_cast<uint32_t*>(base + off + 16);
+    off = align_up(off + 256, 256);
+    a.rej_list = reinterpret_cast<int*>(base + off);
+    off = align_up(off + (size_t)a.R * sizeof(int), 256);
+    a.a_res = reinterpret_cast<uint16_t*>(base + off);
     return DSPARK_OK;
 }
 
@@ -445,12 +515,18 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     prof_end(s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (verify_tc_supported(a)) {
+    a.tc = verify_tc_supported(a) ? 1 : 0;
+    if (a.tc) {
         e = launch_verify_tc_residual(a, s);
-    } else {
-        dim3 g2(a.nch, a.R);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        // CUDA-core residual for codes that are not bf16-exact (or without the
+        // tensor-core pass); exits at once otherwise
+        const long long rt = (long long)a.nch * a.R;
+        const int g2 = (int)(rt < (long long)nsm * 8 ? rt : (long long)nsm * 8);
         prof_begin(kPVerifyResidualGeneric, s);
-        verify_residual_generic<PT, UT, WT><<<g2, 256, a.r * sizeof(float), s>>>(a);
+        verify_residual_generic<PT, UT, WT><<<g2 > 0 ? g2 : 1, 256, a.r * sizeof(float), s>>>(a);
         prof_end(s);
         e = cudaGetLastError();
     }

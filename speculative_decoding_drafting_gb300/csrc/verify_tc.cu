@@ -1,17 +1,418 @@
-// verify_tc.cu -- tensor-core residual pass of the verifier.
+// verify_tc.cu -- tensor-core residual pass of the verifier (sm_103a, tcgen05 + bulk copies).
+//
+// DSpark explainer, section 05: after the first rejection at position j the
+// new token comes from r(v) = max(p_j(v) - q_j(v), 0) / Z.  q_j is never
+// stored, so it is rebuilt here: q_j(v) = exp((U_j + e_j W2)[v] / T - lse_j)
+// with e_j the rank-r code of the draft step (blog section 3.2 MarkovHead,
+// B_j = W1[x_{j-1}] W2).  This pass produces the mass of every 256-column
+// chunk of max(p_j - q_j, 0); the sampling kernel descends from there.
+//
+// One CTA = 128 rejecting requests (compact order, set by the accept pass) x a
+// run of 256-column chunks.  The rows of U and P differ per request (each has
+// its own j), so they arrive by one bulk copy per row into padded shared rows
+// (conflict-free for the row-per-thread reads), while the rank-r product runs
+// as tcgen05.mma (M = 128 requests, N = 64 columns, K = r) with W2 tiles from
+// TMA, exactly as in the draft sweep.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "profile.h"
+#include "sm100.cuh"
 
 namespace dspark {
 
-bool verify_tc_supported(const VerifyArgs& a) {
-    (void)a;
-    return false;
+bool draft_tc_encode_available();
+bool draft_tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, const cuuint64_t* dims,
+                       const cuuint64_t* strides_bytes, const cuuint32_t* box);
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 64;
+constexpr int kNB = 3;             // W2 stages (64 columns x 64 rows of r, 8 KB)
+constexpr int kNS = 2;             // U/P row stages
+constexpr int kNACC = 2;
+constexpr int kEpiWG = 4;
+constexpr int kEpiWarps = 4 * kEpiWG;
+constexpr int kEpiWarp0 = 3;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr uint32_t kTmemCols = 128;
+
+__host__ __device__ constexpr int pitch_of(int es) { return kBN * es + 16; }   // padded row, bytes
+__host__ __device__ constexpr size_t stage_bytes(int esu, int esp) {
+    return (size_t)kBM * (pitch_of(esu) + pitch_of(esp));
 }
+__host__ __device__ constexpr size_t smem_bytes(int r, int esu, int esp) {
+    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * 8192 + (size_t)kNS * stage_bytes(esu, esp) + 256;
+}
+
+struct ResParams {
+    const void* U;
+    const void* P;
+    const int* rej_count;
+    const int* rej_list;
+    const int2* vstate;
+    const uint32_t* vflags;
+    const double* lse;       // draft lse [R, gamma]
+    const double* lsep;      // target lse [R, gamma+1]
+    float* rpart;            // [R][nch256][4]
+    void* ws;
+    int R, gamma, V, r, ntiles, nch256, nslices;
+    float c2;                // log2(e) / T
+};
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+template <int UT, int PT>
+__global__ void __launch_bounds__(kThreads, 1)
+    residual_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ResParams p) {
+    constexpr int esu = UT == DSPARK_F32 ? 4 : 2;
+    constexpr int esp = PT == DSPARK_F32 ? 4 : 2;
+    constexpr int pu = pitch_of(esu), pp = pitch_of(esp);
+    const int n_rej = *p.rej_count;
+    const int mg = blockIdx.y, slice = blockIdx.x;
+    if (mg * kBM >= n_rej || (*p.vflags & 1u)) return;      // nothing to do (block-uniform)
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = base;
+    uint8_t* sB = sA + (size_t)(p.r / 64) * 16384;
+    uint8_t* sS = sB + (size_t)kNB * 8192;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sS + (size_t)kNS * stage_bytes(esu, esp));
+    uint64_t* a_full = bars;
+    uint64_t* b_full = a_full + 1;
+    uint64_t* b_empty = b_full + kNB;
+    uint64_t* s_full = b_empty + kNB;
+    uint64_t* s_empty = s_full + kNS;
+    uint64_t* acc_full = s_empty + kNS;
+    uint64_t* acc_empty = acc_full + kNACC;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + kNACC);
+    volatile int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c_begin = (int)((long long)slice * p.nch256 / p.nslices);
+    const int c_end = (int)((long long)(slice + 1) * p.nch256 / p.nslices);
+    const int t_begin = c_begin * 4;
+    const int t_end = min(c_end * 4, p.ntiles);
+    const int nt = t_end > t_begin ? t_end - t_begin : 0;
+    const int kblocks = p.r / 64;
+    const int rows_here = min(kBM, n_rej - mg * kBM);
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        for (int i = 0; i < kNB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kNACC; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], kEpiWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- U_j / P_j row producer (whole warp; 4 rows per lane)
+        const uint64_t pol_first = policy_evict_first();
+        const char* srcU[4];
+        const char* srcP[4];
+        bool ok[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = lane + 32 * q;
+            ok[q] = i < rows_here;
+            srcU[q] = nullptr;
+            srcP[q] = nullptr;
+            if (ok[q]) {
+                const int r = p.rej_list[mg * kBM + i];
+                const int j = p.vstate[r].y;
+                srcU[q] = static_cast<const char*>(p.U) + ((size_t)r * p.gamma + (j - 1)) * (size_t)p.V * esu;
+                srcP[q] = static_cast<const char*>(p.P) + ((size_t)r * (p.gamma + 1) + (j - 1)) * (size_t)p.V * esp;
+            }
+        }
+        int issued = 0;
+        for (int t = 0; t < nt; ++t) {
+            const int v0 = (t_begin + t) * kBN;
+            const int ncols = min(kBN, p.V - v0);
+            const int st = t % kNS;
+            const uint32_t ph = (uint32_t)(t / kNS) & 1u;
+            bool go = true;
+            if (lane == 0) {
+                go = mbar_wait(&s_empty[st], ph ^ 1u, abort_flag);
+                if (go) mbar_expect_tx(&s_full[st], (uint32_t)rows_here * (uint32_t)ncols * (esu + esp));
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) break;
+            __syncwarp();
+            uint8_t* stage = sS + (size_t)st * stage_bytes(esu, esp);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (ok[q]) {
+                    const int i = lane + 32 * q;
+                    bulk_copy_g2s(stage + (size_t)i * pu, srcU[q] + (size_t)v0 * esu, (uint32_t)(ncols * esu),
+                                  &s_full[st], pol_first);
+                    bulk_copy_g2s(stage + (size_t)kBM * pu + (size_t)i * pp, srcP[q] + (size_t)v0 * esp,
+                                  (uint32_t)(ncols * esp), &s_full[st], pol_first);
+                }
+            issued = t + 1;
+        }
+        if (lane == 0 && *abort_flag)
+            for (int t = (issued > kNS ? issued - kNS : 0); t < issued; ++t)
+                mbar_wait_for(&s_full[t % kNS], (uint32_t)(t / kNS) & 1u, kWaitLimitNs);
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ---------------- A (codes) and W2 producer
+            const uint64_t pol_last = policy_evict_last();
+            mbar_expect_tx(a_full, (uint32_t)kblocks * 16384u);
+            for (int kb = 0; kb < kblocks; ++kb) tma_load_2d(sA + kb * 16384, &tmA, a_full, kb * 64, mg * kBM, pol_last);
+            int issued = 0;
+            for (int g = 0; g < nt * kblocks; ++g) {
+                const int t = g / kblocks, kb = g - t * kblocks;
+                const int bs = g % kNB;
+                const uint32_t bph = (uint32_t)(g / kNB) & 1u;
+                if (!mbar_wait(&b_empty[bs], bph ^ 1u, abort_flag)) break;
+                mbar_expect_tx(&b_full[bs], 8192u);
+                tma_load_2d(sB + (size_t)bs * 8192, &tmB, &b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
+                issued = g + 1;
+            }
+            if (*abort_flag) {
+                mbar_wait_for(a_full, 0, kWaitLimitNs);
+                for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
+                    mbar_wait_for(&b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
+            bool ok = mbar_wait(a_full, 0, abort_flag);
+            tc_fence_after();
+            for (int t = 0; ok && t < nt; ++t) {
+                const int buf = t % kNACC;
+                const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
+                if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * kBN);
+                for (int kb = 0; ok && kb < kblocks; ++kb) {
+                    const int g = t * kblocks + kb;
+                    const int bs = g % kNB;
+                    if (!mbar_wait(&b_full[bs], (uint32_t)(g / kNB) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* bstage = sB + (size_t)bs * 8192;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(sA + kb * 16384 + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
+                        umma_bf16(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                    }
+                    umma_commit(&b_empty[bs]);
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[buf]);
+            }
+        }
+    } else {
+        // ---------------- epilogue: thread = (rejecting request, 16-column quarter)
+        const int wg = (warp - kEpiWarp0) >> 2;
+        const int q = warp & 3;
+        const int rit = q * 32 + lane;
+        const bool row_ok = rit < rows_here;
+        const int r = row_ok ? p.rej_list[mg * kBM + rit] : 0;
+        const int j = row_ok ? p.vstate[r].y : 1;
+        // log2-domain normalisers, split hi + lo so the exponent is formed to
+        // float precision relative to the element, not to the 17-bit lse
+        const double lq2 = row_ok ? p.lse[(size_t)r * p.gamma + (j - 1)] * 1.4426950408889634 : 0.0;
+        const double lp2 = row_ok ? p.lsep[(size_t)r * (p.gamma + 1) + (j - 1)] * 1.4426950408889634 : 0.0;
+        const float lq_hi = (float)lq2, lq_lo = (float)(lq2 - (double)lq_hi);
+        const float lp_hi = (float)lp2, lp_lo = (float)(lp2 - (double)lp_hi);
+        float csum = 0.f;
+        for (int t = 0; t < nt; ++t) {
+            const int tile = t_begin + t;
+            const int v0 = tile * kBN + wg * 16;
+            const int buf = t % kNACC;
+            const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
+            const int st = t % kNS;
+            const uint32_t sph = (uint32_t)(t / kNS) & 1u;
+            bool ready = mbar_wait(&acc_full[buf], aph, abort_flag);
+            ready = ready && mbar_wait(&s_full[st], sph, abort_flag);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            __syncwarp();
+            float y[16];
+            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), y);
+            const uint8_t* stage = sS + (size_t)st * stage_bytes(esu, esp);
+            float pv[16];
+            const uint8_t* urow = stage + (size_t)rit * pu + wg * 16 * esu;
+            const uint8_t* prow = stage + (size_t)kBM * pu + (size_t)rit * pp + wg * 16 * esp;
+            if (esu == 4) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 f = *reinterpret_cast<const float4*>(urow + 16 * c);
+                    y[4 * c + 0] += f.x;
+                    y[4 * c + 1] += f.y;
+                    y[4 * c + 2] += f.z;
+                    y[4 * c + 3] += f.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 f = *reinterpret_cast<const uint4*>(urow + 16 * c);
+                    const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        y[8 * c + 2 * e] += bf16_bits_to_float(w4[e] & 0xFFFFu);
+                        y[8 * c + 2 * e + 1] += bf16_bits_to_float(w4[e] >> 16);
+                    }
+                }
+            }
+            if (esp == 4) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 f = *reinterpret_cast<const float4*>(prow + 16 * c);
+                    pv[4 * c + 0] = f.x;
+                    pv[4 * c + 1] = f.y;
+                    pv[4 * c + 2] = f.z;
+                    pv[4 * c + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 f = *reinterpret_cast<const uint4*>(prow + 16 * c);
+                    const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        pv[8 * c + 2 * e] = bf16_bits_to_float(w4[e] & 0xFFFFu);
+                        pv[8 * c + 2 * e + 1] = bf16_bits_to_float(w4[e] >> 16);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[buf]);
+                mbar_arrive(&s_empty[st]);
+            }
+            if (row_ok) {
+                const int ncols = min(16, p.V - v0);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float qv = ex2_approx(fmaf(y[i], p.c2, -lq_hi) - lq_lo);
+                    const float pw = ex2_approx(fmaf(pv[i], p.c2, -lp_hi) - lp_lo);
+                    const float w = pw - qv;
+                    csum += (i < ncols && w > 0.f) ? w : 0.f;
+                }
+            }
+            if (((tile & 3) == 3 || t == nt - 1) && row_ok && !*abort_flag) {
+                p.rpart[((size_t)r * p.nch256 + (tile >> 2)) * 4 + wg] = csum;
+                csum = 0.f;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) raise_status(p.ws, kStatTimeout);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int UT, int PT>
+cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
+    CUtensorMap tmA, tmB;
+    const int rpad = (a.R + kBM - 1) / kBM * kBM;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.r, (cuuint64_t)rpad};
+        cuuint64_t str[1] = {(cuuint64_t)a.r * 2};
+        cuuint32_t box[2] = {64, kBM};
+        if (!draft_tc_make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.a_res, dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
+        cuuint64_t str[1] = {(cuuint64_t)a.V * 2};
+        cuuint32_t box[2] = {kBN, 64};
+        if (!draft_tc_make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    ResParams p;
+    p.U = a.U;
+    p.P = a.P;
+    p.rej_count = a.rej_count;
+    p.rej_list = a.rej_list;
+    p.vstate = a.vstate;
+    p.vflags = a.vflags;
+    p.lse = a.lse;
+    p.lsep = a.lsep_ws;
+    p.rpart = a.rpart;
+    p.ws = a.ws;
+    p.R = a.R;
+    p.gamma = a.gamma;
+    p.V = a.V;
+    p.r = a.r;
+    p.ntiles = (a.V + kBN - 1) / kBN;
+    p.nch256 = a.nch256;
+    const int ng = (a.R + kBM - 1) / kBM;
+    int ns = num_sms() / ng;
+    if (ns < 1) ns = 1;
+    if (ns > a.nch256) ns = a.nch256;
+    p.nslices = ns;
+    p.c2 = 1.4426950408889634f / a.T;
+    constexpr int esu = UT == DSPARK_F32 ? 4 : 2, esp = PT == DSPARK_F32 ? 4 : 2;
+    const size_t smem = smem_bytes(a.r, esu, esp);
+    auto kern = residual_tc<UT, PT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_begin(kPVerifyResidualTc, s);
+    kern<<<dim3(ns, ng), kThreads, smem, s>>>(tmA, tmB, p);
+    prof_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool verify_tc_supported(const VerifyArgs& a) {
+    if (!(a.T > 0.f)) return false;
+    if (a.w_dtype != DSPARK_BF16 || a.r % 64 != 0 || a.r > 256 || a.V % 8 != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(a.U) & 15) || (reinterpret_cast<uintptr_t>(a.P) & 15) ||
+        (reinterpret_cast<uintptr_t>(a.W2) & 15))
+        return false;
+    const int esu = a.u_dtype == DSPARK_F32 ? 4 : 2, esp = a.p_dtype == DSPARK_F32 ? 4 : 2;
+    if (smem_bytes(a.r, esu, esp) > 232448) return false;
+    return draft_tc_encode_available();
+}
+
 cudaError_t launch_verify_tc_residual(VerifyArgs& a, cudaStream_t s) {
-    (void)a;
-    (void)s;
-    return cudaErrorNotSupported;
+    const int key = a.u_dtype * 2 + a.p_dtype;
+    switch (key) {
+        case 0: return launch_typed<DSPARK_F32, DSPARK_F32>(a, s);
+        case 1: return launch_typed<DSPARK_F32, DSPARK_BF16>(a, s);
+        case 2: return launch_typed<DSPARK_BF16, DSPARK_F32>(a, s);
+        default: return launch_typed<DSPARK_BF16, DSPARK_BF16>(a, s);
+    }
 }
 
 }  // namespace dspark
