@@ -31,17 +31,18 @@ namespace dspark {
 namespace {
 
 constexpr int kBM = 128;           // requests per CTA (one M-group)
-constexpr int kBN = 64;            // vocabulary columns per tile
-constexpr int kNB = 8;             // W2 stages, each 64 columns x 64 rows of r (8 KB)
-constexpr int kNU = 3;             // U stages
+constexpr int kBN = 128;           // vocabulary columns per tile
+constexpr int kNB = 2;             // W2 stages, each 128 columns x 64 rows of r (16 KB)
+constexpr int kNU = 2;             // U stages
 constexpr int kNACC = 2;           // TMEM accumulators
 constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 16 of a tile's 64 columns
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kEpiWarp0 = 3;       // warps 0..2: U producer, MMA issuer, W2 producer
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr uint32_t kTmemCols = 128;
-constexpr int kUStageBytes = kBM * kBN * 4;   // 32 KB (f32); bf16 uses half
-constexpr int kPfTiles = 4;        // tiles covered by one L2 prefetch box (256 columns)
+constexpr uint32_t kTmemCols = 256;
+constexpr int kUStageBytes = kBM * kBN * 4;   // 64 KB (f32); bf16 uses half
+constexpr int kBStageBytes = 16384;
+constexpr int kPfTiles = 2;        // tiles covered by one L2 prefetch box (256 columns)
 // Margin on the candidate test; the exact key decides, the test only has to
 // stay conservative against the rounding of w and 2^(m_t - kthr).
 constexpr float kRaceSafety = 1.0009765625f;   // 1 + 2^-10
@@ -82,7 +83,7 @@ struct Smem {
 };
 
 __host__ __device__ constexpr size_t smem_bytes_for(int r) {
-    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * 8192 + (size_t)kNU * kUStageBytes + 256;
+    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * kBStageBytes + (size_t)kNU * kUStageBytes + 256;
 }
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
@@ -90,7 +91,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.A = base;
     s.B = s.A + (size_t)(r / 64) * 16384;
-    s.U = s.B + (size_t)kNB * 8192;
+    s.U = s.B + (size_t)kNB * kBStageBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.U + (size_t)kNU * kUStageBytes);
     s.a_full = bars;
     s.b_full = bars + 1;
@@ -162,12 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&S.u_full[us], ubytes);
                 uint8_t* dst = S.U + (size_t)us * kUStageBytes;
-                if (UT == DSPARK_F32) {
-                    tma_load_3d(dst, &tmU, &S.u_full[us], v0, p.k - 1, mg * kBM, pol_first);
-                    tma_load_3d(dst + kUStageBytes / 2, &tmU, &S.u_full[us], v0 + 32, p.k - 1, mg * kBM, pol_first);
-                } else {
-                    tma_load_3d(dst, &tmU, &S.u_full[us], v0, p.k - 1, mg * kBM, pol_first);
-                }
+                // boxes of 128 rows x 128 bytes: four (f32) or two (bf16) per tile
+                constexpr int nbox = UT == DSPARK_F32 ? 4 : 2;
+                constexpr int bcols = UT == DSPARK_F32 ? 32 : 64;
+#pragma unroll
+                for (int b = 0; b < nbox; ++b)
+                    tma_load_3d(dst + b * 16384, &tmU, &S.u_full[us], v0 + b * bcols, p.k - 1, mg * kBM, pol_first);
                 issued = t + 1;
             }
             if (*abort_flag)   // wind down: let the copies this thread issued land
@@ -187,8 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int bs = g % kNB;
                 const uint32_t bph = (uint32_t)(g / kNB) & 1u;
                 if (!mbar_wait(&S.b_empty[bs], bph ^ 1u, abort_flag)) break;
-                mbar_expect_tx(&S.b_full[bs], 8192u);
-                tma_load_2d(S.B + (size_t)bs * 8192, &tmB, &S.b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
+                mbar_expect_tx(&S.b_full[bs], (uint32_t)kBStageBytes);
+                // two 64-column swizzle atoms side by side (8 KB apart)
+                tma_load_2d(S.B + (size_t)bs * kBStageBytes, &tmB, &S.b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
+                tma_load_2d(S.B + (size_t)bs * kBStageBytes + 8192, &tmB, &S.b_full[bs], (t_begin + t) * kBN + 64,
+                            kb * 64, pol_last);
                 issued = g + 1;
             }
             if (*abort_flag) {
@@ -218,11 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t* bstage = S.B + (size_t)bs * 8192;
+                    const uint8_t* bstage = S.B + (size_t)bs * kBStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(S.A + kb * 16384 + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
+                        // B is MN-major: 8-row K groups 1 KB apart, 64-column atoms 8 KB apart
+                        const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 8192, 1024);
                         umma_bf16(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
                     }
                     umma_commit(&S.b_empty[bs]);
@@ -249,7 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // winner's), read one tile ahead so the L2 round trip stays hidden
         uint32_t gnext = GREEDY ? kOrderNegInf : ld_relaxed_gpu(gbest);
         for (int t = 0; t < nt; ++t) {
-            const int v0 = (t_begin + t) * kBN + wg * 16;
             const int buf = t % kNACC;
             const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
             const int us = t % kNU;
@@ -262,149 +266,159 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
             tc_fence_after();
             __syncwarp();
-            float y[16];
-            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), y);
             const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
-            if (UT == DSPARK_F32) {
-                const uint8_t* rowp = ust + (wg >> 1) * (kUStageBytes / 2) + rit * 128;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                // this thread's 16 columns of the half: wg * 32 + h * 16 ..
+                const int v0 = (t_begin + t) * kBN + wg * 32 + h * 16;
+                float y[16];
+                __syncwarp();
+                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 32 + h * 16), y);
+                if (UT == DSPARK_F32) {
+                    const uint8_t* rowp = ust + wg * 16384 + rit * 128;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float4 f =
-                        *reinterpret_cast<const float4*>(rowp + ((((wg & 1) * 4 + c) ^ (rit & 7)) << 4));
-                    y[4 * c + 0] += f.x;
-                    y[4 * c + 1] += f.y;
-                    y[4 * c + 2] += f.z;
-                    y[4 * c + 3] += f.w;
-                }
-            } else {
-                const uint8_t* rowp = ust + rit * 128;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint4 f = *reinterpret_cast<const uint4*>(rowp + (((2 * wg + c) ^ (rit & 7)) << 4));
-                    const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        y[8 * c + 2 * e + 0] += bf16_bits_to_float(w4[e] & 0xFFFFu);
-                        y[8 * c + 2 * e + 1] += bf16_bits_to_float(w4[e] >> 16);
+                    for (int c = 0; c < 4; ++c) {
+                        const float4 f = *reinterpret_cast<const float4*>(rowp + (((4 * h + c) ^ (rit & 7)) << 4));
+                        y[4 * c + 0] += f.x;
+                        y[4 * c + 1] += f.y;
+                        y[4 * c + 2] += f.z;
+                        y[4 * c + 3] += f.w;
                     }
-                }
-            }
-            // the tile's data is in registers: hand the buffers back early
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&S.acc_empty[buf]);
-                mbar_arrive(&S.u_empty[us]);
-            }
-            if (!(row_ok && v0 + 16 <= p.V)) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (!(row_ok && v0 + i < p.V)) y[i] = -INFINITY;     // edge of the vocabulary
-            }
-            if (GREEDY) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (y[i] > kb) {          // columns rise along the thread: first max wins ties
-                        kb = y[i];
-                        ib = v0 + i;
-                    }
-                continue;
-            }
-            // y holds z = U + B here; the race and the mass work in bits (y c2).
-            // The mass is summed against a per-row reference m (the first chunk's
-            // maximum), so the common path needs no per-chunk maximum.
-            if (!__any_sync(0xffffffffu, row_ok && v0 < p.V)) continue;
-            uint32_t word[16];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(v0 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), p.ks);
-                word[4 * g + 0] = w4.x;
-                word[4 * g + 1] = w4.y;
-                word[4 * g + 2] = w4.z;
-                word[4 * g + 3] = w4.w;
-            }
-            if (m == -INFINITY) {
-                // first chunk of this thread: reference = the chunk's maximum (if any column is valid)
-                float zt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
-                m = zt * p.c2;
-            }
-            float kthr = fmaxf(kb, kglob);
-            bool any = false;
-            if (m != -INFINITY) {
-                const float nm = -m;
-                if (kthr == -INFINITY) {
-                    // nothing known for this row yet (every lane is in its first chunk):
-                    // exact keys for the whole chunk give a strong starting threshold
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (y[i] != -INFINITY) acc_take_inline(kb, zb, ib, race_key2(y[i] * p.c2, word[i]), y[i] * p.c2, v0 + i);
-                    if (kb != -INFINITY) atomicMax(p.best + row, key_order(kb));
-                    float st = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, nm));
-                    s32 += st;
-                    continue;
-                }
-                // an element can beat kthr only if t < 2^(y - kthr) (its key is at most
-                // y - log2 t); with f = 1 + t_lower in [1, 2): candidate iff
-                // f < 1 + 2^(y - m) 2^(m - kthr)
-                const float cthr = ex2_approx(m - kthr) * kRaceSafety;
-                float st = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float w = ex2_approx(fmaf(y[i], p.c2, nm));
-                    st += w;
-                    const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
-                    any = (f < fmaf(w, cthr, 1.f)) | any;
-                }
-                if (!(st <= 1.0e30f)) {
-                    // a column far above the reference: move the reference up and redo the sums
-                    float zt = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
-                    const float mt = zt * p.c2;
-                    st = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, -mt));
-                    s32 = fmaf(s32, ex2_approx(m - mt), st);
-                    m = mt;
-                    any = true;
                 } else {
-                    s32 += st;
-                }
-                if (any) {
-                    // exact keys of the candidates, one per round
-                    const float nm2 = -m;
-                    const float cthr2 = ex2_approx(m - kthr) * kRaceSafety;
-                    uint32_t cand = 0;
+                    const uint8_t* rowp = ust + (wg >> 1) * 16384 + rit * 128;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float w = ex2_approx(fmaf(y[i], p.c2, nm2));
-                        const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
-                        cand |= (f < fmaf(w, cthr2, 1.f)) ? (1u << i) : 0u;
-                    }
-                    while (cand) {
-                        const int i = __ffs(cand) - 1;
-                        cand &= cand - 1;
-                        float zi = y[0];
-                        uint32_t wi = word[0];
+                    for (int c = 0; c < 2; ++c) {
+                        const uint4 f =
+                            *reinterpret_cast<const uint4*>(rowp + ((((wg & 1) * 4 + 2 * h + c) ^ (rit & 7)) << 4));
+                        const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-                        for (int j = 1; j < 16; ++j) {
-                            zi = (i == j) ? y[j] : zi;
-                            wi = (i == j) ? word[j] : wi;
-                        }
-                        const float yi = zi * p.c2;
-                        const float kk = race_key2(yi, wi);
-                        if (key_better(kk, v0 + i, kb, ib)) {
-                            kb = kk;
-                            zb = yi;
-                            ib = v0 + i;
-                            if (kk > kglob) atomicMax(p.best + row, key_order(kk));
+                        for (int e = 0; e < 4; ++e) {
+                            y[8 * c + 2 * e + 0] += bf16_bits_to_float(w4[e] & 0xFFFFu);
+                            y[8 * c + 2 * e + 1] += bf16_bits_to_float(w4[e] >> 16);
                         }
                     }
                 }
+                if (h == 1) {
+                    // the tile's data is in registers: hand the buffers back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&S.acc_empty[buf]);
+                        mbar_arrive(&S.u_empty[us]);
+                    }
+                }
+                do {
+                    if (!(row_ok && v0 + 16 <= p.V)) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (!(row_ok && v0 + i < p.V)) y[i] = -INFINITY;     // edge of the vocabulary
+                    }
+                    if (GREEDY) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (y[i] > kb) {          // columns rise along the thread: first max wins ties
+                                kb = y[i];
+                                ib = v0 + i;
+                            }
+                        break;
+                    }
+                    // y holds z = U + B here; the race and the mass work in bits (y c2).
+                    // The mass is summed against a per-row reference m (the first chunk's
+                    // maximum), so the common path needs no per-chunk maximum.
+                    if (!__any_sync(0xffffffffu, row_ok && v0 < p.V)) break;
+                    uint32_t word[16];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(v0 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), p.ks);
+                        word[4 * g + 0] = w4.x;
+                        word[4 * g + 1] = w4.y;
+                        word[4 * g + 2] = w4.z;
+                        word[4 * g + 3] = w4.w;
+                    }
+                    if (m == -INFINITY) {
+                        // first chunk of this thread: reference = the chunk's maximum (if any column is valid)
+                        float zt = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
+                        m = zt * p.c2;
+                    }
+                    float kthr = fmaxf(kb, kglob);
+                    bool any = false;
+                    if (m != -INFINITY) {
+                        const float nm = -m;
+                        if (kthr == -INFINITY) {
+                            // nothing known for this row yet (every lane is in its first chunk):
+                            // exact keys for the whole chunk give a strong starting threshold
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (y[i] != -INFINITY) acc_take_inline(kb, zb, ib, race_key2(y[i] * p.c2, word[i]), y[i] * p.c2, v0 + i);
+                            if (kb != -INFINITY) atomicMax(p.best + row, key_order(kb));
+                            float st = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, nm));
+                            s32 += st;
+                            break;
+                        }
+                        // an element can beat kthr only if t < 2^(y - kthr) (its key is at most
+                        // y - log2 t); with f = 1 + t_lower in [1, 2): candidate iff
+                        // f < 1 + 2^(y - m) 2^(m - kthr)
+                        const float cthr = ex2_approx(m - kthr) * kRaceSafety;
+                        float st = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float w = ex2_approx(fmaf(y[i], p.c2, nm));
+                            st += w;
+                            const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
+                            any = (f < fmaf(w, cthr, 1.f)) | any;
+                        }
+                        if (!(st <= 1.0e30f)) {
+                            // a column far above the reference: move the reference up and redo the sums
+                            float zt = -INFINITY;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
+                            const float mt = zt * p.c2;
+                            st = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, -mt));
+                            s32 = fmaf(s32, ex2_approx(m - mt), st);
+                            m = mt;
+                            any = true;
+                        } else {
+                            s32 += st;
+                        }
+                        if (any) {
+                            // exact keys of the candidates, one per round
+                            const float nm2 = -m;
+                            const float cthr2 = ex2_approx(m - kthr) * kRaceSafety;
+                            uint32_t cand = 0;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float w = ex2_approx(fmaf(y[i], p.c2, nm2));
+                                const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
+                                cand |= (f < fmaf(w, cthr2, 1.f)) ? (1u << i) : 0u;
+                            }
+                            while (cand) {
+                                const int i = __ffs(cand) - 1;
+                                cand &= cand - 1;
+                                float zi = y[0];
+                                uint32_t wi = word[0];
+#pragma unroll
+                                for (int j = 1; j < 16; ++j) {
+                                    zi = (i == j) ? y[j] : zi;
+                                    wi = (i == j) ? word[j] : wi;
+                                }
+                                const float yi = zi * p.c2;
+                                const float kk = race_key2(yi, wi);
+                                if (key_better(kk, v0 + i, kb, ib)) {
+                                    kb = kk;
+                                    zb = yi;
+                                    ib = v0 + i;
+                                    if (kk > kglob) atomicMax(p.best + row, key_order(kk));
+                                }
+                            }
+                        }
+                    }
+                } while (0);
             }
         }
         if (row_ok && !*abort_flag) {
@@ -449,6 +463,10 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, cons
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    // host-side guard: a swizzled box row must fit the 128-byte swizzle span
+    const cuuint32_t es = (dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ? 4u : 2u;
+    if (swz != CU_TENSOR_MAP_SWIZZLE_NONE && box[0] * es > 128u) return false;
+    if ((box[0] * es) % 16u) return false;
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt, (cuuint32_t)rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -461,7 +479,7 @@ int slices_for(const DraftArgs& a) {
     int ns = num_sms() / n_mg;
     if (ns < 1) ns = 1;
     if (ns > ntiles) ns = ntiles;
-    if (ns > 1024) ns = 1024;
+    if (ns > 256) ns = 256;          // 4 partials per slice must fit the 1024 slots per row
     return ns;
 }
 
@@ -480,7 +498,7 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
         cuuint64_t str[1] = {(cuuint64_t)a.V * 2};
-        cuuint32_t box[2] = {kBN, 64};
+        cuuint32_t box[2] = {64, 64};     // one 64-column swizzle atom per copy
         if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
             return cudaErrorInvalidValue;
     }
