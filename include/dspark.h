@@ -181,6 +181,36 @@ int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype,
                   float* p_tok, double* lse_p,
                   void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * dspark_verify_noalloc -- dspark_verify for callers that cannot allocate
+ * device memory (no counterpart on the pages: it changes where scratch lives,
+ * not what is computed).  Some callers are handed only their input and output
+ * buffers -- a plugin inside another framework, an engine whose memory
+ * planner owns the whole device, a path that must not pay for or synchronise
+ * on an allocation -- so they have no workspace to pass.  This entry point
+ * takes the same arguments as dspark_verify except the workspace, runs the
+ * same kernels, and allocates nothing: its scratch is an 8 MiB array built
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.
+ *  - Sizes whose workspace (dspark_verify_workspace_size) exceeds 8 MiB are
+ *    rejected with DSPARK_ERR_SHAPE before any work is enqueued (the 5-token,
+ *    256-request, 151936-word case needs about 4.4 MiB).
+ *  - The first call on a device looks up the array's device address; make it
+ *    before capturing a stream into a graph.
+ *  - All calls share the array and leave their contents in it.  Calls whose
+ *    work overlaps on the GPU race: order them (one stream, or events).
+ *  - Each call clears the array's status word; device-side conditions
+ *    (token ids outside [0, V)) are not reported by this variant.
+ */
+int dspark_verify_noalloc(const void* P, int p_dtype, const void* U, int u_dtype,
+                          const void* W2, int w_dtype,
+                          const int32_t* tokens, const float* q_tok, const double* lse,
+                          const float* code, const int32_t* verify_len,
+                          int R, int gamma, int V, int r,
+                          uint64_t seed, const uint32_t* req_ids, float temperature,
+                          int32_t* out_tokens, int32_t* accept_len, int32_t* n_out,
+                          float* p_tok, double* lse_p, void* stream);
+
 /* --------------------------------------------------------------- schedule */
 
 size_t dspark_schedule_workspace_size(int R, int gamma);
