@@ -202,29 +202,38 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
         }
     }
     __syncwarp();
+    // every verified position tested at once (lane k-1 takes position k), then
+    // the first rejection decides: everything after it is discarded
+    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+    const PhiloxKey key = philox_key(A.seed);
     int j = 0;
-    if (lane == 0) {
-        const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
-        const PhiloxKey key = philox_key(A.seed);
-        for (int k = 1; k <= L; ++k) {
-            int x = A.tokens[(size_t)r * A.gamma + (k - 1)];
+    for (int k0 = 1; k0 <= L && !j; k0 += 32) {
+        const int k = k0 + lane;
+        bool rej = false;
+        int x = 0;
+        double px = 0.0;
+        if (k <= L) {
+            x = A.tokens[(size_t)r * A.gamma + (k - 1)];
             if (x < 0 || x >= V) {
                 raise_status(A.ws, kStatBadToken);
                 x = 0;
             }
             const size_t prow = ((size_t)r * G1 + (k - 1)) * (size_t)V;
-            // p(x) = exp(P_x / T - lse_P), with the difference formed in double
-            const double px = exp_from_double((double)ld_elem(A.P, PT, prow + x) * (double)invT - lsep[k - 1]);
-            if (A.p_tok) A.p_tok[(size_t)r * A.gamma + (k - 1)] = (float)px;
+            // p(x) = exp(P_x / T - lse_P), the difference formed in double
+            px = exp_from_double((double)ld_elem(A.P, PT, prow + x) * (double)invT - lsep[k - 1]);
             const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + (k - 1)];
             const double u = rng_uniform_d(key, req, (uint32_t)k, 1u, 0u);
-            if (u < ratio) {
-                out[k - 1] = x;
-            } else {
-                j = k;
-                break;
-            }
+            rej = !(u < ratio);
         }
+        const unsigned rmask = __ballot_sync(0xffffffffu, rej);
+        const int first = rmask ? (k0 + __ffs(rmask) - 1) : 0;      // first rejected position, if any here
+        if (k <= L && (!first || k <= first)) {
+            if (A.p_tok) A.p_tok[(size_t)r * A.gamma + (k - 1)] = (float)px;
+            if (!first || k < first) out[k - 1] = x;
+        }
+        j = first;
+    }
+    if (lane == 0) {
         if (j) {
             A.vstate[r] = make_int2(kModeResidual, j);
             A.accept_len[r] = j - 1;
@@ -234,7 +243,6 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
         }
         A.n_out[r] = A.accept_len[r] + 1;
     }
-    j = __shfl_sync(0xffffffffu, j, 0);
     if (!j) return;
     // queue the rejecting request for the residual pass with its code e_j in bf16
     int slot = 0;
@@ -337,12 +345,44 @@ __device__ double leaf_weight(const VerifyArgs& A, int r, int mode, int pos, boo
     return w > 0.0 ? w : 0.0;
 }
 
+// Inverse CDF down the binary sum tree over leaves[0 .. 2^levels): the CTA
+// first builds every inner node's mass (pairwise sums, in parallel), then one
+// thread walks from the root: at depth d it draws u = stream-2 uniform number
+// (level0 + d) and goes left iff u (mL + mR) < mL.  The chosen leaf index goes
+// to *out.  Every thread of the block must call it.
+__device__ void tree_descend(const double* leaves, double* tree, int levels, PhiloxKey key, uint32_t req,
+                             uint32_t pos, uint32_t level0, int* out) {
+    // tree[1] = root, tree[n + i] = leaves[i] for n = 2^levels (leaves read directly)
+    const int n = 1 << levels;
+    for (int w = n >> 1; w >= 1; w >>= 1) {
+        for (int i = threadIdx.x; i < w; i += blockDim.x) {
+            const double l = (w == n >> 1) ? leaves[2 * i] : tree[2 * (w + i)];
+            const double rr = (w == n >> 1) ? leaves[2 * i + 1] : tree[2 * (w + i) + 1];
+            tree[w + i] = l + rr;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        int node = 1;   // heap index; children 2 node, 2 node + 1
+        for (int d = 0; d < levels; ++d) {
+            const int lc = 2 * node;
+            const bool leaf_level = (d == levels - 1);
+            const double mL = leaf_level ? leaves[lc - n] : tree[lc];
+            const double mR = leaf_level ? leaves[lc + 1 - n] : tree[lc + 1];
+            const double u = rng_uniform_d(key, req, pos, 2u, level0 + (uint32_t)d);
+            node = (u * (mL + mR) < mL) ? lc : lc + 1;
+        }
+        *out = levels > 0 ? node - n : 0;
+    }
+}
+
 template <int PT, int UT, int WT>
 __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     __shared__ double cm[1024];        // node masses: chunk masses first, then leaf weights
+    __shared__ double tree[1024];      // inner nodes of the sum tree over cm
     __shared__ float e_sh[1024];
     __shared__ double sh[8];
-    __shared__ int s_chunk;
+    __shared__ int s_chunk, s_leaf;
     __shared__ int s_use_p;
     const int r = blockIdx.x;
     const int2 st = A.vstate[r];
@@ -393,19 +433,8 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
         cm[c] = m;
     }
     __syncthreads();
-    // top levels over the chunk masses: build sums bottom-up, then descend
-    if (threadIdx.x == 0) {
-        int lo = 0;
-        for (int d = 0; d < Ltop; ++d) {
-            const int half = 1 << (Ltop - d - 1);
-            double mL = 0.0, mR = 0.0;
-            for (int c = lo; c < lo + half; ++c) mL += cm[c];
-            for (int c = lo + half; c < lo + 2 * half; ++c) mR += cm[c];
-            const double u = rng_uniform_d(key, req, (uint32_t)pos, 2u, (uint32_t)d);
-            if (!(u * (mL + mR) < mL)) lo += half;
-        }
-        s_chunk = lo;
-    }
+    // top levels over the chunk masses
+    tree_descend(cm, tree, Ltop, key, req, (uint32_t)pos, 0u, &s_chunk);
     __syncthreads();
     const int chunk = s_chunk;
     // exact leaf weights of the chosen chunk, in double
@@ -432,17 +461,10 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
         cm[i] = w;
     }
     __syncthreads();
+    tree_descend(cm, tree, Lbot, key, req, (uint32_t)pos, (uint32_t)Ltop, &s_leaf);
+    __syncthreads();
     if (threadIdx.x == 0) {
-        int lo = 0;
-        for (int d = 0; d < Lbot; ++d) {
-            const int half = 1 << (Lbot - d - 1);
-            double mL = 0.0, mR = 0.0;
-            for (int i = lo; i < lo + half; ++i) mL += cm[i];
-            for (int i = lo + half; i < lo + 2 * half; ++i) mR += cm[i];
-            const double u = rng_uniform_d(key, req, (uint32_t)pos, 2u, (uint32_t)(Ltop + d));
-            if (!(u * (mL + mR) < mL)) lo += half;
-        }
-        int y = (chunk << clog) + lo;
+        int y = (chunk << clog) + s_leaf;
         if (y >= V) y = V - 1;
         A.out_tokens[(size_t)r * G1 + (pos - 1)] = y;
     }

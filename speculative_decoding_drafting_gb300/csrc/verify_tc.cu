@@ -1,4 +1,4 @@
-// verify_tc.cu -- tensor-core residual pass of the verifier (sm_103a, tcgen05 + bulk copies).
+// verify_tc.cu -- tensor-core residual pass of the verifier (sm_103a, tcgen05 + cp.async).
 //
 // DSpark explainer, section 05: after the first rejection at position j the
 // new token comes from r(v) = max(p_j(v) - q_j(v), 0) / Z.  q_j is never
@@ -9,10 +9,11 @@
 //
 // One CTA = 128 rejecting requests (compact order, set by the accept pass) x a
 // run of 256-column chunks.  The rows of U and P differ per request (each has
-// its own j), so they arrive by one bulk copy per row into padded shared rows
-// (conflict-free for the row-per-thread reads), while the rank-r product runs
-// as tcgen05.mma (M = 128 requests, N = 64 columns, K = r) with W2 tiles from
-// TMA, exactly as in the draft sweep.
+// its own j), so no tensor map describes them: every epilogue warp fetches the
+// 16 columns of its own 32 rows with cp.async, two tiles ahead, into padded
+// shared rows (conflict-free for the row-per-thread reads), while the rank-r
+// product runs as tcgen05.mma (M = 128 requests, N = 64 columns, K = r) with
+// W2 tiles from TMA, as in the draft sweep.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -61,6 +62,16 @@ struct ResParams {
     int R, gamma, V, r, ntiles, nch256, nslices;
     float c2;                // log2(e) / T
 };
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                               uint64_t policy) {
@@ -132,53 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        // ---------------- U_j / P_j row producer (whole warp; 4 rows per lane)
-        const uint64_t pol_first = policy_evict_first();
-        const char* srcU[4];
-        const char* srcP[4];
-        bool ok[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = lane + 32 * q;
-            ok[q] = i < rows_here;
-            srcU[q] = nullptr;
-            srcP[q] = nullptr;
-            if (ok[q]) {
-                const int r = p.rej_list[mg * kBM + i];
-                const int j = p.vstate[r].y;
-                srcU[q] = static_cast<const char*>(p.U) + ((size_t)r * p.gamma + (j - 1)) * (size_t)p.V * esu;
-                srcP[q] = static_cast<const char*>(p.P) + ((size_t)r * (p.gamma + 1) + (j - 1)) * (size_t)p.V * esp;
-            }
-        }
-        int issued = 0;
-        for (int t = 0; t < nt; ++t) {
-            const int v0 = (t_begin + t) * kBN;
-            const int ncols = min(kBN, p.V - v0);
-            const int st = t % kNS;
-            const uint32_t ph = (uint32_t)(t / kNS) & 1u;
-            bool go = true;
-            if (lane == 0) {
-                go = mbar_wait(&s_empty[st], ph ^ 1u, abort_flag);
-                if (go) mbar_expect_tx(&s_full[st], (uint32_t)rows_here * (uint32_t)ncols * (esu + esp));
-            }
-            go = __shfl_sync(0xffffffffu, go, 0);
-            if (!go) break;
-            __syncwarp();
-            uint8_t* stage = sS + (size_t)st * stage_bytes(esu, esp);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (ok[q]) {
-                    const int i = lane + 32 * q;
-                    bulk_copy_g2s(stage + (size_t)i * pu, srcU[q] + (size_t)v0 * esu, (uint32_t)(ncols * esu),
-                                  &s_full[st], pol_first);
-                    bulk_copy_g2s(stage + (size_t)kBM * pu + (size_t)i * pp, srcP[q] + (size_t)v0 * esp,
-                                  (uint32_t)(ncols * esp), &s_full[st], pol_first);
-                }
-            issued = t + 1;
-        }
-        if (lane == 0 && *abort_flag)
-            for (int t = (issued > kNS ? issued - kNS : 0); t < issued; ++t)
-                mbar_wait_for(&s_full[t % kNS], (uint32_t)(t / kNS) & 1u, kWaitLimitNs);
+        // (rows of U_j and P_j are fetched by the epilogue warps themselves)
     } else if (warp == 2) {
         if (lane == 0) {
             // ---------------- A (codes) and W2 producer
@@ -249,18 +214,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lq_hi = (float)lq2, lq_lo = (float)(lq2 - (double)lq_hi);
         const float lp_hi = (float)lp2, lp_lo = (float)(lp2 - (double)lp_hi);
         float csum = 0.f;
+        // Each warp fetches U_j and P_j for its own 32 rows and 16 columns of a
+        // tile with cp.async (instruction i: lane l takes row 8i + l/4, 16-byte
+        // piece l%4), kNS tiles ahead, into padded rows of its stage slot.
+        const int fr_row = lane >> 2, fr_piece = lane & 3;
+        const char* fsrcU[4];
+        const char* fsrcP[4];
+        bool fok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = q * 32 + 8 * i + fr_row;            // row inside the group
+            fok[i] = rr < rows_here;
+            fsrcU[i] = nullptr;
+            fsrcP[i] = nullptr;
+            if (fok[i]) {
+                const int r2 = p.rej_list[mg * kBM + rr];
+                const int j2 = p.vstate[r2].y;
+                fsrcU[i] = static_cast<const char*>(p.U) + ((size_t)r2 * p.gamma + (j2 - 1)) * (size_t)p.V * esu;
+                fsrcP[i] = static_cast<const char*>(p.P) + ((size_t)r2 * (p.gamma + 1) + (j2 - 1)) * (size_t)p.V * esp;
+            }
+        }
+        auto fetch = [&](int tt) {
+            if (tt < nt) {
+                const int vv = (t_begin + tt) * kBN + wg * 16;          // first column of this warp's slice
+                uint8_t* stage = sS + (size_t)(tt % kNS) * stage_bytes(esu, esp);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = q * 32 + 8 * i + fr_row;
+                    // 16 columns = 64 B (f32) or 32 B (bf16) per row; piece fr_piece of it
+                    if (fok[i] && fr_piece * 16 < 16 * esu && vv + fr_piece * (16 / esu) < p.V)
+                        cp_async16(stage + (size_t)rr * pu + wg * 16 * esu + fr_piece * 16,
+                                   fsrcU[i] + (size_t)vv * esu + fr_piece * 16);
+                    if (fok[i] && fr_piece * 16 < 16 * esp && vv + fr_piece * (16 / esp) < p.V)
+                        cp_async16(stage + (size_t)kBM * pu + (size_t)rr * pp + wg * 16 * esp + fr_piece * 16,
+                                   fsrcP[i] + (size_t)vv * esp + fr_piece * 16);
+                }
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int tt = 0; tt < kNS; ++tt) fetch(tt);
         for (int t = 0; t < nt; ++t) {
             const int tile = t_begin + t;
             const int v0 = tile * kBN + wg * 16;
             const int buf = t % kNACC;
             const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
             const int st = t % kNS;
-            const uint32_t sph = (uint32_t)(t / kNS) & 1u;
             bool ready = mbar_wait(&acc_full[buf], aph, abort_flag);
-            ready = ready && mbar_wait(&s_full[st], sph, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) break;
+            cp_async_wait<kNS - 1>();       // this thread's pieces of tile t have landed
+            __syncwarp();                   // ... and the rest of the warp's
             tc_fence_after();
-            __syncwarp();
             float y[16];
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), y);
             const uint8_t* stage = sS + (size_t)st * stage_bytes(esu, esp);
@@ -310,11 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&acc_empty[buf]);
-                mbar_arrive(&s_empty[st]);
-            }
+            __syncwarp();                   // every lane has read stage st and the accumulator
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            fetch(t + kNS);                 // refill this stage slot with tile t + kNS
             if (row_ok) {
                 const int ncols = min(16, p.V - v0);
 #pragma unroll
