@@ -21,6 +21,9 @@
  */
 #include "dspark_oracle.h"
 
+/* Width of the chunks of the draft's two-level Gumbel-max. */
+#define ORACLE_DRAFT_CHUNK 256
+
 #include <float.h>
 #include <math.h>
 #include <pthread.h>
@@ -160,12 +163,30 @@ static void draft_position(const draft_job* J, int ri, int k, const double* B,
         double s = 0.0;
         for (int v = 0; v < V; ++v) s += exp(z[v] - m);
         double lse = m + log(s);
-        /* Gumbel-max: x = argmax_v z_v + G_v, G_v = -ln(-ln u_v). */
+        /* Gumbel-max in two levels (an exact sampler of softmax(z)):
+         * (1) over the chunks of 256 consecutive indices, with key
+         *     ln(sum_{v in c} e^{z_v}) + G_c (stream 3, index c);
+         * (2) inside the chosen chunk, with key z_v + G_v (stream 0, index v).
+         * G = -ln(-ln u).  Ties go to the lowest index at both levels. */
+        const int C = ORACLE_DRAFT_CHUNK;
+        const int nC = (V + C - 1) / C;
         uint32_t key[2] = {(uint32_t)(J->seed & 0xFFFFFFFFu), (uint32_t)(J->seed >> 32)};
+        double cbest = -INFINITY, csecond = -INFINITY;
+        int carg = 0;
+        for (int c = 0; c < nC; ++c) {
+            double mass = 0.0;
+            int hi = (c + 1) * C < V ? (c + 1) * C : V;
+            for (int v = c * C; v < hi; ++v) mass += exp(z[v] - m);
+            double u = oracle_rng_uniform(J->seed, req, (uint32_t)k, 3u, (uint32_t)c);
+            double kc = (log(mass) + m) - log(-log(u));
+            if (kc > cbest) { csecond = cbest; cbest = kc; carg = c; }
+            else if (kc > csecond) { csecond = kc; }
+        }
         double best = -INFINITY, second = -INFINITY;
         int arg = -1;
         uint32_t words[4];
-        for (int v = 0; v < V; ++v) {
+        int hi = (carg + 1) * C < V ? (carg + 1) * C : V;
+        for (int v = carg * C; v < hi; ++v) {
             if ((v & 3) == 0) {
                 uint32_t ctr[4] = {(uint32_t)v >> 2, req, (uint32_t)k, 0u};
                 oracle_philox4x32_10(ctr, key, words);
@@ -179,7 +200,8 @@ static void draft_position(const draft_job* J, int ri, int k, const double* B,
         *x_out = arg;
         *qx_out = exp(z[arg] - lse);
         *lse_out = lse;
-        *margin_out = best - second;
+        double m1 = cbest - csecond, m2 = best - second;
+        *margin_out = m1 < m2 ? m1 : m2;
     } else {
         double best = -INFINITY, second = -INFINITY;
         int arg = -1;

@@ -46,9 +46,13 @@ void oracle_residual_weights(const double* p, const double* q, int V, double* w)
 int oracle_tree_sample(const double* w, int V, uint64_t seed, uint32_t req, uint32_t pos, double* min_gap);
 
 /* Draft with the Markov head (blog section 3.2; explainer section 03).
- * Outputs: tokens [R,gamma], qx [R,gamma] = q_k(x_k), lse [R,gamma] of the
- * tempered logits, code [R,gamma,r] = W1[x_{k-1}], margin [R,gamma] = gap
- * between the best and second-best Gumbel keys (or logits at T = 0).
+ * x_k is drawn from softmax(z), z = (U_k + B_k)/T, by Gumbel-max in two
+ * levels: over chunks of 256 indices with keys ln(chunk mass) + G (stream 3,
+ * index = chunk), then inside the chosen chunk with keys z_v + G (stream 0,
+ * index = v).  Outputs: tokens [R,gamma], qx [R,gamma] = q_k(x_k),
+ * lse [R,gamma] of the tempered logits, code [R,gamma,r] = W1[x_{k-1}],
+ * margin [R,gamma] = the smaller of the two levels' best-minus-second key
+ * gaps (logit gap at T = 0).
  * req_ids may be NULL (request index).  Returns 0 or a negative error. */
 int oracle_draft_markov(const void* U, int u_dtype, const int32_t* anchor,
                         const void* W1, const void* W2, int w_dtype,

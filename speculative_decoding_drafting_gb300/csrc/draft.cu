@@ -52,9 +52,8 @@ __device__ RowAcc reduce_partials(const DraftPartial* p, int n) {
     return a;
 }
 
-// Finish step k-1 for request r from its partials; returns x_{k-1} (valid id)
-// to every thread of the block.
-__device__ int finish_step(const DraftArgs& A, int r, int kprev, const DraftPartial* parts) {
+// Greedy step (T = 0): x_{k-1} = argmax over the V-slice partials.
+__device__ int finish_greedy(const DraftArgs& A, int r, int kprev, const DraftPartial* parts) {
     __shared__ int s_x;
     RowAcc a = reduce_partials(parts, A.n_slices);
     if (threadIdx.x == 0) {
@@ -65,18 +64,201 @@ __device__ int finish_step(const DraftArgs& A, int r, int kprev, const DraftPart
             x = 0;
         }
         A.tokens[o] = x;
-        if (A.T > 0.f) {
-            // base-2 state: q(x) = 2^(y_x - m) / s;  lse = ln2 (m + log2 s)
-            A.q_tok[o] = (float)((double)exp2f(a.zb - a.m) / a.s);
-            A.lse[o] = 0.69314718055994531 * ((double)a.m + log2(a.s));
-        } else {
-            A.q_tok[o] = 1.f;
-            A.lse[o] = 0.0;
-        }
+        A.q_tok[o] = 1.f;
+        A.lse[o] = 0.0;
         s_x = x;
     }
     __syncthreads();
     return s_x;
+}
+
+// Block-wide argmax of (key, index), ties to the lower index; result in
+// thread 0's return value.
+__device__ void block_argmax(float& key, int& idx) {
+    __shared__ float sk[32];
+    __shared__ int si[32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (key_better(k2, i2, key, idx)) {
+            key = k2;
+            idx = i2;
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    __syncthreads();
+    if (lane == 0) {
+        sk[warp] = key;
+        si[warp] = idx;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        key = lane < nw ? sk[lane] : -INFINITY;
+        idx = lane < nw ? si[lane] : INT_MAX;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+            if (key_better(k2, i2, key, idx)) {
+                key = k2;
+                idx = i2;
+            }
+        }
+    }
+}
+
+// Sampling step (T > 0): Gumbel-max in two levels, an exact sampler of
+// q = softmax(z).  Level 1 picks a 256-column chunk c with key
+// log2(chunk mass) - log2(E_c) (E = -ln u, stream 3, index c); level 2 picks
+// the column inside it with key y_v - log2(E_v) (stream 0, index v), the
+// chunk's logits rebuilt here from e_k, W2 and U_k.  The chunk masses come
+// from the V sweep as (reference, sum of 2^(y - reference)) per quarter.
+template <int UT, int WT>
+__device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
+    __shared__ float e_sh[1024];
+    __shared__ float s_red[64];
+    __shared__ int s_c, s_x;
+    __shared__ float s_lse2, s_yx;
+    const int V = A.V, NC = A.nchunk;
+    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+    const PhiloxKey key = philox_key(A.seed);
+    for (int i = threadIdx.x; i < A.r; i += blockDim.x)
+        e_sh[i] = A.code[((size_t)r * A.gamma + (kprev - 1)) * A.r + i];
+    // level 1: chunk log-masses (bits), their log-sum-exp and the chunk race
+    float M = -INFINITY, S = 0.f;          // online: S = sum 2^(lm - M)
+    float kbest = -INFINITY;
+    int cbest = INT_MAX;
+    const float2* cm = A.cmass + (size_t)r * NC * 4;
+    for (int c = threadIdx.x; c < NC; c += blockDim.x) {
+        float mq = -INFINITY;
+        float2 e4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            e4[q] = cm[(size_t)c * 4 + q];
+            if (e4[q].y > 0.f) mq = fmaxf(mq, e4[q].x);
+        }
+        if (mq == -INFINITY) continue;
+        float sq = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (e4[q].y > 0.f) sq += e4[q].y * ex2_approx(e4[q].x - mq);
+        const float lm = mq + log2f(sq);                 // log2 of the chunk mass
+        if (lm > M) {
+            S = S * ex2_approx(M - lm) + 1.f;
+            M = lm;
+        } else {
+            S += ex2_approx(lm - M);
+        }
+        const uint4 w = philox4x32_10(make_uint4((uint32_t)c >> 2, req, (uint32_t)kprev, 3u), key);
+        const float kc = race_key2(lm, pick_word(w, (uint32_t)c & 3u));
+        if (key_better(kc, c, kbest, cbest)) {
+            kbest = kc;
+            cbest = c;
+        }
+    }
+    // log-sum-exp over the block
+    {
+        float m = M;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        float mb = -INFINITY;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mb = fmaxf(mb, s_red[i]);
+        float sv = (M == -INFINITY) ? 0.f : S * ex2_approx(M - mb);
+        sv = warp_sum(sv);
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) s_red[32 + (threadIdx.x >> 5)] = sv;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += (double)s_red[32 + i];
+            s_lse2 = mb + (float)log2(tot);
+        }
+    }
+    block_argmax(kbest, cbest);
+    if (threadIdx.x == 0) s_c = (cbest >= 0 && cbest < NC) ? cbest : 0;
+    __syncthreads();
+    const int c = s_c;
+    // level 2: rebuild the chosen chunk's logits, B = e W2 on its 256 columns:
+    // warp w takes rank rows w, w + 8, ..., lane l columns 8l .. 8l + 7 (one
+    // coalesced 8-element load per row), then the eight warps' sums are added
+    // in a fixed order.
+    __shared__ float s_b[8][kRChunk];
+    {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int c0 = c * kRChunk + 8 * lane;
+        float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int i = warp; i < A.r; i += 8) {
+            const float ei = e_sh[i];
+            if (c0 + 4 <= V) {
+                const float4 w0 = load4<WT>(A.W2, (size_t)i * V + c0);
+                b[0] = fmaf(ei, w0.x, b[0]);
+                b[1] = fmaf(ei, w0.y, b[1]);
+                b[2] = fmaf(ei, w0.z, b[2]);
+                b[3] = fmaf(ei, w0.w, b[3]);
+            }
+            if (c0 + 8 <= V) {
+                const float4 w1 = load4<WT>(A.W2, (size_t)i * V + c0 + 4);
+                b[4] = fmaf(ei, w1.x, b[4]);
+                b[5] = fmaf(ei, w1.y, b[5]);
+                b[6] = fmaf(ei, w1.z, b[6]);
+                b[7] = fmaf(ei, w1.w, b[7]);
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) s_b[warp][8 * lane + jj] = b[jj];
+    }
+    __syncthreads();
+    const float invT = 1.f / A.T;
+    float kx = -INFINITY;
+    int ix = INT_MAX;
+    float yx = 0.f;
+    for (int j = threadIdx.x; j < kRChunk; j += blockDim.x) {
+        const int v = c * kRChunk + j;
+        if (v >= V) continue;
+        float b = 0.f;
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) b += s_b[w8][j];
+        const float u = Elem<UT>::get(static_cast<const typename Elem<UT>::T*>(A.U),
+                                      ((size_t)r * A.gamma + (kprev - 1)) * V + v);
+        const float y = (u + b) * invT * kLog2e;
+        const uint4 w = philox4x32_10(make_uint4((uint32_t)v >> 2, req, (uint32_t)kprev, 0u), key);
+        const float kv = race_key2(y, pick_word(w, (uint32_t)v & 3u));
+        if (key_better(kv, v, kx, ix)) {
+            kx = kv;
+            ix = v;
+            yx = y;
+        }
+    }
+    const int ix_own = ix;
+    block_argmax(kx, ix);
+    if (threadIdx.x == 0) s_x = ix;
+    __syncthreads();
+    if (ix_own == s_x) s_yx = yx;                     // the thread that owns the winner
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int x = s_x;
+        const size_t o = (size_t)r * A.gamma + (kprev - 1);
+        if (x < 0 || x >= V) {
+            raise_status(A.ws, kStatBadToken);
+            x = 0;
+            s_x = 0;
+        }
+        A.tokens[o] = x;
+        A.q_tok[o] = (float)exp2((double)s_yx - (double)s_lse2);
+        A.lse[o] = 0.69314718055994531 * (double)s_lse2;
+    }
+    __syncthreads();
+    return s_x;
+}
+
+template <int UT, int WT>
+__device__ int finish_step(const DraftArgs& A, int r, int kprev) {
+    if (A.T > 0.f) return finish_sample<UT, WT>(A, r, kprev);
+    const DraftPartial* p = A.parts + (size_t)(kprev & 1) * A.parts_stride + (size_t)r * A.n_slices;
+    return finish_greedy(A, r, kprev, p);
 }
 
 __device__ __forceinline__ int read_anchor(const DraftArgs& A, int r) {
@@ -107,14 +289,14 @@ __device__ __forceinline__ void store_code(const DraftArgs& A, int r, int k, int
 }
 
 // prep(k) for the Markov head: x_{k-1} then e_k = W1[x_{k-1}].
+template <int UT, int WT>
 __global__ void __launch_bounds__(256) draft_prep_markov(DraftArgs A, int k) {
     const int r = blockIdx.x;
     int x;
     if (k == 1) {
         x = read_anchor(A, r);
     } else {
-        const DraftPartial* p = A.parts + (size_t)((k - 1) & 1) * A.parts_stride + (size_t)r * A.n_slices;
-        x = finish_step(A, r, k - 1, p);
+        x = finish_step<UT, WT>(A, r, k - 1);
     }
     if (k > A.gamma) return;
     if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
@@ -125,6 +307,7 @@ __global__ void __launch_bounds__(256) draft_prep_markov(DraftArgs A, int k) {
 // prep(k) for the RNN head (blog section 3.2 RNNHead.step):
 //   z = [s_{k-1}, W1[x_{k-1}], h_k];  G = z Wgco = (gate | cand | out)
 //   s_k = sigmoid(gate) s_{k-1} + (1 - sigmoid(gate)) tanh(cand);  e_k = tanh(out)
+template <int UT, int WT>
 __global__ void __launch_bounds__(256) draft_prep_rnn(DraftArgs A, int k) {
     extern __shared__ float zin[];   // 2r + d
     const int r = blockIdx.x;
@@ -132,8 +315,7 @@ __global__ void __launch_bounds__(256) draft_prep_rnn(DraftArgs A, int k) {
     if (k == 1) {
         x = read_anchor(A, r);
     } else {
-        const DraftPartial* p = A.parts + (size_t)((k - 1) & 1) * A.parts_stride + (size_t)r * A.n_slices;
-        x = finish_step(A, r, k - 1, p);
+        x = finish_step<UT, WT>(A, r, k - 1);
     }
     const int rr = A.r;
     float* srow = A.rnn_state + (size_t)r * rr;
@@ -204,47 +386,82 @@ __global__ void __launch_bounds__(256) draft_sweep_generic(DraftArgs A, int k) {
                 acc[g][3] = fmaf(ei, w.w, acc[g][3]);
             }
     }
-    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
-    const PhiloxKey key = philox_key(A.seed);
     const float c2 = GREEDY ? 1.f : kLog2e / A.T;     // tempered logits in bits
     const size_t urow = ((size_t)r * A.gamma + (k - 1)) * (size_t)V;
-    RowAcc a;
-    acc_init(a);
+    float y[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        float y[4];
-        int c4[4];
-        bool v4[4];
-        float4 u = ok[g] ? load4<UT>(A.U, urow + col[g]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 u = ok[g] ? load4<UT>(A.U, urow + col[g]) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            y[q] = GREEDY ? (uu[q] + acc[g][q]) : (uu[q] + acc[g][q]) * c2;
-            c4[q] = col[g] + q;
-            v4[q] = ok[g];
-        }
-        if (GREEDY) {
-            acc_update_greedy<4>(a, y, c4, v4);
-        } else {
-            uint4 w = ok[g] ? philox4x32_10(make_uint4((uint32_t)col[g] >> 2, req, (uint32_t)k, 0u), key)
-                            : make_uint4(0, 0, 0, 0);
-            const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-            acc_update_exact<4>(a, y, wd, c4, v4);
-        }
+        for (int q = 0; q < 4; ++q) y[g][q] = ok[g] ? (uu[q] + acc[g][q]) * c2 : -INFINITY;
     }
-    // block reduce -> partial of this slice
     __shared__ RowAcc sh[8];
-    acc_warp_reduce(a);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) sh[warp] = a;
+    if (GREEDY) {
+        RowAcc a;
+        acc_init(a);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            int c4[4];
+            bool v4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                c4[q] = col[g] + q;
+                v4[q] = ok[g];
+            }
+            acc_update_greedy<4>(a, y[g], c4, v4);
+        }
+        acc_warp_reduce(a);
+        if (lane == 0) sh[warp] = a;
+        __syncthreads();
+        if (warp == 0) {
+            RowAcc b;
+            acc_init(b);
+            if (lane < 8) b = sh[lane];
+            acc_warp_reduce(b);
+            if (lane == 0)
+                A.parts[(size_t)(k & 1) * A.parts_stride + (size_t)r * A.n_slices + slice] = acc_to_partial(b);
+        }
+        return;
+    }
+    // sampling: mass of each 256-column chunk of the slice against the slice max.
+    // Thread t's group g lies in chunk 4 g + t / 64 of the slice, which the 64
+    // threads of warps 2 (t / 64) and 2 (t / 64) + 1 cover together.
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mloc = fmaxf(mloc, y[g][q]);
+    __shared__ float s_m[8];
+    __shared__ float s_sum[G][8];
+    mloc = warp_max(mloc);
+    if (lane == 0) s_m[warp] = mloc;
     __syncthreads();
-    if (warp == 0) {
-        RowAcc b;
-        acc_init(b);
-        if (lane < 8) b = sh[lane];
-        acc_warp_reduce(b);
-        if (lane == 0)
-            A.parts[(size_t)(k & 1) * A.parts_stride + (size_t)r * A.n_slices + slice] = acc_to_partial(b);
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) M = fmaxf(M, s_m[i]);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float sg = 0.f;
+        if (M != -INFINITY)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sg += ex2_approx(y[g][q] - M);
+        sg = warp_sum(sg);
+        if (lane == 0) s_sum[g][warp] = sg;
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {
+        const int g = threadIdx.x >> 2, h = threadIdx.x & 3;     // chunk 4 g + h of the slice
+        const int chunk = slice * (kGenericSlice / kRChunk) + 4 * g + h;
+        if (chunk < A.nchunk) {
+            const float sc = s_sum[g][2 * h] + s_sum[g][2 * h + 1];
+            float2* e = A.cmass + ((size_t)r * A.nchunk + chunk) * 4;
+            e[0] = make_float2(M, sc);
+            e[1] = make_float2(-INFINITY, 0.f);
+            e[2] = make_float2(-INFINITY, 0.f);
+            e[3] = make_float2(-INFINITY, 0.f);
+        }
     }
 }
 
@@ -259,6 +476,7 @@ size_t draft_workspace_bytes(int R, int gamma, int V, int r, int d) {
     off = align_up(off + 2ull * R * r * sizeof(uint16_t), 256);
     off = align_up(off + (size_t)R * r * sizeof(float), 256);
     off = align_up(off + (size_t)R * sizeof(uint32_t), 256);
+    off = align_up(off + (size_t)R * ((V + kRChunk - 1) / kRChunk) * 4 * sizeof(float2), 256);
     return off;
 }
 
@@ -277,6 +495,9 @@ int draft_carve(DraftArgs& a, size_t ws_bytes) {
     a.rnn_state = reinterpret_cast<float*>(base + off);
     off = align_up(off + (size_t)a.R * a.r * sizeof(float), 256);
     a.best = reinterpret_cast<uint32_t*>(base + off);
+    off = align_up(off + (size_t)a.R * sizeof(uint32_t), 256);
+    a.cmass = reinterpret_cast<float2*>(base + off);
+    a.nchunk = (a.V + kRChunk - 1) / kRChunk;
     return DSPARK_OK;
 }
 
@@ -310,18 +531,25 @@ cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
     const bool use_tc = draft_tc_supported(a);
     a.n_slices = use_tc ? draft_tc_slices(a) : (a.V + kGenericSlice - 1) / kGenericSlice;
     const size_t rnn_smem = (size_t)(2 * a.r + a.d) * sizeof(float);
+    void (*prep_m)(DraftArgs, int);
+    void (*prep_r)(DraftArgs, int);
+    switch (a.u_dtype * 2 + a.w_dtype) {
+        case 0: prep_m = draft_prep_markov<DSPARK_F32, DSPARK_F32>; prep_r = draft_prep_rnn<DSPARK_F32, DSPARK_F32>; break;
+        case 1: prep_m = draft_prep_markov<DSPARK_F32, DSPARK_BF16>; prep_r = draft_prep_rnn<DSPARK_F32, DSPARK_BF16>; break;
+        case 2: prep_m = draft_prep_markov<DSPARK_BF16, DSPARK_F32>; prep_r = draft_prep_rnn<DSPARK_BF16, DSPARK_F32>; break;
+        default: prep_m = draft_prep_markov<DSPARK_BF16, DSPARK_BF16>; prep_r = draft_prep_rnn<DSPARK_BF16, DSPARK_BF16>; break;
+    }
     if (rnn && rnn_smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(draft_prep_rnn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)rnn_smem);
+        cudaError_t e = cudaFuncSetAttribute(prep_r, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rnn_smem);
         if (e != cudaSuccess) return e;
     }
     for (int k = 1; k <= a.gamma + 1; ++k) {
         if (rnn) {
             prof_begin(kPDraftPrepRnn, s);
-            draft_prep_rnn<<<a.R, 256, rnn_smem, s>>>(a, k);
+            prep_r<<<a.R, 256, rnn_smem, s>>>(a, k);
         } else {
             prof_begin(kPDraftPrep, s);
-            draft_prep_markov<<<a.R, 256, 0, s>>>(a, k);
+            prep_m<<<a.R, 256, 0, s>>>(a, k);
         }
         prof_end(s);
         cudaError_t e = cudaGetLastError();

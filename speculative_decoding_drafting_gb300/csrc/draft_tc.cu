@@ -43,28 +43,17 @@ constexpr uint32_t kTmemCols = 256;
 constexpr int kUStageBytes = kBM * kBN * 4;   // 64 KB (f32); bf16 uses half
 constexpr int kBStageBytes = 16384;
 constexpr int kPfTiles = 2;        // tiles covered by one L2 prefetch box (256 columns)
-// Margin on the candidate test; the exact key decides, the test only has to
-// stay conservative against the rounding of w and 2^(m_t - kthr).
-constexpr float kRaceSafety = 1.0009765625f;   // 1 + 2^-10
-
-__device__ __forceinline__ void acc_take_inline(float& kb, float& zb, int& ib, float key, float y, int col) {
-    if (key_better(key, col, kb, ib)) {
-        kb = key;
-        zb = y;
-        ib = col;
-    }
-}
 
 struct TcParams {
-    DraftPartial* parts;     // this step's partial buffer [R][n_slices]
-    uint32_t* best;          // [R] best race key so far in this step, shared by every CTA
+    DraftPartial* parts;     // greedy: this step's partial buffer [R][n_slices]
+    float2* cmass;           // sampling: [R][nchunk][4] chunk masses
+    int nchunk;
     const uint32_t* req_ids;
     void* ws;
     int R, V, r, k;          // k = 1-based step
     int ntiles, nslices;
     float c2;                // log2(e) / T
     int pf_dist;             // L2 prefetch distance in tiles (0 = off)
-    PhiloxSchedule ks;
 };
 
 struct Smem {
@@ -113,8 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Smem S = carve(smem_raw, p.r);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x, mg = blockIdx.y;
-    const int t_begin = (int)((long long)slice * p.ntiles / p.nslices);
-    const int t_end = (int)((long long)(slice + 1) * p.ntiles / p.nslices);
+    // slices hold whole 256-column chunks (two tiles each)
+    const int t_begin = 2 * (int)((long long)slice * p.nchunk / p.nslices);
+    const int t_end = min(2 * (int)((long long)(slice + 1) * p.nchunk / p.nslices), p.ntiles);
     const int nt = t_end - t_begin;
     const int kblocks = p.r / 64;
     volatile int* abort_flag = S.abort_flag;
@@ -237,40 +227,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue: thread = (request row, 16-column quarter of each tile)
-        const int wg = (warp - kEpiWarp0) >> 2;      // column quarter
+        // ---------------- epilogue: thread = (request row, 32 columns of each tile)
+        const int wg = (warp - kEpiWarp0) >> 2;      // which 32-column quarter of a tile
         const int q = warp & 3;                      // TMEM lane quarter of this warp
         const int rit = q * 32 + lane;               // row inside the tile
         const int row = mg * kBM + rit;
         const bool row_ok = row < p.R;
-        const uint32_t req = row_ok ? (p.req_ids ? p.req_ids[row] : (uint32_t)row) : 0u;
-        const uint32_t* gbest = p.best + (row_ok ? row : 0);
-        // running state: log-sum-exp mass in float against a reference max
-        // (folded into double at the end), race winner
-        float m = -INFINITY, s32 = 0.f;
-        float kb = -INFINITY, zb = 0.f;
+        // sampling: mass of every 256-column chunk against a per-thread reference
+        // mref (bits), folded in place if a later column lies far above it;
+        // greedy: the running argmax of the logits
+        float mref = -INFINITY, csum = 0.f;
+        float kb = -INFINITY;
         int ib = INT_MAX;
-        // the best key any CTA has found for this row (a lower bound on the
-        // winner's), read one tile ahead so the L2 round trip stays hidden
-        uint32_t gnext = GREEDY ? kOrderNegInf : ld_relaxed_gpu(gbest);
         for (int t = 0; t < nt; ++t) {
+            const int tile = t_begin + t;
             const int buf = t % kNACC;
             const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
             const int us = t % kNU;
             const uint32_t uph = (uint32_t)(t / kNU) & 1u;
-            const uint32_t gcur = gnext;
-            if (!GREEDY && t + 1 < nt) gnext = ld_relaxed_gpu(gbest);
-            const float kglob = key_from_order(gcur);
             bool ready = mbar_wait(&S.acc_full[buf], aph, abort_flag);
             ready = ready && mbar_wait(&S.u_full[us], uph, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
             tc_fence_after();
-            __syncwarp();
             const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
-                // this thread's 16 columns of the half: wg * 32 + h * 16 ..
-                const int v0 = (t_begin + t) * kBN + wg * 32 + h * 16;
+                const int v0 = tile * kBN + wg * 32 + h * 16;
                 float y[16];
                 __syncwarp();
                 tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 32 + h * 16), y);
@@ -307,126 +289,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(&S.u_empty[us]);
                     }
                 }
-                do {
-                    if (!(row_ok && v0 + 16 <= p.V)) {
+                if (!(row_ok && v0 + 16 <= p.V)) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (!(row_ok && v0 + i < p.V)) y[i] = -INFINITY;     // edge of the vocabulary
-                    }
-                    if (GREEDY) {
+                    for (int i = 0; i < 16; ++i)
+                        if (!(row_ok && v0 + i < p.V)) y[i] = -INFINITY;     // edge of the vocabulary
+                }
+                if (GREEDY) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (y[i] > kb) {          // columns rise along the thread: first max wins ties
-                                kb = y[i];
-                                ib = v0 + i;
-                            }
-                        break;
-                    }
-                    // y holds z = U + B here; the race and the mass work in bits (y c2).
-                    // The mass is summed against a per-row reference m (the first chunk's
-                    // maximum), so the common path needs no per-chunk maximum.
-                    if (!__any_sync(0xffffffffu, row_ok && v0 < p.V)) break;
-                    uint32_t word[16];
+                    for (int i = 0; i < 16; ++i)
+                        if (y[i] > kb) {          // columns rise along the thread: first max wins ties
+                            kb = y[i];
+                            ib = v0 + i;
+                        }
+                    continue;
+                }
+                // y holds z = U + B; the mass is 2^(z c2 - mref)
+                if (mref == -INFINITY) {
+                    float zt = -INFINITY;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)(v0 + 4 * g) >> 2, req, (uint32_t)p.k, 0u), p.ks);
-                        word[4 * g + 0] = w4.x;
-                        word[4 * g + 1] = w4.y;
-                        word[4 * g + 2] = w4.z;
-                        word[4 * g + 3] = w4.w;
-                    }
-                    if (m == -INFINITY) {
-                        // first chunk of this thread: reference = the chunk's maximum (if any column is valid)
+                    for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
+                    mref = zt * p.c2;
+                }
+                if (mref != -INFINITY) {
+                    const float nm = -mref;
+                    float sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) sp[i & 3] += ex2_approx(fmaf(y[i], p.c2, nm));
+                    const float st = (sp[0] + sp[1]) + (sp[2] + sp[3]);
+                    if (st <= 1.0e30f) {
+                        csum += st;
+                    } else {
+                        // a column far above the reference: move it up and fold the sum
                         float zt = -INFINITY;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
-                        m = zt * p.c2;
+                        const float mt = zt * p.c2;
+                        float s2 = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) s2 += ex2_approx(fmaf(y[i], p.c2, -mt));
+                        csum = fmaf(csum, ex2_approx(mref - mt), s2);
+                        mref = mt;
                     }
-                    float kthr = fmaxf(kb, kglob);
-                    bool any = false;
-                    if (m != -INFINITY) {
-                        const float nm = -m;
-                        if (kthr == -INFINITY) {
-                            // nothing known for this row yet (every lane is in its first chunk):
-                            // exact keys for the whole chunk give a strong starting threshold
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (y[i] != -INFINITY) acc_take_inline(kb, zb, ib, race_key2(y[i] * p.c2, word[i]), y[i] * p.c2, v0 + i);
-                            if (kb != -INFINITY) atomicMax(p.best + row, key_order(kb));
-                            float st = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, nm));
-                            s32 += st;
-                            break;
-                        }
-                        // an element can beat kthr only if t < 2^(y - kthr) (its key is at most
-                        // y - log2 t); with f = 1 + t_lower in [1, 2): candidate iff
-                        // f < 1 + 2^(y - m) 2^(m - kthr)
-                        const float cthr = ex2_approx(m - kthr) * kRaceSafety;
-                        float st = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float w = ex2_approx(fmaf(y[i], p.c2, nm));
-                            st += w;
-                            const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
-                            any = (f < fmaf(w, cthr, 1.f)) | any;
-                        }
-                        if (!(st <= 1.0e30f)) {
-                            // a column far above the reference: move the reference up and redo the sums
-                            float zt = -INFINITY;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) zt = fmaxf(zt, y[i]);
-                            const float mt = zt * p.c2;
-                            st = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) st += ex2_approx(fmaf(y[i], p.c2, -mt));
-                            s32 = fmaf(s32, ex2_approx(m - mt), st);
-                            m = mt;
-                            any = true;
-                        } else {
-                            s32 += st;
-                        }
-                        if (any) {
-                            // exact keys of the candidates, one per round
-                            const float nm2 = -m;
-                            const float cthr2 = ex2_approx(m - kthr) * kRaceSafety;
-                            uint32_t cand = 0;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float w = ex2_approx(fmaf(y[i], p.c2, nm2));
-                                const float f = __uint_as_float(0x3F800000u | ((~word[i]) >> 9));
-                                cand |= (f < fmaf(w, cthr2, 1.f)) ? (1u << i) : 0u;
-                            }
-                            while (cand) {
-                                const int i = __ffs(cand) - 1;
-                                cand &= cand - 1;
-                                float zi = y[0];
-                                uint32_t wi = word[0];
-#pragma unroll
-                                for (int j = 1; j < 16; ++j) {
-                                    zi = (i == j) ? y[j] : zi;
-                                    wi = (i == j) ? word[j] : wi;
-                                }
-                                const float yi = zi * p.c2;
-                                const float kk = race_key2(yi, wi);
-                                if (key_better(kk, v0 + i, kb, ib)) {
-                                    kb = kk;
-                                    zb = yi;
-                                    ib = v0 + i;
-                                    if (kk > kglob) atomicMax(p.best + row, key_order(kk));
-                                }
-                            }
-                        }
-                    }
-                } while (0);
+                }
+            }
+            if (!GREEDY && ((tile & 1) || t == nt - 1)) {
+                // end of a 256-column chunk (or of the vocabulary)
+                if (row_ok && !*abort_flag)
+                    p.cmass[((size_t)row * p.nchunk + (tile >> 1)) * 4 + wg] = make_float2(mref, csum);
+                csum = 0.f;
             }
         }
-        if (row_ok && !*abort_flag) {
+        if (GREEDY && row_ok && !*abort_flag) {
             DraftPartial part;
-            part.m = m;
-            part.s = (double)s32;
+            part.m = -INFINITY;
+            part.s = 0.0;
             part.kb = kb;
-            part.zb = GREEDY ? kb : zb;
+            part.zb = kb;
             part.ib = ib;
             p.parts[((size_t)row * p.nslices + slice) * kEpiWG + wg] = part;
         }
@@ -475,10 +393,10 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, cons
 
 int slices_for(const DraftArgs& a) {
     const int n_mg = (a.R + kBM - 1) / kBM;
-    const int ntiles = (a.V + kBN - 1) / kBN;
+    const int nchunk = (a.V + 255) / 256;
     int ns = num_sms() / n_mg;
     if (ns < 1) ns = 1;
-    if (ns > ntiles) ns = ntiles;
+    if (ns > nchunk) ns = nchunk;
     if (ns > 256) ns = 256;          // 4 partials per slice must fit the 1024 slots per row
     return ns;
 }
@@ -526,7 +444,8 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     TcParams p;
     p.pf_dist = 8;
     p.parts = a.parts + (size_t)(k & 1) * a.parts_stride;
-    p.best = a.best;
+    p.cmass = a.cmass;
+    p.nchunk = a.nchunk;
     p.req_ids = a.req_ids;
     p.ws = a.ws;
     p.R = a.R;
@@ -536,7 +455,6 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.ntiles = (a.V + kBN - 1) / kBN;
     p.nslices = a.n_slices / kEpiWG;
     p.c2 = a.T > 0.f ? kLog2e / a.T : 1.f;
-    p.ks = philox_schedule(a.seed);
     const size_t smem = smem_bytes_for(a.r);
     auto kern = draft_sweep_tc<UT, GREEDY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

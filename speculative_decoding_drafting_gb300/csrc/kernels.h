@@ -41,6 +41,8 @@ struct DraftArgs {
     uint16_t* ebf;            // [2][R][r] bf16 bits (hi, lo) of e_k
     float* rnn_state;         // [R][r]
     uint32_t* best;           // [R] best race key of the current step (order-preserving bits)
+    float2* cmass;            // [R][nchunk][4] (reference m, sum 2^(y - m)) per 256-column chunk
+    int nchunk;               // ceil(V / 256)
     int rnn;                  // 1 for the RNN head
     int n_slices;             // V-slices per request in the active sweep
     int parts_stride;         // R * n_slices_max
@@ -84,7 +86,7 @@ struct VerifyArgs {
 
 constexpr int kChunk = 1024;          // chunk of the target-row partials (bonus draws)
 constexpr int kChunkLog2 = 10;
-constexpr int kRChunk = 256;          // chunk of the residual masses
+constexpr int kRChunk = 256;          // chunk of the residual masses and of the draft's first Gumbel level
 constexpr int kRChunkLog2 = 8;
 constexpr int kGenericSlice = 4096;   // V-slice of the generic draft sweep
 

@@ -167,6 +167,49 @@ def test_zero_W2_reduces_to_independent_softmax():
     np.testing.assert_allclose(d["qx"], qx, rtol=1e-12)
 
 
+def test_two_level_gumbel_draft_law_over_many_chunks():
+    """The draft's chunk-then-element Gumbel-max samples softmax(z) exactly:
+    chi-square of many independent draws (request ids) over a 5-chunk
+    vocabulary against the library softmax."""
+    rng = np.random.default_rng(17)
+    V, n = 1100, 200_000
+    logits = rng.normal(0, 1.0, V).astype(np.float32)
+    logits[256:512] += 1.5                       # one heavy chunk
+    U = np.broadcast_to(logits, (n, 1, V)).copy()
+    W1 = np.zeros((V, 1), np.float32)
+    W2 = np.zeros((1, V), np.float32)
+    d = oracle.draft_markov(U, np.zeros(n, np.int32), W1, W2, 1.0, 31)
+    probs = special.softmax(logits.astype(np.float64))
+    cnt = np.bincount(d["tokens"][:, 0], minlength=V).astype(float)
+    # pool rare cells so every expected count is at least 5
+    order = np.argsort(probs)
+    exp_c, obs_c, acc_e, acc_o = [], [], 0.0, 0.0
+    for i in order:
+        acc_e += n * probs[i]
+        acc_o += cnt[i]
+        if acc_e >= 5:
+            exp_c.append(acc_e)
+            obs_c.append(acc_o)
+            acc_e = acc_o = 0.0
+    exp_c[-1] += acc_e
+    obs_c[-1] += acc_o
+    assert stats.chisquare(obs_c, exp_c).pvalue > 1e-3
+    # chunk frequencies match the chunk masses
+    chunk = d["tokens"][:, 0] // 256
+    cm = np.array([probs[c * 256:(c + 1) * 256].sum() for c in range(5)])
+    assert stats.chisquare(np.bincount(chunk, minlength=5), n * cm).pvalue > 1e-3
+
+
+def test_two_level_gumbel_draft_never_leaves_the_only_live_chunk():
+    V, R = 1024, 64
+    U = np.full((R, 2, V), -1.0e4, np.float32)
+    U[:, :, 512:768] = np.random.default_rng(3).normal(0, 1, (R, 2, 256))
+    W1 = np.zeros((V, 1), np.float32)
+    W2 = np.zeros((1, V), np.float32)
+    d = oracle.draft_markov(U, np.zeros(R, np.int32), W1, W2, 1.0, 5)
+    assert np.all((d["tokens"] >= 512) & (d["tokens"] < 768))
+
+
 def test_markov_code_is_embedding_of_previous_token():
     rng = np.random.default_rng(8)
     R, gamma, V, r = 5, 4, 64, 6
