@@ -3,17 +3,28 @@
 // For step k the Markov head's bias is B_k = e_k W2 with e_k = W1[x_{k-1}]
 // ("DSpark: DeepSeek 线上跑的投机解码" blog, section 3.2 MarkovHead; DSpark
 // explainer, section 03, q_k = softmax(U_k + B_k)).  One CTA owns 128
-// requests (an M-group) and a contiguous slice of 64-wide vocabulary tiles:
+// requests (an M-group) and a slice of whole 256-column chunks, walked as
+// 128-column tiles:
 //
-//   warp 0  TMA producer: e_k rows (A, once), then per tile the W2 tile
-//           (B, r x 64 bf16, kept in L2 with evict-last) and the U_k tile
-//           (128 x 64, streamed with evict-first) into a ring of stages
-//   warp 1  MMA issuer: r/16 tcgen05.mma (M=128, N=64, K=16, bf16 -> f32)
-//           into one of two TMEM accumulators, committed to mbarriers
-//   warps 2-5  epilogue: thread = one request row; tcgen05.ld its 64
-//           accumulator columns, add U_k from shared memory, z = (U+B)/T,
-//           online log-sum-exp and the Gumbel race (row_acc.cuh); at the end
-//           one partial per (row, slice) goes to the workspace
+//   warp 0  U producer: the U_k tile (128 rows x 128 columns, streamed with
+//           evict-first) into a ring of two stages
+//   warp 1  MMA issuer: r/16 tcgen05.mma (M=128, N=128, K=16, bf16 -> f32)
+//           per tile into one of two TMEM accumulators
+//   warp 2  W2 producer: per tile and 64-row K block the W2 stage
+//           (64 x 128 bf16, evict-last) into a ring of six stages
+//   warps 3-18  first the A operand: the codes e_k of the M-group go to
+//           tensor memory (lane = request row), next to the accumulators,
+//           which leaves shared memory to the U and W2 rings;
+//           then the epilogue: thread = (request row, 32 columns of the tile);
+//           tcgen05.ld the accumulator, add U_k from shared memory; sampling
+//           keeps each chunk's (reference, sum of 2^(y - reference)) pair,
+//           greedy the running argmax of the logits
+//
+// The M-groups that share a column slice form a thread-block cluster: every
+// W2 stage is cut into one piece per CTA, each CTA loads its piece and the
+// copy is multicast to all of them, so W2 leaves HBM once per slice however
+// many M-groups read it.  A stage is reused only after every CTA's MMAs have
+// released it (the release is multicast as well).
 //
 // B_k and q_k never leave the SM.  Every wait is bounded (mbar_wait); a CTA
 // that gives up records DSPARK_ERR_TIMEOUT in the workspace status word,
@@ -32,19 +43,20 @@ namespace {
 
 constexpr int kBM = 128;           // requests per CTA (one M-group)
 constexpr int kBN = 128;           // vocabulary columns per tile
-constexpr int kNB = 2;             // W2 stages, each 128 columns x 64 rows of r (16 KB)
+constexpr int kNB = 6;             // W2 stages, each 128 columns x 64 rows of r (16 KB)
 constexpr int kNU = 2;             // U stages
 constexpr int kNACC = 2;           // TMEM accumulators
-constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 16 of a tile's 64 columns
+constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 32 of a tile's 128 columns
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kEpiWarp0 = 3;       // warps 0..2: U producer, MMA issuer, W2 producer
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol = kNACC * kBN;   // A: columns [256, 256 + r/2) of tensor memory
 constexpr int kUStageBytes = kBM * kBN * 4;   // 64 KB (f32); bf16 uses half
 constexpr int kBStageBytes = 16384;
-constexpr int kPfTiles = 2;        // tiles covered by one L2 prefetch box (256 columns)
 
 struct TcParams {
+    const uint16_t* ebf;     // codes e_k, [R][r] bf16 bits
     DraftPartial* parts;     // greedy: this step's partial buffer [R][n_slices]
     float2* cmass;           // sampling: [R][nchunk][4] chunk masses
     int nchunk;
@@ -53,11 +65,10 @@ struct TcParams {
     int R, V, r, k;          // k = 1-based step
     int ntiles, nslices;
     float c2;                // log2(e) / T
-    int pf_dist;             // L2 prefetch distance in tiles (0 = off)
+    int cs;                  // CTAs per cluster (M-groups sharing each W2 stage): 1, 2 or 4
 };
 
 struct Smem {
-    uint8_t* A;
     uint8_t* B;
     uint8_t* U;
     uint64_t* a_full;
@@ -71,15 +82,14 @@ struct Smem {
     int* abort_flag;
 };
 
-__host__ __device__ constexpr size_t smem_bytes_for(int r) {
-    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * kBStageBytes + (size_t)kNU * kUStageBytes + 256;
+__host__ __device__ constexpr size_t smem_bytes_for(int /*r*/) {
+    return 1024 + (size_t)kNB * kBStageBytes + (size_t)kNU * kUStageBytes + 256;
 }
 
-__device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
+__device__ __forceinline__ Smem carve(uint8_t* raw) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-    s.A = base;
-    s.B = s.A + (size_t)(r / 64) * 16384;
+    s.B = base;
     s.U = s.B + (size_t)kNB * kBStageBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(s.U + (size_t)kNU * kUStageBytes);
     s.a_full = bars;
@@ -96,10 +106,10 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, int r) {
 
 template <int UT, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 1)
-    draft_sweep_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmUP, TcParams p) {
+    draft_sweep_tc(const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmU, TcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem S = carve(smem_raw, p.r);
+    const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x, mg = blockIdx.y;
     // slices hold whole 256-column chunks (two tiles each)
@@ -110,10 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = S.abort_flag;
 
     if (threadIdx.x == 0) {
-        mbar_init(S.a_full, 1);
+        mbar_init(S.a_full, kEpiWarps);
         for (int i = 0; i < kNB; ++i) {
             mbar_init(&S.b_full[i], 1);
-            mbar_init(&S.b_empty[i], 1);
+            mbar_init(&S.b_empty[i], (uint32_t)p.cs);   // one release per CTA of the cluster
         }
         for (int i = 0; i < kNU; ++i) {
             mbar_init(&S.u_full[i], 1);
@@ -125,13 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *S.abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmU);
     }
     if (warp == 1) tmem_alloc(S.tmem_holder, kTmemCols);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // the peers' barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *S.tmem_holder;
 
@@ -141,15 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_first = policy_evict_first();
             const uint32_t ubytes = UT == DSPARK_F32 ? (uint32_t)kUStageBytes : (uint32_t)(kUStageBytes / 2);
             int issued = 0;
-            if (p.pf_dist > 0)   // warm L2 with the first rows of the slice in 1 KB runs
-                for (int t = 0; t < p.pf_dist && t < nt; t += kPfTiles)
-                    tma_prefetch_3d(&tmUP, (t_begin + t) * kBN, p.k - 1, mg * kBM);
             for (int t = 0; t < nt; ++t) {
                 const int v0 = (t_begin + t) * kBN;
                 const int us = t % kNU;
                 const uint32_t uph = (uint32_t)(t / kNU) & 1u;
-                if (p.pf_dist > 0 && (t % kPfTiles) == 0 && t + p.pf_dist < nt)
-                    tma_prefetch_3d(&tmUP, (t_begin + t + p.pf_dist) * kBN, p.k - 1, mg * kBM);
                 if (!mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&S.u_full[us], ubytes);
                 uint8_t* dst = S.U + (size_t)us * kUStageBytes;
@@ -167,26 +171,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 2) {
         if (lane == 0) {
-            // ---------------- A and W2 producer
+            // ---------------- W2 producer
             const uint64_t pol_last = policy_evict_last();
-            mbar_expect_tx(S.a_full, (uint32_t)kblocks * 16384u);
-            for (int kb = 0; kb < kblocks; ++kb)
-                tma_load_2d(S.A + kb * 16384, &tmA, S.a_full, kb * 64, mg * kBM, pol_last);
+            // a stage is two 64-column swizzle atoms side by side (8 KB apart);
+            // in a cluster of cs CTAs, CTA i loads piece i (atom i / (cs/2),
+            // K rows (i % (cs/2)) * 128/cs ..) and multicasts it to all
+            const uint32_t rank = cluster_ctarank();
+            const int per = p.cs > 1 ? p.cs / 2 : 1;
+            const int prow = 64 / per;
+            const int atom = (int)rank / per, ro = ((int)rank % per) * prow;
+            const uint16_t mask = (uint16_t)((1u << p.cs) - 1u);
+            const int ng = nt * kblocks;
             int issued = 0;
-            for (int g = 0; g < nt * kblocks; ++g) {
+            for (int g = 0; g < ng; ++g) {
                 const int t = g / kblocks, kb = g - t * kblocks;
                 const int bs = g % kNB;
                 const uint32_t bph = (uint32_t)(g / kNB) & 1u;
                 if (!mbar_wait(&S.b_empty[bs], bph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&S.b_full[bs], (uint32_t)kBStageBytes);
-                // two 64-column swizzle atoms side by side (8 KB apart)
-                tma_load_2d(S.B + (size_t)bs * kBStageBytes, &tmB, &S.b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
-                tma_load_2d(S.B + (size_t)bs * kBStageBytes + 8192, &tmB, &S.b_full[bs], (t_begin + t) * kBN + 64,
-                            kb * 64, pol_last);
+                uint8_t* st = S.B + (size_t)bs * kBStageBytes;
+                const int v0 = (t_begin + t) * kBN;
+                if (p.cs == 1) {
+                    tma_load_2d(st, &tmB, &S.b_full[bs], v0, kb * 64, pol_last);
+                    tma_load_2d(st + 8192, &tmB, &S.b_full[bs], v0 + 64, kb * 64, pol_last);
+                } else {
+                    tma_load_2d_mc(st + atom * 8192 + ro * 128, &tmB, &S.b_full[bs], v0 + atom * 64, kb * 64 + ro,
+                                   mask, pol_last);
+                }
                 issued = g + 1;
             }
+            // the last release of every stage (the peers' included) lands
+            // here before the CTA may exit
+            for (int g = (issued > kNB ? issued - kNB : 0); g < issued && !*abort_flag; ++g)
+                mbar_wait(&S.b_empty[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag);
             if (*abort_flag) {
-                mbar_wait_for(S.a_full, 0, kWaitLimitNs);
                 for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
                     mbar_wait_for(&S.b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitNs);
             }
@@ -215,12 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t* bstage = S.B + (size_t)bs * kBStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(S.A + kb * 16384 + kk * 32, 16, 1024);
+                        // A: 16 K values = 8 tensor-memory columns per step
+                        const uint32_t at = tmem + kACol + (uint32_t)(kb * 32 + kk * 8);
                         // B is MN-major: 8-row K groups 1 KB apart, 64-column atoms 8 KB apart
                         const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 8192, 1024);
-                        umma_bf16(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                        umma_bf16_ts(d, at, bd, idesc, (kb | kk) ? 1u : 0u);
                     }
-                    umma_commit(&S.b_empty[bs]);
+                    if (p.cs > 1)
+                        umma_commit_mc(&S.b_empty[bs], (uint16_t)((1u << p.cs) - 1u));
+                    else
+                        umma_commit(&S.b_empty[bs]);
                 }
                 if (!ok) break;
                 umma_commit(&S.acc_full[buf]);
@@ -233,6 +255,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rit = q * 32 + lane;               // row inside the tile
         const int row = mg * kBM + rit;
         const bool row_ok = row < p.R;
+        {
+            // A operand: this thread's share (r/8 columns, r/4 values) of its
+            // row's code goes to tensor memory; column j of the row holds the
+            // bf16 values 2j (low half) and 2j + 1 (high half)
+            const int ncol = p.r / 8;
+            const int c0 = wg * ncol;
+            for (int c = 0; c < ncol; c += 8) {
+                uint32_t v[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (row_ok) {
+                    const uint4* src = reinterpret_cast<const uint4*>(p.ebf + (size_t)row * p.r + 2 * (c0 + c));
+                    const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
+                    v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+                    v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+                }
+                tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + kACol + (uint32_t)(c0 + c), v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.a_full);
+        }
         // sampling: mass of every 256-column chunk against a per-thread reference
         // mref (bits), folded in place if a later column lies far above it;
         // greedy: the running argmax of the logits
@@ -351,7 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && *abort_flag) raise_status(p.ws, kStatTimeout);
+    if (*abort_flag) {
+        // a peer's multicast copies or releases may still be on their way to
+        // this CTA's shared memory: give them a millisecond before leaving
+        if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+    }
+    cluster_sync();   // no CTA leaves while a peer may still write into it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -391,32 +442,75 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, cons
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int slices_for(const DraftArgs& a) {
+// M-groups per cluster: the largest of 4, 2, 1 that divides the number of
+// M-groups (a cluster shares every W2 stage among its CTAs).
+int cluster_size_for(int n_mg) { return n_mg % 4 == 0 ? 4 : (n_mg % 2 == 0 ? 2 : 1); }
+
+// Clusters of `cs` sweep CTAs that fit on the device at once (0 if unknown).
+int active_clusters(int cs, size_t smem) {
+    static int cache[3][8] = {};   // [log2 cs][r / 64 - 1]
+    const int ci = cs == 4 ? 2 : cs - 1, ri = (int)(smem / 16384) & 7;
+    if (cache[ci][ri]) return cache[ci][ri];
+    auto kern = draft_sweep_tc<DSPARK_F32, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, cs, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cache[ci][ri] = n;
+    return n;
+}
+
+struct TcPlan {
+    int cs;        // CTAs per cluster
+    int nslices;   // column slices (grid.x); grid.y = M-groups
+};
+
+// One wave: as many column slices as co-resident clusters allow.
+TcPlan plan_for(const DraftArgs& a) {
     const int n_mg = (a.R + kBM - 1) / kBM;
     const int nchunk = (a.V + 255) / 256;
-    int ns = num_sms() / n_mg;
+    TcPlan pl;
+    pl.cs = cluster_size_for(n_mg);
+    int ctas = num_sms();
+    if (pl.cs > 1) {
+        const int nc = active_clusters(pl.cs, smem_bytes_for(a.r));
+        if (nc > 0)
+            ctas = nc * pl.cs;
+        else
+            pl.cs = 1;
+    }
+    int ns = ctas / n_mg;
     if (ns < 1) ns = 1;
     if (ns > nchunk) ns = nchunk;
     if (ns > 256) ns = 256;          // 4 partials per slice must fit the 1024 slots per row
-    return ns;
+    pl.nslices = ns;
+    return pl;
 }
 
 template <int UT, bool GREEDY>
 cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
-    CUtensorMap tmA, tmB, tmU;
-    // A: the bf16 codes e_k, [R rows x r], boxes of 64 x 128 rows
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)a.r, (cuuint64_t)a.R};
-        cuuint64_t str[1] = {(cuuint64_t)a.r * 2};
-        cuuint32_t box[2] = {64, kBM};
-        if (!make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.ebf, dims, str, box))
-            return cudaErrorInvalidValue;
-    }
-    // B: W2 [r rows x V], boxes of 64 columns x r rows
+    CUtensorMap tmB, tmU;
+    const TcPlan pl = plan_for(a);
+    if (pl.nslices * kEpiWG != a.n_slices) return cudaErrorInvalidValue;
+    // B: W2 [r rows x V]; a copy is one 64-column swizzle atom of 64 K rows,
+    // or the piece of it one CTA of a cluster loads (64 / (cs / 2) rows)
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
         cuuint64_t str[1] = {(cuuint64_t)a.V * 2};
-        cuuint32_t box[2] = {64, 64};     // one 64-column swizzle atom per copy
+        cuuint32_t box[2] = {64, (cuuint32_t)(pl.cs > 1 ? 128 / pl.cs : 64)};
         if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
             return cudaErrorInvalidValue;
     }
@@ -430,19 +524,8 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
                       3, const_cast<void*>(a.U), dims, str, box))
             return cudaErrorInvalidValue;
     }
-    // U again, as 256-column boxes, for L2 prefetches in long row runs
-    CUtensorMap tmUP;
-    {
-        const size_t es = UT == DSPARK_F32 ? 4 : 2;
-        cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
-        cuuint64_t str[2] = {(cuuint64_t)a.V * es, (cuuint64_t)a.gamma * a.V * es};
-        cuuint32_t box[3] = {(cuuint32_t)(kPfTiles * kBN), 1u, (cuuint32_t)kBM};
-        if (!make_map(&tmUP, UT == DSPARK_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      3, const_cast<void*>(a.U), dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-    }
     TcParams p;
-    p.pf_dist = 8;
+    p.ebf = a.ebf;
     p.parts = a.parts + (size_t)(k & 1) * a.parts_stride;
     p.cmass = a.cmass;
     p.nchunk = a.nchunk;
@@ -453,16 +536,29 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.r = a.r;
     p.k = k;
     p.ntiles = (a.V + kBN - 1) / kBN;
-    p.nslices = a.n_slices / kEpiWG;
+    p.nslices = pl.nslices;
+    p.cs = pl.cs;
     p.c2 = a.T > 0.f ? kLog2e / a.T : 1.f;
     const size_t smem = smem_bytes_for(a.r);
     auto kern = draft_sweep_tc<UT, GREEDY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.n_slices / kEpiWG, (a.R + kBM - 1) / kBM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.nslices, (a.R + kBM - 1) / kBM, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)pl.cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     prof_begin(kPDraftSweepTc, s);
-    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmU, tmUP, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmB, tmU, p);
     prof_end(s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -485,7 +581,7 @@ bool draft_tc_supported(const DraftArgs& a) {
     return encode_fn() != nullptr;
 }
 
-int draft_tc_slices(const DraftArgs& a) { return slices_for(a) * kEpiWG; }
+int draft_tc_slices(const DraftArgs& a) { return plan_for(a).nslices * kEpiWG; }
 
 cudaError_t launch_draft_tc_sweep(DraftArgs& a, int k, cudaStream_t s) {
     const bool greedy = !(a.T > 0.f);

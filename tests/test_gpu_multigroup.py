@@ -1,0 +1,80 @@
+"""GPU parity with several 128-request M-groups, and at the full headline size.
+
+The tensor-core draft sweep gives each 128-request M-group its own CTAs; the
+M-groups that share a column slice run as one thread-block cluster and share
+every W2 stage (two groups per cluster when their number is even, four when it
+is a multiple of four, no cluster otherwise).  These cases cover each cluster
+shape, a ragged last M-group, and the full-size launch the benchmark times
+(R = 256, gamma = 5, V = 151936, r = 256), where the oracle checks a sample of
+requests through their request ids.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _parity import compare_draft, compare_verify, gpu_draft, gpu_verify_on, oracle_draft, oracle_verify_on
+from speculative_decoding_drafting_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+MULTI = {
+    # two M-groups -> clusters of two; ragged last tile and chunk (V = 48 tiles + 8 columns)
+    "mg2": synth.Workload("mg2", R=256, gamma=2, V=6152, r=64, T=1.0),
+    # three M-groups (the last one 44 requests) -> no cluster
+    "mg3": synth.Workload("mg3", R=300, gamma=2, V=4104, r=128, T=0.9),
+    # four M-groups -> clusters of four (each W2 stage in four 32-row pieces)
+    "mg4": synth.Workload("mg4", R=512, gamma=2, V=4104, r=64, T=1.0),
+    # greedy with two M-groups
+    "mg2_greedy": synth.Workload("mg2_greedy", R=256, gamma=2, V=4104, r=64, T=0.0, sigma_u=2.0),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+@pytest.mark.parametrize("name", list(MULTI))
+def test_draft_parity_multigroup(name):
+    w = MULTI[name]
+    x = synth.gen_all(w)
+    g = gpu_draft(w, x, seed=31)
+    o = oracle_draft(w, x, seed=31)
+    n, nflag, m = compare_draft(g, o, tag=name)
+    assert n >= w.R and nflag <= max(2, w.R // 50)
+    np.testing.assert_array_equal(g["code"][m], o["code"][m].astype(np.float32))
+
+
+@pytest.mark.parametrize("name", ["mg2", "mg3"])
+def test_verify_parity_multigroup(name):
+    w = MULTI[name]
+    x = synth.gen_all(w)
+    dr = oracle_draft(w, x, 8)
+    g = gpu_verify_on(w, x, dr, 8)
+    o = oracle_verify_on(w, x, dr, 8)
+    n, nflag = compare_verify(g, o, np.ones(w.R, bool), tag=name)
+    assert n + nflag == w.R and nflag <= max(2, w.R // 50)
+
+
+@pytest.mark.parametrize("name", ["headline", "greedy"])
+def test_full_size_sampled(name):
+    """The benchmark's launch at full size: GPU draft and verify on every
+    request; the oracle recomputes a sample of requests (both M-groups, their
+    edges) from the same bytes and request ids."""
+    w = synth.WORKLOADS[name]
+    x = synth.gen_all(w)
+    seed = 2024
+    g = gpu_draft(w, x, seed)
+    gv = gpu_verify_on(w, x, g, seed)
+    idx = np.array([0, 1, 126, 127, 128, 200, 254, 255])
+    xs = {k: (v[idx] if k in ("U", "P", "anchor", "H") else v) for k, v in x.items()}
+    o = oracle_draft(w, xs, seed, req_ids=idx.astype(np.uint32))
+    gs = {k: v[idx] for k, v in g.items()}
+    _, _, m = compare_draft(gs, o, tag=name)
+    same = (gs["tokens"] == o["tokens"]).all(axis=1)
+    ov = oracle_verify_on(w, xs, o, seed, req_ids=idx.astype(np.uint32))
+    gvs = {k: v[idx] for k, v in gv.items()}
+    n, _ = compare_verify(gvs, ov, same, tag=name)
+    assert n >= len(idx) - 2
