@@ -11,7 +11,9 @@ Prints ONE JSON line (rank 0).  `value` is draft+verify positions per second
 (R * gamma per step, all ranks) with inputs resident in HBM; `e2e` is the same
 metric through the C ABI with host buffers (pinned host -> device copies of
 U, P, anchors and confidences, and device -> host reads of the outputs,
-inside the timed region).
+inside the timed region).  The timed region holds the cycles alone; a second
+pass over the same steps brackets every launch with CUDA events for the
+kernel table and the roofline figure (`ms_per_step_profiled`).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dspark|reference]
 """
@@ -239,23 +241,34 @@ def main(argv=None):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    binding.profile_enable(True)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    outs = []
-    torch.cuda.synchronize()
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()                                   # evict L2 between steps
-        ev[i][0].record(stream)
-        d, s, v = step(1000 + i, wss)
-        ev[i][1].record(stream)
-        outs.append((v["accept_len"].clone(),))
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    binding.profile_enable(False)
-    launches = binding.profile_collect()
+
+    def timed(k_steps, seed0, profiled):
+        """k_steps cycles, each between a pair of events on the launch stream,
+        L2 flushed before each; with `profiled` the library also brackets
+        every launch with its own events (kernel table, roofline)."""
+        binding.profile_enable(profiled)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k_steps)]
+        outs = []
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(k_steps):
+            flush.zero_()                                   # evict L2 between steps
+            ev[i][0].record(stream)
+            d, s, v = step(seed0 + i, wss)
+            ev[i][1].record(stream)
+            outs.append((v["accept_len"].clone(),))
+        torch.cuda.synchronize()
+        t_w = time.perf_counter() - t0
+        binding.profile_enable(False)
+        return [a.elapsed_time(b) for a, b in ev], outs, t_w, (binding.profile_collect() if profiled else [])
+
+    # the timed region: nothing but the cycles (and the flush between them)
+    step_ms, outs, t_wall, _ = timed(args.steps, 1000, False)
+    # the same steps again with an event pair around every launch: the per-kernel
+    # durations of the kernel table and the roofline (events between launches
+    # also keep consecutive kernels from overlapping, so this pass is slower)
+    prof_ms, _, _, launches = timed(args.steps, 1000, True)
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     tot_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([tot_ms], device=devc, dtype=torch.float64)
@@ -350,6 +363,7 @@ def main(argv=None):
                       "rejecting_requests_per_step": n_rej},
             "kernels": kernels,
             "draft_sweep_ms_by_position": sweep_by_k,
+            "ms_per_step_profiled": round(sum(prof_ms) / len(prof_ms), 4),
             "gpu_launches": len(launches),
             "clocks": clk,
             "wall_s_timed": round(t_wall, 3),

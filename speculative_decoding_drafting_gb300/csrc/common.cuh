@@ -29,6 +29,14 @@ __device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
     atomicOr(reinterpret_cast<uint32_t*>(ws), bits);
 }
 
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled, and wait until the previous kernel has finished and its memory
+// operations are visible (returns at once for a kernel launched without it).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- Philox
 struct PhiloxKey {
     uint32_t k0, k1;
@@ -197,6 +205,53 @@ __device__ __forceinline__ float4 load4_stream<DSPARK_BF16>(const void* base, si
     return make_float4(bf16_bits_to_float(v.x & 0xFFFFu), bf16_bits_to_float(v.x >> 16),
                        bf16_bits_to_float(v.y & 0xFFFFu), bf16_bits_to_float(v.y >> 16));
 }
+
+// 8 consecutive elements starting at i (a multiple of 8 for bf16, of 4 for
+// f32); `avail` = how many of them exist (elements past it read as 0).
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, size_t i, int avail, float (&w)[8]);
+template <>
+__device__ __forceinline__ void load8<DSPARK_BF16>(const void* base, size_t i, int avail, float (&w)[8]) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (avail >= 8) v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i));
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        w[2 * e] = bf16_bits_to_float(x[e] & 0xFFFFu);
+        w[2 * e + 1] = bf16_bits_to_float(x[e] >> 16);
+    }
+}
+template <>
+__device__ __forceinline__ void load8<DSPARK_F32>(const void* base, size_t i, int avail, float (&w)[8]) {
+    const float* p = static_cast<const float*>(base) + i;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    if (avail >= 4) a = __ldg(reinterpret_cast<const float4*>(p));
+    if (avail >= 8) b = __ldg(reinterpret_cast<const float4*>(p + 4));
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// 8 consecutive values of one W2 row (bf16: kept packed until used).
+template <int WT>
+struct Row8;
+template <>
+struct Row8<DSPARK_BF16> {
+    uint4 v;
+    __device__ __forceinline__ void load(const void* base, size_t i, int avail) {
+        v = avail >= 8 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + i))
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __device__ __forceinline__ float get(int jj) const {
+        const uint32_t x = jj < 2 ? v.x : (jj < 4 ? v.y : (jj < 6 ? v.z : v.w));
+        return bf16_bits_to_float((jj & 1) ? (x >> 16) : (x & 0xFFFFu));
+    }
+};
+template <>
+struct Row8<DSPARK_F32> {
+    float w[8];
+    __device__ __forceinline__ void load(const void* base, size_t i, int avail) { load8<DSPARK_F32>(base, i, avail, w); }
+    __device__ __forceinline__ float get(int jj) const { return w[jj]; }
+};
 
 __device__ __forceinline__ float ld_elem(const void* p, int dt, size_t i) {
     if (dt == DSPARK_F32) return __ldg(static_cast<const float*>(p) + i);

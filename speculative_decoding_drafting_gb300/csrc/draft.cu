@@ -29,6 +29,8 @@ bool draft_tc_supported(const DraftArgs& a);
 int draft_tc_slices(const DraftArgs& a);
 cudaError_t launch_draft_tc_sweep(DraftArgs& a, int k, cudaStream_t s);
 
+constexpr int kPrepThreads = 512;   // threads of a prep CTA (one request)
+
 // ------------------------------------------------------------------ reduce
 // Block-wide reduction of n partials into thread 0's RowAcc.
 __device__ RowAcc reduce_partials(const DraftPartial* p, int n) {
@@ -116,64 +118,85 @@ __device__ void block_argmax(float& key, int& idx) {
 // from the V sweep as (reference, sum of 2^(y - reference)) per quarter.
 template <int UT, int WT>
 __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
+    constexpr int NW = kPrepThreads / 32;
     __shared__ float e_sh[1024];
-    __shared__ float s_red[64];
+    __shared__ float s_red[2 * NW];
     __shared__ int s_c, s_x;
     __shared__ float s_lse2, s_yx;
     const int V = A.V, NC = A.nchunk;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
     const PhiloxKey key = philox_key(A.seed);
-    for (int i = threadIdx.x; i < A.r; i += blockDim.x)
-        e_sh[i] = A.code[((size_t)r * A.gamma + (kprev - 1)) * A.r + i];
+    // the code e of step k-1: loads issued now, stored to shared memory after level 1
+    const float* crow = A.code + ((size_t)r * A.gamma + (kprev - 1)) * A.r;
+    float ev[1024 / kPrepThreads];
+#pragma unroll
+    for (int t = 0; t < 1024 / kPrepThreads; ++t) {
+        const int i = threadIdx.x + t * kPrepThreads;
+        ev[t] = i < A.r ? crow[i] : 0.f;
+    }
     // level 1: chunk log-masses (bits), their log-sum-exp and the chunk race
     float M = -INFINITY, S = 0.f;          // online: S = sum 2^(lm - M)
     float kbest = -INFINITY;
     int cbest = INT_MAX;
-    const float2* cm = A.cmass + (size_t)r * NC * 4;
-    for (int c = threadIdx.x; c < NC; c += blockDim.x) {
-        float mq = -INFINITY;
-        float2 e4[4];
+    const float4* cm = reinterpret_cast<const float4*>(A.cmass + (size_t)r * NC * 4);
+    for (int cb = threadIdx.x; cb < NC; cb += 2 * kPrepThreads) {
+        // up to two chunks per pass, their (reference, sum) quads loaded first
+        float4 e8[2][2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            e4[q] = cm[(size_t)c * 4 + q];
-            if (e4[q].y > 0.f) mq = fmaxf(mq, e4[q].x);
+        for (int t = 0; t < 2; ++t) {
+            const int c = cb + t * kPrepThreads;
+            e8[t][0] = c < NC ? cm[(size_t)c * 2] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+            e8[t][1] = c < NC ? cm[(size_t)c * 2 + 1] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         }
-        if (mq == -INFINITY) continue;
-        float sq = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (e4[q].y > 0.f) sq += e4[q].y * ex2_approx(e4[q].x - mq);
-        const float lm = mq + log2f(sq);                 // log2 of the chunk mass
-        if (lm > M) {
-            S = S * ex2_approx(M - lm) + 1.f;
-            M = lm;
-        } else {
-            S += ex2_approx(lm - M);
+        for (int t = 0; t < 2; ++t) {
+            const int c = cb + t * kPrepThreads;
+            const float2 e4[4] = {make_float2(e8[t][0].x, e8[t][0].y), make_float2(e8[t][0].z, e8[t][0].w),
+                                  make_float2(e8[t][1].x, e8[t][1].y), make_float2(e8[t][1].z, e8[t][1].w)};
+            float mq = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (e4[q].y > 0.f) mq = fmaxf(mq, e4[q].x);
+            if (c >= NC || mq == -INFINITY) continue;
+            float sq = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (e4[q].y > 0.f) sq += e4[q].y * ex2_approx(e4[q].x - mq);
+            const float lm = mq + log2f(sq);                 // log2 of the chunk mass
+            if (lm > M) {
+                S = S * ex2_approx(M - lm) + 1.f;
+                M = lm;
+            } else {
+                S += ex2_approx(lm - M);
+            }
+            const uint4 w = philox4x32_10(make_uint4((uint32_t)c >> 2, req, (uint32_t)kprev, 3u), key);
+            const float kc = race_key2(lm, pick_word(w, (uint32_t)c & 3u));
+            if (key_better(kc, c, kbest, cbest)) {
+                kbest = kc;
+                cbest = c;
+            }
         }
-        const uint4 w = philox4x32_10(make_uint4((uint32_t)c >> 2, req, (uint32_t)kprev, 3u), key);
-        const float kc = race_key2(lm, pick_word(w, (uint32_t)c & 3u));
-        if (key_better(kc, c, kbest, cbest)) {
-            kbest = kc;
-            cbest = c;
-        }
+    }
+#pragma unroll
+    for (int t = 0; t < 1024 / kPrepThreads; ++t) {
+        const int i = threadIdx.x + t * kPrepThreads;
+        if (i < A.r) e_sh[i] = ev[t];
     }
     // log-sum-exp over the block
     {
-        float m = M;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+        const float m = warp_max(M);
+        if (lane == 0) s_red[warp] = m;
         __syncthreads();
         float mb = -INFINITY;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mb = fmaxf(mb, s_red[i]);
-        float sv = (M == -INFINITY) ? 0.f : S * ex2_approx(M - mb);
-        sv = warp_sum(sv);
-        __syncthreads();
-        if ((threadIdx.x & 31) == 0) s_red[32 + (threadIdx.x >> 5)] = sv;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) mb = fmaxf(mb, s_red[i]);
+        const float sv = warp_sum((M == -INFINITY) ? 0.f : S * ex2_approx(M - mb));
+        if (lane == 0) s_red[NW + warp] = sv;
         __syncthreads();
         if (threadIdx.x == 0) {
             double tot = 0.0;
-            for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += (double)s_red[32 + i];
+            for (int i = 0; i < NW; ++i) tot += (double)s_red[NW + i];
             s_lse2 = mb + (float)log2(tot);
         }
     }
@@ -181,30 +204,34 @@ __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
     if (threadIdx.x == 0) s_c = (cbest >= 0 && cbest < NC) ? cbest : 0;
     __syncthreads();
     const int c = s_c;
-    // level 2: rebuild the chosen chunk's logits, B = e W2 on its 256 columns:
-    // warp w takes rank rows w, w + 8, ..., lane l columns 8l .. 8l + 7 (one
-    // coalesced 8-element load per row), then the eight warps' sums are added
-    // in a fixed order.
-    __shared__ float s_b[8][kRChunk];
+    // level 2: rebuild the chosen chunk's logits, B = e W2 on its 256 columns.
+    // Thread j < 256 owns column c 256 + j; its U value is fetched first so
+    // that its latency hides behind the W2 rows.  Warp w takes rank rows
+    // w, w + NW, ..., lane l columns 8l .. 8l + 7, a batch of rows' loads in
+    // flight at once; the warps' sums are added in a fixed order.
+    const int j = threadIdx.x;
+    const int v = c * kRChunk + j;
+    const bool own = j < kRChunk && v < V;
+    float u = 0.f;
+    if (own) u = Elem<UT>::get(static_cast<const typename Elem<UT>::T*>(A.U), ((size_t)r * A.gamma + (kprev - 1)) * V + v);
+    __shared__ float s_b[NW][kRChunk];
     {
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        constexpr int kBatch = WT == DSPARK_BF16 ? 16 : 8;
         const int c0 = c * kRChunk + 8 * lane;
         float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int i = warp; i < A.r; i += 8) {
-            const float ei = e_sh[i];
-            if (c0 + 4 <= V) {
-                const float4 w0 = load4<WT>(A.W2, (size_t)i * V + c0);
-                b[0] = fmaf(ei, w0.x, b[0]);
-                b[1] = fmaf(ei, w0.y, b[1]);
-                b[2] = fmaf(ei, w0.z, b[2]);
-                b[3] = fmaf(ei, w0.w, b[3]);
+        for (int i0 = warp; i0 < A.r; i0 += kBatch * NW) {
+            Row8<WT> w[kBatch];
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+                const int i = i0 + NW * t;
+                w[t].load(A.W2, (size_t)i * V + c0, i < A.r ? V - c0 : 0);
             }
-            if (c0 + 8 <= V) {
-                const float4 w1 = load4<WT>(A.W2, (size_t)i * V + c0 + 4);
-                b[4] = fmaf(ei, w1.x, b[4]);
-                b[5] = fmaf(ei, w1.y, b[5]);
-                b[6] = fmaf(ei, w1.z, b[6]);
-                b[7] = fmaf(ei, w1.w, b[7]);
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+                const int i = i0 + NW * t;
+                const float ei = i < A.r ? e_sh[i] : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) b[jj] = fmaf(ei, w[t].get(jj), b[jj]);
             }
         }
 #pragma unroll
@@ -215,22 +242,15 @@ __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
     float kx = -INFINITY;
     int ix = INT_MAX;
     float yx = 0.f;
-    for (int j = threadIdx.x; j < kRChunk; j += blockDim.x) {
-        const int v = c * kRChunk + j;
-        if (v >= V) continue;
-        float b = 0.f;
+    if (own) {
+        float bs = 0.f;
 #pragma unroll
-        for (int w8 = 0; w8 < 8; ++w8) b += s_b[w8][j];
-        const float u = Elem<UT>::get(static_cast<const typename Elem<UT>::T*>(A.U),
-                                      ((size_t)r * A.gamma + (kprev - 1)) * V + v);
-        const float y = (u + b) * invT * kLog2e;
-        const uint4 w = philox4x32_10(make_uint4((uint32_t)v >> 2, req, (uint32_t)kprev, 0u), key);
-        const float kv = race_key2(y, pick_word(w, (uint32_t)v & 3u));
-        if (key_better(kv, v, kx, ix)) {
-            kx = kv;
-            ix = v;
-            yx = y;
-        }
+        for (int w8 = 0; w8 < NW; ++w8) bs += s_b[w8][j];
+        const float y = (u + bs) * invT * kLog2e;
+        const uint4 wd = philox4x32_10(make_uint4((uint32_t)v >> 2, req, (uint32_t)kprev, 0u), key);
+        kx = race_key2(y, pick_word(wd, (uint32_t)v & 3u));
+        ix = v;
+        yx = y;
     }
     const int ix_own = ix;
     block_argmax(kx, ix);
@@ -290,7 +310,9 @@ __device__ __forceinline__ void store_code(const DraftArgs& A, int r, int k, int
 
 // prep(k) for the Markov head: x_{k-1} then e_k = W1[x_{k-1}].
 template <int UT, int WT>
-__global__ void __launch_bounds__(256) draft_prep_markov(DraftArgs A, int k) {
+__global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, int k) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     int x;
     if (k == 1) {
@@ -308,8 +330,10 @@ __global__ void __launch_bounds__(256) draft_prep_markov(DraftArgs A, int k) {
 //   z = [s_{k-1}, W1[x_{k-1}], h_k];  G = z Wgco = (gate | cand | out)
 //   s_k = sigmoid(gate) s_{k-1} + (1 - sigmoid(gate)) tanh(cand);  e_k = tanh(out)
 template <int UT, int WT>
-__global__ void __launch_bounds__(256) draft_prep_rnn(DraftArgs A, int k) {
+__global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int k) {
     extern __shared__ float zin[];   // 2r + d
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     int x;
     if (k == 1) {
@@ -357,6 +381,8 @@ __global__ void __launch_bounds__(256) draft_prep_rnn(DraftArgs A, int k) {
 template <int UT, int WT, bool GREEDY>
 __global__ void __launch_bounds__(256) draft_sweep_generic(DraftArgs A, int k) {
     extern __shared__ float e_sh[];
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.y;
     const int slice = blockIdx.x;
     const int V = A.V;
@@ -505,9 +531,10 @@ template <int UT, int WT, bool GREEDY>
 static cudaError_t sweep_generic(DraftArgs& a, int k, cudaStream_t s) {
     dim3 grid((a.V + kGenericSlice - 1) / kGenericSlice, a.R);
     prof_begin(kPDraftSweepGeneric, s);
-    draft_sweep_generic<UT, WT, GREEDY><<<grid, 256, a.r * sizeof(float), s>>>(a, k);
+    cudaError_t e = launch_kernel(draft_sweep_generic<UT, WT, GREEDY>, grid, dim3(256), a.r * sizeof(float), s, true,
+                                  a, k);
     prof_end(s);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 static cudaError_t launch_sweep(DraftArgs& a, int k, bool use_tc, cudaStream_t s) {
@@ -544,15 +571,18 @@ cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     for (int k = 1; k <= a.gamma + 1; ++k) {
+        // prep(1) waits for the caller's work; every later launch overlaps
+        // the previous kernel's tail
+        cudaError_t e;
         if (rnn) {
             prof_begin(kPDraftPrepRnn, s);
-            prep_r<<<a.R, 256, rnn_smem, s>>>(a, k);
+            e = launch_kernel(prep_r, dim3(a.R), dim3(kPrepThreads), rnn_smem, s, k > 1, a, k);
         } else {
             prof_begin(kPDraftPrep, s);
-            prep_m<<<a.R, 256, 0, s>>>(a, k);
+            e = launch_kernel(prep_m, dim3(a.R), dim3(kPrepThreads), 0, s, k > 1, a, k);
         }
         prof_end(s);
-        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (k > a.gamma) break;
         e = launch_sweep(a, k, use_tc, s);

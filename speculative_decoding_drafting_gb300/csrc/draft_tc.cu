@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmU, TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x, mg = blockIdx.y;
     // slices hold whole 256-column chunks (two tiles each)
@@ -255,6 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rit = q * 32 + lane;               // row inside the tile
         const int row = mg * kBM + rit;
         const bool row_ok = row < p.R;
+        // the codes and the chunk-mass buffer belong to the previous kernel
+        // until it has finished (U and W2 are the caller's inputs)
+        pdl_wait();
         {
             // A operand: this thread's share (r/8 columns, r/4 values) of its
             // row's code goes to tensor memory; column j of the row holds the
@@ -548,13 +552,15 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = (unsigned)pl.cs;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     prof_begin(kPDraftSweepTc, s);
     e = cudaLaunchKernelEx(&cfg, kern, tmB, tmU, p);
     prof_end(s);

@@ -106,4 +106,26 @@ cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R,
 
 int num_sms();
 
+// Launch `kern` on `s`.  With `pdl` set the launch may begin while the
+// previous kernel in the stream is still running (programmatic dependent
+// launch); such a kernel executes griddepcontrol.wait (pdl_wait) before it
+// touches anything that kernel writes or reads.  The first kernel of every
+// entry point is launched without it, so work the caller queued before the
+// call is complete and visible as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace dspark

@@ -34,6 +34,7 @@ __device__ __forceinline__ double sps_at(const double* sps, int n_sps, long long
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c, const double* sps, int n_sps,
                                                                  int R, int gamma, int Np, int32_t* len,
                                                                  double* theta, int32_t* nstar) {
+    pdl_launch_dependents();
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
     double* val = reinterpret_cast<double*>(smem + (size_t)Np * 8);

@@ -47,6 +47,7 @@ __device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
 // ------------------------------------------------------------------ pass 1
 template <int PT, bool GREEDY>
 __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
+    pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0) {   // the accept pass appends to these
         *A.rej_count = 0;
         *A.vflags = 0u;
@@ -126,6 +127,8 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
 // ------------------------------------------------------------------ accept
 template <int PT, bool GREEDY>
 __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (r >= A.R) return;
@@ -269,6 +272,8 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
 // ran and every code was bf16-exact, this kernel has nothing to do.
 template <int PT, int UT, int WT>
 __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
+    pdl_launch_dependents();
+    pdl_wait();
     if (A.tc && !(*A.vflags & 1u)) return;
     extern __shared__ float e_sh[];
     __shared__ double sh[8];
@@ -327,24 +332,6 @@ __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
 }
 
 // ------------------------------------------------------------------ sample
-// Weights of the draw, in double, for one element (used inside the chosen chunk).
-template <int PT, int UT, int WT>
-__device__ double leaf_weight(const VerifyArgs& A, int r, int mode, int pos, bool use_p, int v,
-                              const float* e_sh) {
-    const int V = A.V, G1 = A.gamma + 1;
-    const double invT = 1.0 / (double)A.T;
-    const double lp = A.lsep_ws[(size_t)r * G1 + (pos - 1)];
-    const double pv = exp((double)ld_elem(A.P, PT, ((size_t)r * G1 + (pos - 1)) * V + v) * invT - lp);
-    if (mode == kModeBonus || use_p) return pv;
-    float b = 0.f;
-    for (int i = 0; i < A.r; ++i) b = fmaf(e_sh[i], ld_elem(A.W2, WT, (size_t)i * V + v), b);
-    const double lq = A.lse[(size_t)r * A.gamma + (pos - 1)];
-    const double z = ((double)ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + v) + (double)b) * invT;
-    const double qv = exp(z - lq);
-    const double w = pv - qv;
-    return w > 0.0 ? w : 0.0;
-}
-
 // Inverse CDF down the binary sum tree over leaves[0 .. 2^levels): the CTA
 // first builds every inner node's mass (pairwise sums, in parallel), then one
 // thread walks from the root: at depth d it draws u = stream-2 uniform number
@@ -382,6 +369,8 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     __shared__ double tree[1024];      // inner nodes of the sum tree over cm
     __shared__ float e_sh[1024];
     __shared__ double sh[8];
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int s_chunk, s_leaf;
     __shared__ int s_use_p;
     const int r = blockIdx.x;
@@ -441,6 +430,34 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     const int Lbot = L - Ltop;
     const int nleaf = 1 << Lbot;
     const double invT = 1.0 / (double)A.T;
+    // residual: B = e W2 on the chunk's (at most 256) columns first.  Warp w
+    // takes rank rows w, w + 8, ..., lane l columns 8l .. 8l + 7, a batch of
+    // rows' loads in flight at once; the warps' sums are added in a fixed order.
+    __shared__ float s_b[8][kRChunk];
+    if (!use_p) {
+        constexpr int kBatch = WT == DSPARK_BF16 ? 16 : 8;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int c0 = (chunk << clog) + 8 * lane;
+        float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int i0 = warp; i0 < A.r; i0 += kBatch * 8) {
+            Row8<WT> w[kBatch];
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+                const int i = i0 + 8 * t;
+                w[t].load(A.W2, (size_t)i * V + c0, i < A.r ? V - c0 : 0);
+            }
+#pragma unroll
+            for (int t = 0; t < kBatch; ++t) {
+                const int i = i0 + 8 * t;
+                const float ei = i < A.r ? e_sh[i] : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) b[jj] = fmaf(ei, w[t].get(jj), b[jj]);
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) s_b[warp][8 * lane + jj] = b[jj];
+        __syncthreads();
+    }
     const double lq = (mode == kModeResidual) ? A.lse[(size_t)r * A.gamma + (pos - 1)] : 0.0;
     for (int i = threadIdx.x; i < nleaf; i += blockDim.x) {
         const int v = (chunk << clog) + i;
@@ -452,7 +469,8 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
                 w = pv;
             } else {
                 float b = 0.f;
-                for (int k = 0; k < A.r; ++k) b = fmaf(e_sh[k], ld_elem(A.W2, WT, (size_t)k * V + v), b);
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) b += s_b[w8][i];
                 const double z = ((double)ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + v) + (double)b) * invT;
                 const double qv = exp_from_double(z - lq);
                 w = pv > qv ? pv - qv : 0.0;
@@ -520,22 +538,27 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     long long want = (tasks + 7) / 8;
     int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
     if (grid < 1) grid = 1;
+    // pass 1 waits for the caller's work; every later launch overlaps the
+    // previous kernel's tail
+    cudaError_t e;
     if (greedy) {
         prof_begin(kPVerifyPass1, s);
-        verify_pass1<PT, true><<<grid, 256, 0, s>>>(a);
+        e = launch_kernel(verify_pass1<PT, true>, dim3(grid), dim3(256), 0, s, false, a);
         prof_end(s);
+        if (e != cudaSuccess) return e;
         prof_begin(kPVerifyAccept, s);
-        verify_accept<PT, true><<<(a.R + 7) / 8, 256, 0, s>>>(a);
+        e = launch_kernel(verify_accept<PT, true>, dim3((a.R + 7) / 8), dim3(256), 0, s, true, a);
         prof_end(s);
-        return cudaGetLastError();
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     prof_begin(kPVerifyPass1, s);
-    verify_pass1<PT, false><<<grid, 256, 0, s>>>(a);
+    e = launch_kernel(verify_pass1<PT, false>, dim3(grid), dim3(256), 0, s, false, a);
     prof_end(s);
+    if (e != cudaSuccess) return e;
     prof_begin(kPVerifyAccept, s);
-    verify_accept<PT, false><<<(a.R + 7) / 8, 256, 0, s>>>(a);
+    e = launch_kernel(verify_accept<PT, false>, dim3((a.R + 7) / 8), dim3(256), 0, s, true, a);
     prof_end(s);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     a.tc = verify_tc_supported(a) ? 1 : 0;
     if (a.tc) {
@@ -548,15 +571,16 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
         const long long rt = (long long)a.nch * a.R;
         const int g2 = (int)(rt < (long long)nsm * 8 ? rt : (long long)nsm * 8);
         prof_begin(kPVerifyResidualGeneric, s);
-        verify_residual_generic<PT, UT, WT><<<g2 > 0 ? g2 : 1, 256, a.r * sizeof(float), s>>>(a);
+        e = launch_kernel(verify_residual_generic<PT, UT, WT>, dim3(g2 > 0 ? g2 : 1), dim3(256), a.r * sizeof(float),
+                          s, true, a);
         prof_end(s);
-        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
     prof_begin(kPVerifySample, s);
-    verify_sample<PT, UT, WT><<<a.R, 256, 0, s>>>(a);
+    e = launch_kernel(verify_sample<PT, UT, WT>, dim3(a.R), dim3(256), 0, s, true, a);
     prof_end(s);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_verify(VerifyArgs& a, cudaStream_t s) {

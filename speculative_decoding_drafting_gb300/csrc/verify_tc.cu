@@ -85,6 +85,8 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 template <int UT, int PT>
 __global__ void __launch_bounds__(kThreads, 1)
     residual_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ResParams p) {
+    pdl_launch_dependents();
+    pdl_wait();   // the rejecting requests come from the acceptance pass
     constexpr int esu = UT == DSPARK_F32 ? 4 : 2;
     constexpr int esp = PT == DSPARK_F32 ? 4 : 2;
     constexpr int pu = pitch_of(esu), pp = pitch_of(esp);
@@ -389,9 +391,9 @@ cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_begin(kPVerifyResidualTc, s);
-    kern<<<dim3(ns, ng), kThreads, smem, s>>>(tmA, tmB, p);
+    e = launch_kernel(kern, dim3(ns, ng), dim3(kThreads), smem, s, true, tmA, tmB, p);
     prof_end(s);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
