@@ -13,7 +13,9 @@
 // One CTA of 1024 threads does the whole batch in shared memory:
 //   1. a = running float32 product of c along each request
 //   2. 64-bit keys (~bits(a) << 32 | r * gamma + j) bitonic-sorted ascending,
-//      i.e. a descending, then r, then j ascending; a <= 0 sorts last
+//      i.e. a descending, then r, then j ascending; a <= 0 sorts last.  A
+//      pass with stride <= 32 only touches the 64 keys of its warp, so block
+//      barriers are needed only around passes of stride >= 64.
 //   3. tau_n = R + inclusive scan of the sorted a (double)
 //   4. Theta(n) = tau_n * SPS[R + n]; n* = first n with Theta(n+1) <= Theta(n)
 //   5. l_r = number of the first n* candidates that belong to r
@@ -26,6 +28,7 @@
 namespace dspark {
 
 constexpr int kSchedThreads = 1024;
+constexpr int kSchedMaxPer = 8;    // candidates per thread at the largest batch (R gamma <= 8192)
 
 __device__ __forceinline__ double sps_at(const double* sps, int n_sps, long long B) {
     return (B >= 0 && B < n_sps) ? sps[B] : 0.0;
@@ -44,24 +47,39 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     const int tid = threadIdx.x;
     const int N = R * gamma;
 
-    // 1-2: products and keys
+    // the SPS values step 4 reads (candidate n = tid + k blockDim needs
+    // SPS[R + n] and SPS[R + n + 1]), fetched now so their latency hides
+    // behind the sort
+    double sp0[kSchedMaxPer], sp1[kSchedMaxPer];
+#pragma unroll
+    for (int k = 0; k < kSchedMaxPer; ++k) {
+        const int n = tid + k * kSchedThreads;
+        sp0[k] = n < N ? sps_at(sps, n_sps, (long long)R + n) : 0.0;
+        sp1[k] = n < N ? sps_at(sps, n_sps, (long long)R + n + 1) : 0.0;
+    }
+    // 1-2: products and keys; c goes through shared memory (val is free until step 3)
+    float* c_sh = reinterpret_cast<float*>(val);
+    for (int i = tid; i < N; i += blockDim.x) c_sh[i] = c[i];
+    if (tid == 0) s_nvalid = 0;
+    __syncthreads();
     for (int r = tid; r < R; r += blockDim.x) {
         float prod = 1.0f;
         for (int j = 0; j < gamma; ++j) {
-            prod = __fmul_rn(prod, c[(size_t)r * gamma + j]);
             const int idx = r * gamma + j;
+            prod = __fmul_rn(prod, c_sh[idx]);
             keys[idx] = (prod > 0.0f) ? (((unsigned long long)(~__float_as_uint(prod)) << 32) | (unsigned)idx)
                                       : ~0ull;
         }
         cnt[r] = 0;
     }
     for (int i = N + tid; i < Np; i += blockDim.x) keys[i] = ~0ull;
-    if (tid == 0) s_nvalid = 0;
     __syncthreads();
-    for (int size = 2; size <= Np; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    for (int ls = 1; (1 << ls) <= Np; ++ls) {
+        const int size = 1 << ls;
+        for (int lst = ls - 1; lst >= 0; --lst) {
+            const int stride = 1 << lst;
             for (int i = tid; i < Np / 2; i += blockDim.x) {
-                const int lo = (i / stride) * stride * 2 + (i % stride);
+                const int lo = ((i >> lst) << (lst + 1)) | (i & (stride - 1));
                 const int hi = lo + stride;
                 const bool up = ((lo & size) == 0);
                 const unsigned long long a = keys[lo], b = keys[hi];
@@ -70,9 +88,15 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
                     keys[hi] = a;
                 }
             }
-            __syncthreads();
+            // the next pass: stride / 2 within this size, else the next size's first
+            const int next_stride = lst > 0 ? stride >> 1 : size;
+            if (stride >= 64 || next_stride >= 64)
+                __syncthreads();
+            else
+                __syncwarp();
         }
     }
+    __syncthreads();
     // 3: scan of the sorted a (double), sequential within a thread's run
     const int per = (Np + blockDim.x - 1) / blockDim.x;
     const int b0 = tid * per;
@@ -115,12 +139,16 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     __syncthreads();
     const int nvalid = s_nvalid;
     // 4: first non-improvement.  Theta(n) = (R + S_{n-1}) * SPS[R + n]
-    for (int n = tid; n < nvalid; n += blockDim.x) {
-        const double tn = (double)R + (n > 0 ? val[n - 1] : 0.0);
-        const double tn1 = (double)R + val[n];
-        const double th_n = tn * sps_at(sps, n_sps, (long long)R + n);
-        const double th_n1 = tn1 * sps_at(sps, n_sps, (long long)R + n + 1);
-        if (!(th_n1 > th_n)) atomicMin(&s_nstar, n);
+#pragma unroll
+    for (int k = 0; k < kSchedMaxPer; ++k) {
+        const int n = tid + k * kSchedThreads;
+        if (n < nvalid) {
+            const double tn = (double)R + (n > 0 ? val[n - 1] : 0.0);
+            const double tn1 = (double)R + val[n];
+            const double th_n = tn * sp0[k];
+            const double th_n1 = tn1 * sp1[k];
+            if (!(th_n1 > th_n)) atomicMin(&s_nstar, n);
+        }
     }
     __syncthreads();
     const int ns = s_nstar == INT_MAX ? nvalid : s_nstar;
@@ -157,9 +185,10 @@ cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R,
     cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_begin(kPSchedule, s);
-    schedule_kernel<<<1, kSchedThreads, smem, s>>>(c, sps, n_sps, R, gamma, Np, len, theta, nstar);
+    e = launch_kernel(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, false, c, sps, n_sps, R, gamma, Np, len,
+                      theta, nstar);
     prof_end(s);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dspark

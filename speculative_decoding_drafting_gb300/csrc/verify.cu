@@ -125,32 +125,50 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
 }
 
 // ------------------------------------------------------------------ accept
+// One CTA per request.  Warp w reduces rows w, w + 8, ... of pass 1's
+// partials (the log-sum-exp of each P row, or its argmax at T = 0) while the
+// drafted tokens and their target logits P_k[x_k] are fetched, which do not
+// depend on it; then every verified position is tested at once and the first
+// rejection decides (everything after it is discarded).
 template <int PT, bool GREEDY>
 __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
+    __shared__ double s_lse[65];
+    __shared__ int s_arg[65];
+    __shared__ int s_x[64];
+    __shared__ float s_px[64];
+    __shared__ int s_first;
     pdl_launch_dependents();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= A.R) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+    const int r = blockIdx.x;
     const int G1 = A.gamma + 1, NCH = A.nch, V = A.V;
     const int L = verify_len_of(A, r);
     const float invT = GREEDY ? 1.f : 1.f / A.T;
     int32_t* out = A.out_tokens + (size_t)r * G1;
-    for (int i = lane; i < G1; i += 32) {
-        out[i] = -1;
-        if (A.lse_p) A.lse_p[(size_t)r * G1 + i] = NAN;
-        if (A.p_tok && i < A.gamma) A.p_tok[(size_t)r * A.gamma + i] = NAN;
+    if (tid < G1) {
+        out[tid] = -1;
+        if (A.lse_p && (GREEDY || tid > L)) A.lse_p[(size_t)r * G1 + tid] = NAN;   // rows 0..L: below
+        if (A.p_tok && tid < A.gamma) A.p_tok[(size_t)r * A.gamma + tid] = NAN;
     }
-    __syncwarp();
+    if (tid == 0) s_first = INT_MAX;
+    // drafted token x_k and its raw target logit, thread k - 1 for position k <= L
+    if (tid < L) {
+        int x = A.tokens[(size_t)r * A.gamma + tid];
+        if (x < 0 || x >= V) {
+            raise_status(A.ws, kStatBadToken);
+            x = 0;
+        }
+        s_x[tid] = x;
+        if (!GREEDY) s_px[tid] = ld_elem(A.P, PT, ((size_t)r * G1 + tid) * (size_t)V + x);
+    }
     const float2* parts = A.vparts + (size_t)r * G1 * NCH;
-    if (GREEDY) {
-        int j = 0;
-        for (int k = 1; k <= L + 1; ++k) {
-            const int row = k - 1;
+    for (int row = warp; row <= L; row += blockDim.x >> 5) {
+        const float2* pr = parts + (size_t)row * NCH;
+        if (GREEDY) {
             float best = -INFINITY;
             int arg = INT_MAX;
             for (int c = lane; c < NCH; c += 32) {
-                const float2 p = parts[(size_t)row * NCH + c];
+                const float2 p = pr[c];
                 const int a2 = __float_as_int(p.y);
                 if (p.x > best || (p.x == best && a2 < arg)) {
                     best = p.x;
@@ -166,103 +184,81 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
                     arg = a2;
                 }
             }
-            if (arg < 0 || arg >= V) arg = 0;
-            if (k == L + 1) {               // bonus: all L drafts matched
-                if (lane == 0) out[L] = arg;
-                break;
+            if (lane == 0) s_arg[row] = (arg < 0 || arg >= V) ? 0 : arg;
+        } else {
+            float m = -INFINITY;
+            for (int c = lane; c < NCH; c += 32) m = fmaxf(m, pr[c].x);
+            m = warp_max(m);
+            double sum = 0.0;
+            for (int c = lane; c < NCH; c += 32) {
+                const float2 p = pr[c];
+                sum += (double)p.y * (double)expf(p.x - m);      // exact difference: both are float maxima
             }
-            int x = A.tokens[(size_t)r * A.gamma + row];
-            if (lane == 0) out[row] = arg;  // equals x when accepted
-            if (x != arg) {
-                j = k;
-                break;
+            sum = warp_sum_d(sum);
+            if (lane == 0) {
+                const double l = (double)m + log(sum);
+                s_lse[row] = l;
+                A.lsep_ws[(size_t)r * G1 + row] = l;
+                if (A.lse_p) A.lse_p[(size_t)r * G1 + row] = l;
             }
-        }
-        if (lane == 0) {
-            const int acc = j ? j - 1 : L;
-            A.accept_len[r] = acc;
-            A.n_out[r] = acc + 1;
-            A.vstate[r] = make_int2(kModeDone, 0);
-        }
-        return;
-    }
-    // T > 0: log-sum-exp of every row the request reads.
-    double* lsep = A.lsep_ws + (size_t)r * G1;
-    for (int row = 0; row <= L; ++row) {
-        float m = -INFINITY;
-        for (int c = lane; c < NCH; c += 32) m = fmaxf(m, parts[(size_t)row * NCH + c].x);
-        m = warp_max(m);
-        double s = 0.0;
-        for (int c = lane; c < NCH; c += 32) {
-            const float2 p = parts[(size_t)row * NCH + c];
-            s += (double)p.y * (double)expf(p.x - m);      // exact difference: both are float maxima
-        }
-        s = warp_sum_d(s);
-        const double l = (double)m + log(s);
-        if (lane == 0) {
-            lsep[row] = l;
-            if (A.lse_p) A.lse_p[(size_t)r * G1 + row] = l;
         }
     }
-    __syncwarp();
-    // every verified position tested at once (lane k-1 takes position k), then
-    // the first rejection decides: everything after it is discarded
-    const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
-    const PhiloxKey key = philox_key(A.seed);
-    int j = 0;
-    for (int k0 = 1; k0 <= L && !j; k0 += 32) {
-        const int k = k0 + lane;
-        bool rej = false;
-        int x = 0;
-        double px = 0.0;
-        if (k <= L) {
-            x = A.tokens[(size_t)r * A.gamma + (k - 1)];
-            if (x < 0 || x >= V) {
-                raise_status(A.ws, kStatBadToken);
-                x = 0;
-            }
-            const size_t prow = ((size_t)r * G1 + (k - 1)) * (size_t)V;
+    __syncthreads();
+    // position k <= L (thread k - 1): accept or reject
+    double px = 0.0;
+    if (tid < L) {
+        const int k = tid + 1;
+        bool rej;
+        if (GREEDY) {
+            rej = s_x[tid] != s_arg[tid];
+        } else {
             // p(x) = exp(P_x / T - lse_P), the difference formed in double
-            px = exp_from_double((double)ld_elem(A.P, PT, prow + x) * (double)invT - lsep[k - 1]);
-            const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + (k - 1)];
-            const double u = rng_uniform_d(key, req, (uint32_t)k, 1u, 0u);
+            px = exp_from_double((double)s_px[tid] * (double)invT - s_lse[tid]);
+            const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + tid];
+            const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+            const double u = rng_uniform_d(philox_key(A.seed), req, (uint32_t)k, 1u, 0u);
             rej = !(u < ratio);
         }
-        const unsigned rmask = __ballot_sync(0xffffffffu, rej);
-        const int first = rmask ? (k0 + __ffs(rmask) - 1) : 0;      // first rejected position, if any here
-        if (k <= L && (!first || k <= first)) {
-            if (A.p_tok) A.p_tok[(size_t)r * A.gamma + (k - 1)] = (float)px;
-            if (!first || k < first) out[k - 1] = x;
-        }
-        j = first;
+        if (rej) atomicMin(&s_first, k);
     }
-    if (lane == 0) {
-        if (j) {
-            A.vstate[r] = make_int2(kModeResidual, j);
-            A.accept_len[r] = j - 1;
+    __syncthreads();
+    const int j = s_first == INT_MAX ? 0 : s_first;      // first rejected position, 0 if none
+    if (tid < L) {
+        const int k = tid + 1;
+        if (!GREEDY && A.p_tok && (!j || k <= j)) A.p_tok[(size_t)r * A.gamma + tid] = (float)px;
+        if (!j || k < j) out[tid] = s_x[tid];
+        else if (GREEDY && k == j) out[tid] = s_arg[tid];   // the target's own token replaces x_j
+    }
+    if (tid == 0) {
+        const int acc = j ? j - 1 : L;
+        if (GREEDY) {
+            if (!j) out[L] = s_arg[L];                   // bonus: all L drafts matched
+            A.vstate[r] = make_int2(kModeDone, 0);
         } else {
-            A.vstate[r] = make_int2(kModeBonus, L + 1);
-            A.accept_len[r] = L;
+            A.vstate[r] = j ? make_int2(kModeResidual, j) : make_int2(kModeBonus, L + 1);
         }
-        A.n_out[r] = A.accept_len[r] + 1;
+        A.accept_len[r] = acc;
+        A.n_out[r] = acc + 1;
     }
-    if (!j) return;
+    if (GREEDY || !j) return;
     // queue the rejecting request for the residual pass with its code e_j in bf16
-    int slot = 0;
-    if (lane == 0) {
-        slot = atomicAdd(A.rej_count, 1);
+    __shared__ int s_slot;
+    if (tid == 0) {
+        const int slot = atomicAdd(A.rej_count, 1);
         A.rej_list[slot] = r;
+        s_slot = slot;
     }
-    slot = __shfl_sync(0xffffffffu, slot, 0);
+    __syncthreads();
+    const int slot = s_slot;
     const float* e = A.code + ((size_t)r * A.gamma + (j - 1)) * A.r;
     bool inexact = false;
-    for (int i = lane; i < A.r; i += 32) {
+    for (int i = tid; i < A.r; i += blockDim.x) {
         const float v = e[i];
         const __nv_bfloat16 h = __float2bfloat16_rn(v);
         A.a_res[(size_t)slot * A.r + i] = __bfloat16_as_ushort(h);
         inexact |= __bfloat162float(h) != v;
     }
-    if (__any_sync(0xffffffffu, inexact) && lane == 0) atomicOr(A.vflags, 1u);
+    if (__syncthreads_or(inexact) && tid == 0) atomicOr(A.vflags, 1u);
 }
 
 // ------------------------------------------------------------------ residual (generic)
@@ -332,32 +328,39 @@ __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
 }
 
 // ------------------------------------------------------------------ sample
-// Inverse CDF down the binary sum tree over leaves[0 .. 2^levels): the CTA
-// first builds every inner node's mass (pairwise sums, in parallel), then one
-// thread walks from the root: at depth d it draws u = stream-2 uniform number
-// (level0 + d) and goes left iff u (mL + mR) < mL.  The chosen leaf index goes
-// to *out.  Every thread of the block must call it.
-__device__ void tree_descend(const double* leaves, double* tree, int levels, PhiloxKey key, uint32_t req,
-                             uint32_t pos, uint32_t level0, int* out) {
-    // tree[1] = root, tree[n + i] = leaves[i] for n = 2^levels (leaves read directly)
+// Inverse CDF down the binary sum tree over leaves[0 .. 2^levels): node k of
+// the heap (root 1, children 2k and 2k + 1, leaf i = node 2^levels + i)
+// holds the mass under it; at depth d the walk draws u = u_level[d] and goes
+// left iff u (mL + mR) < mL.  The uniforms do not depend on the path, so the
+// caller draws them in parallel beforehand.  The inner nodes are built by
+// eight warps, each over its own subtree with warp barriers only, then the
+// few nodes above the subtrees by one thread; the chosen leaf goes to *out.
+// Every thread of the (256-thread) block must call it.
+__device__ void tree_descend(const double* leaves, double* tree, int levels, const double* u_level, int* out) {
     const int n = 1 << levels;
-    for (int w = n >> 1; w >= 1; w >>= 1) {
-        for (int i = threadIdx.x; i < w; i += blockDim.x) {
-            const double l = (w == n >> 1) ? leaves[2 * i] : tree[2 * (w + i)];
-            const double rr = (w == n >> 1) ? leaves[2 * i + 1] : tree[2 * (w + i) + 1];
-            tree[w + i] = l + rr;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ls = levels >= 3 ? 3 : 0;          // log2 of the number of subtrees
+    const int S = 1 << ls;
+    auto mass = [&](int k) { return k >= n ? leaves[k - n] : tree[k]; };
+    if (warp < S) {
+        for (int h = levels - 1; h >= ls; --h) {     // depth h: nodes [2^h, 2^(h+1)), 2^(h-ls) per subtree
+            const int per = 1 << (h - ls);
+            const int k0 = (1 << h) + warp * per;
+            for (int i = lane; i < per; i += 32) {
+                const int k = k0 + i;
+                tree[k] = mass(2 * k) + mass(2 * k + 1);
+            }
+            __syncwarp();
         }
-        __syncthreads();
     }
+    __syncthreads();
     if (threadIdx.x == 0) {
-        int node = 1;   // heap index; children 2 node, 2 node + 1
+        for (int k = S - 1; k >= 1; --k) tree[k] = mass(2 * k) + mass(2 * k + 1);
+        int node = 1;
         for (int d = 0; d < levels; ++d) {
             const int lc = 2 * node;
-            const bool leaf_level = (d == levels - 1);
-            const double mL = leaf_level ? leaves[lc - n] : tree[lc];
-            const double mR = leaf_level ? leaves[lc + 1 - n] : tree[lc + 1];
-            const double u = rng_uniform_d(key, req, pos, 2u, level0 + (uint32_t)d);
-            node = (u * (mL + mR) < mL) ? lc : lc + 1;
+            const double mL = mass(lc), mR = mass(lc + 1);
+            node = (u_level[d] * (mL + mR) < mL) ? lc : lc + 1;
         }
         *out = levels > 0 ? node - n : 0;
     }
@@ -369,34 +372,42 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     __shared__ double tree[1024];      // inner nodes of the sum tree over cm
     __shared__ float e_sh[1024];
     __shared__ double sh[8];
-    pdl_launch_dependents();
-    pdl_wait();
+    __shared__ double s_u[32];         // the uniform of every tree level
     __shared__ int s_chunk, s_leaf;
     __shared__ int s_use_p;
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     const int2 st = A.vstate[r];
     if (st.x == kModeDone) return;
     const int mode = st.x, pos = st.y;
     const int V = A.V, G1 = A.gamma + 1;
     const int L = ceil_log2_i(V);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
-    const PhiloxKey key = philox_key(A.seed);
+    if (tid < L) s_u[tid] = rng_uniform_d(philox_key(A.seed), req, (uint32_t)pos, 2u, (uint32_t)tid);
     const double lp = A.lsep_ws[(size_t)r * G1 + (pos - 1)];
     if (mode == kModeResidual)
-        for (int i = threadIdx.x; i < A.r; i += blockDim.x)
-            e_sh[i] = A.code[((size_t)r * A.gamma + (pos - 1)) * A.r + i];
-    // chunk masses: 256-wide residual masses, or 1024-wide masses of p
+        for (int i = tid; i < A.r; i += blockDim.x) e_sh[i] = A.code[((size_t)r * A.gamma + (pos - 1)) * A.r + i];
+    // chunk masses: 256-wide residual masses (their total decides whether the
+    // residual is empty), or 1024-wide masses of p
     bool use_p = mode != kModeResidual;
     if (!use_p) {
+        const int Ltop = L > kRChunkLog2 ? L - kRChunkLog2 : 0;
         double tot = 0.0;
-        for (int c = threadIdx.x; c < A.nch256; c += blockDim.x) {
-            const float4 q4 = *reinterpret_cast<const float4*>(A.rpart + ((size_t)r * A.nch256 + c) * 4);
-            tot += (((double)q4.x + (double)q4.y) + (double)q4.z) + (double)q4.w;
+        for (int c = tid; c < (1 << Ltop); c += blockDim.x) {
+            double m = 0.0;
+            if (c < A.nch256) {
+                const float4 q4 = *reinterpret_cast<const float4*>(A.rpart + ((size_t)r * A.nch256 + c) * 4);
+                m = (((double)q4.x + (double)q4.y) + (double)q4.z) + (double)q4.w;
+            }
+            cm[c] = m;
+            tot += m;
         }
         tot = warp_sum_d(tot);
-        if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = tot;
+        if (lane == 0) sh[warp] = tot;
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (tid == 0) {
             double t = 0.0;
             for (int i = 0; i < 8; ++i) t += sh[i];
             s_use_p = t > 0.0 ? 0 : 1;        // empty residual (rounding only): draw from p_j
@@ -405,38 +416,42 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
         use_p = s_use_p != 0;
     }
     const int clog = use_p ? kChunkLog2 : kRChunkLog2;
-    const int nch = use_p ? A.nch : A.nch256;
     const int Ltop = L > clog ? L - clog : 0;
-    const int nleaf_top = 1 << Ltop;      // <= 1024 for V <= 2^20 and 256-wide chunks up to 2^18
-    for (int c = threadIdx.x; c < nleaf_top; c += blockDim.x) {
-        double m = 0.0;
-        if (c < nch) {
-            if (!use_p) {
-                const float4 q4 = *reinterpret_cast<const float4*>(A.rpart + ((size_t)r * A.nch256 + c) * 4);
-                m = (((double)q4.x + (double)q4.y) + (double)q4.z) + (double)q4.w;
-            } else {
+    if (use_p) {
+        for (int c = tid; c < (1 << Ltop); c += blockDim.x) {
+            double m = 0.0;
+            if (c < A.nch) {
                 const float2 p2 = A.vparts[((size_t)r * G1 + (pos - 1)) * A.nch + c];
                 m = (double)p2.y * exp_from_double((double)p2.x - lp);
             }
+            cm[c] = m;
         }
-        cm[c] = m;
     }
     __syncthreads();
     // top levels over the chunk masses
-    tree_descend(cm, tree, Ltop, key, req, (uint32_t)pos, 0u, &s_chunk);
+    tree_descend(cm, tree, Ltop, s_u, &s_chunk);
     __syncthreads();
     const int chunk = s_chunk;
-    // exact leaf weights of the chosen chunk, in double
+    // exact leaf weights of the chosen chunk, in double; the P (and U) values
+    // of this thread's columns are fetched first
     const int Lbot = L - Ltop;
-    const int nleaf = 1 << Lbot;
+    const int nleaf = 1 << Lbot;           // <= 256 (residual) or 1024 (p)
     const double invT = 1.0 / (double)A.T;
-    // residual: B = e W2 on the chunk's (at most 256) columns first.  Warp w
-    // takes rank rows w, w + 8, ..., lane l columns 8l .. 8l + 7, a batch of
-    // rows' loads in flight at once; the warps' sums are added in a fixed order.
+    float pvals[4], uval = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int i = tid + t * 256;
+        const int v = (chunk << clog) + i;
+        pvals[t] = (i < nleaf && v < V) ? ld_elem(A.P, PT, ((size_t)r * G1 + (pos - 1)) * V + v) : 0.f;
+    }
+    if (!use_p && tid < nleaf && (chunk << clog) + tid < V)
+        uval = ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + (chunk << clog) + tid);
+    // residual: B = e W2 on the chunk's (at most 256) columns.  Warp w takes
+    // rank rows w, w + 8, ..., lane l columns 8l .. 8l + 7, a batch of rows'
+    // loads in flight at once; the warps' sums are added in a fixed order.
     __shared__ float s_b[8][kRChunk];
     if (!use_p) {
         constexpr int kBatch = WT == DSPARK_BF16 ? 16 : 8;
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const int c0 = (chunk << clog) + 8 * lane;
         float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int i0 = warp; i0 < A.r; i0 += kBatch * 8) {
@@ -459,19 +474,21 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
         __syncthreads();
     }
     const double lq = (mode == kModeResidual) ? A.lse[(size_t)r * A.gamma + (pos - 1)] : 0.0;
-    for (int i = threadIdx.x; i < nleaf; i += blockDim.x) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int i = tid + t * 256;
+        if (i >= nleaf) break;
         const int v = (chunk << clog) + i;
         double w = 0.0;
         if (v < V) {
-            const double pv =
-                exp_from_double((double)ld_elem(A.P, PT, ((size_t)r * G1 + (pos - 1)) * V + v) * invT - lp);
+            const double pv = exp_from_double((double)pvals[t] * invT - lp);
             if (use_p) {
                 w = pv;
             } else {
                 float b = 0.f;
 #pragma unroll
                 for (int w8 = 0; w8 < 8; ++w8) b += s_b[w8][i];
-                const double z = ((double)ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + v) + (double)b) * invT;
+                const double z = ((double)uval + (double)b) * invT;
                 const double qv = exp_from_double(z - lq);
                 w = pv > qv ? pv - qv : 0.0;
             }
@@ -479,9 +496,9 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
         cm[i] = w;
     }
     __syncthreads();
-    tree_descend(cm, tree, Lbot, key, req, (uint32_t)pos, (uint32_t)Ltop, &s_leaf);
+    tree_descend(cm, tree, Lbot, s_u + Ltop, &s_leaf);
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         int y = (chunk << clog) + s_leaf;
         if (y >= V) y = V - 1;
         A.out_tokens[(size_t)r * G1 + (pos - 1)] = y;
@@ -547,7 +564,7 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
         prof_end(s);
         if (e != cudaSuccess) return e;
         prof_begin(kPVerifyAccept, s);
-        e = launch_kernel(verify_accept<PT, true>, dim3((a.R + 7) / 8), dim3(256), 0, s, true, a);
+        e = launch_kernel(verify_accept<PT, true>, dim3(a.R), dim3(256), 0, s, true, a);
         prof_end(s);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
@@ -556,7 +573,7 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     prof_end(s);
     if (e != cudaSuccess) return e;
     prof_begin(kPVerifyAccept, s);
-    e = launch_kernel(verify_accept<PT, false>, dim3((a.R + 7) / 8), dim3(256), 0, s, true, a);
+    e = launch_kernel(verify_accept<PT, false>, dim3(a.R), dim3(256), 0, s, true, a);
     prof_end(s);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;

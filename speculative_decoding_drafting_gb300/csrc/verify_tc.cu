@@ -12,8 +12,12 @@
 // its own j), so no tensor map describes them: every epilogue warp fetches the
 // 16 columns of its own 32 rows with cp.async, two tiles ahead, into padded
 // shared rows (conflict-free for the row-per-thread reads), while the rank-r
-// product runs as tcgen05.mma (M = 128 requests, N = 64 columns, K = r) with
-// W2 tiles from TMA, as in the draft sweep.
+// product runs as tcgen05.mma (M = 128 requests, N = 64 columns, K = r): the
+// codes (A) sit in tensor memory next to the accumulators, W2 tiles come by
+// TMA through a six-stage ring.  As in the draft sweep, the M-groups of a
+// column slice form a cluster that shares every W2 stage by multicast; a
+// cluster member whose M-group has no rejecting requests still runs the W2
+// pipeline so that its peers are served.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -31,24 +35,26 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = 64;
-constexpr int kNB = 3;             // W2 stages (64 columns x 64 rows of r, 8 KB)
+constexpr int kNB = 6;             // W2 stages (64 columns x 64 rows of r, 8 KB)
 constexpr int kNS = 2;             // U/P row stages
 constexpr int kNACC = 2;
 constexpr int kEpiWG = 4;
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kEpiWarp0 = 3;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kACol = kNACC * kBN;   // A: columns [128, 128 + r/2) of tensor memory
 
 __host__ __device__ constexpr int pitch_of(int es) { return kBN * es + 16; }   // padded row, bytes
 __host__ __device__ constexpr size_t stage_bytes(int esu, int esp) {
     return (size_t)kBM * (pitch_of(esu) + pitch_of(esp));
 }
-__host__ __device__ constexpr size_t smem_bytes(int r, int esu, int esp) {
-    return 1024 + (size_t)(r / 64) * 16384 + (size_t)kNB * 8192 + (size_t)kNS * stage_bytes(esu, esp) + 256;
+__host__ __device__ constexpr size_t smem_bytes(int /*r*/, int esu, int esp) {
+    return 1024 + (size_t)kNB * 8192 + (size_t)kNS * stage_bytes(esu, esp) + 256;
 }
 
 struct ResParams {
+    const uint16_t* a_res;   // codes of the rejecting requests, compact order, [.][r] bf16 bits
     const void* U;
     const void* P;
     const int* rej_count;
@@ -60,6 +66,7 @@ struct ResParams {
     float* rpart;            // [R][nch256][4]
     void* ws;
     int R, gamma, V, r, ntiles, nch256, nslices;
+    int cs;                  // CTAs per cluster (M-groups sharing each W2 stage)
     float c2;                // log2(e) / T
 };
 
@@ -73,18 +80,9 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 template <int UT, int PT>
 __global__ void __launch_bounds__(kThreads, 1)
-    residual_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ResParams p) {
+    residual_tc(const __grid_constant__ CUtensorMap tmB, ResParams p) {
     pdl_launch_dependents();
     pdl_wait();   // the rejecting requests come from the acceptance pass
     constexpr int esu = UT == DSPARK_F32 ? 4 : 2;
@@ -92,12 +90,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int pu = pitch_of(esu), pp = pitch_of(esp);
     const int n_rej = *p.rej_count;
     const int mg = blockIdx.y, slice = blockIdx.x;
-    if (mg * kBM >= n_rej || (*p.vflags & 1u)) return;      // nothing to do (block-uniform)
+    const int mg_first = mg - mg % p.cs;                      // first M-group of this cluster
+    if (mg_first * kBM >= n_rej || (*p.vflags & 1u)) return;  // nothing to do (cluster-uniform)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = base;
-    uint8_t* sB = sA + (size_t)(p.r / 64) * 16384;
+    uint8_t* sB = base;
     uint8_t* sS = sB + (size_t)kNB * 8192;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sS + (size_t)kNS * stage_bytes(esu, esp));
     uint64_t* a_full = bars;
@@ -117,13 +115,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_end = min(c_end * 4, p.ntiles);
     const int nt = t_end > t_begin ? t_end - t_begin : 0;
     const int kblocks = p.r / 64;
-    const int rows_here = min(kBM, n_rej - mg * kBM);
+    const int rows_here = max(0, min(kBM, n_rej - mg * kBM));   // 0 for an empty M-group
 
     if (threadIdx.x == 0) {
-        mbar_init(a_full, 1);
+        mbar_init(a_full, kEpiWarps);
         for (int i = 0; i < kNB; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);
+            mbar_init(&b_empty[i], (uint32_t)p.cs);   // one release per CTA of the cluster
         }
         for (int i = 0; i < kNS; ++i) {
             mbar_init(&s_full[i], 1);
@@ -135,12 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
     }
     if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();   // the peers' barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
@@ -148,10 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (rows of U_j and P_j are fetched by the epilogue warps themselves)
     } else if (warp == 2) {
         if (lane == 0) {
-            // ---------------- A (codes) and W2 producer
+            // ---------------- W2 producer: in a cluster of cs CTAs, CTA i loads
+            // K rows [i 64/cs, (i + 1) 64/cs) of every stage and multicasts them
             const uint64_t pol_last = policy_evict_last();
-            mbar_expect_tx(a_full, (uint32_t)kblocks * 16384u);
-            for (int kb = 0; kb < kblocks; ++kb) tma_load_2d(sA + kb * 16384, &tmA, a_full, kb * 64, mg * kBM, pol_last);
+            const int prow = 64 / p.cs;
+            const int ro = (int)cluster_ctarank() * prow;
+            const uint16_t mask = (uint16_t)((1u << p.cs) - 1u);
             int issued = 0;
             for (int g = 0; g < nt * kblocks; ++g) {
                 const int t = g / kblocks, kb = g - t * kblocks;
@@ -159,11 +158,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bph = (uint32_t)(g / kNB) & 1u;
                 if (!mbar_wait(&b_empty[bs], bph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&b_full[bs], 8192u);
-                tma_load_2d(sB + (size_t)bs * 8192, &tmB, &b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
+                if (p.cs == 1)
+                    tma_load_2d(sB + (size_t)bs * 8192, &tmB, &b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
+                else
+                    tma_load_2d_mc(sB + (size_t)bs * 8192 + ro * 128, &tmB, &b_full[bs], (t_begin + t) * kBN,
+                                   kb * 64 + ro, mask, pol_last);
                 issued = g + 1;
             }
+            // the last release of every stage (the peers' included) lands
+            // here before the CTA may exit
+            for (int g = (issued > kNB ? issued - kNB : 0); g < issued && !*abort_flag; ++g)
+                mbar_wait(&b_empty[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag);
             if (*abort_flag) {
-                mbar_wait_for(a_full, 0, kWaitLimitNs);
                 for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
                     mbar_wait_for(&b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitNs);
             }
@@ -191,11 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t* bstage = sB + (size_t)bs * 8192;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(sA + kb * 16384 + kk * 32, 16, 1024);
+                        // A: 16 K values = 8 tensor-memory columns per step
+                        const uint32_t at = tmem + kACol + (uint32_t)(kb * 32 + kk * 8);
                         const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
-                        umma_bf16(d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                        umma_bf16_ts(d, at, bd, idesc, (kb | kk) ? 1u : 0u);
                     }
-                    umma_commit(&b_empty[bs]);
+                    if (p.cs > 1)
+                        umma_commit_mc(&b_empty[bs], (uint16_t)((1u << p.cs) - 1u));
+                    else
+                        umma_commit(&b_empty[bs]);
                 }
                 if (!ok) break;
                 umma_commit(&acc_full[buf]);
@@ -207,6 +217,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int rit = q * 32 + lane;
         const bool row_ok = rit < rows_here;
+        {
+            // A operand: this thread's share (r/8 columns, r/4 values) of its
+            // row's code goes to tensor memory; column j of the row holds the
+            // bf16 values 2j (low half) and 2j + 1 (high half)
+            const int ncol = p.r / 8;
+            const int c0 = wg * ncol;
+            for (int c = 0; c < ncol; c += 8) {
+                uint32_t v[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (row_ok) {
+                    const uint4* src =
+                        reinterpret_cast<const uint4*>(p.a_res + (size_t)(mg * kBM + rit) * p.r + 2 * (c0 + c));
+                    const uint4 a0 = src[0], a1 = src[1];
+                    v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+                    v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+                }
+                tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + kACol + (uint32_t)(c0 + c), v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full);
+        }
         const int r = row_ok ? p.rej_list[mg * kBM + rit] : 0;
         const int j = row_ok ? p.vstate[r].y : 1;
         // log2-domain normalisers, split hi + lo so the exponent is formed to
@@ -337,32 +369,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0 && *abort_flag) raise_status(p.ws, kStatTimeout);
+    if (*abort_flag) {
+        // a peer's multicast copies or releases may still be on their way to
+        // this CTA's shared memory: give them a millisecond before leaving
+        if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+    }
+    cluster_sync();   // no CTA leaves while a peer may still write into it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
+// Clusters of `cs` residual CTAs that fit on the device at once (0 if unknown).
+template <int UT, int PT>
+int active_clusters(int cs, size_t smem) {
+    static int cache[3] = {0, 0, 0};
+    const int ci = cs == 4 ? 2 : cs - 1;
+    if (cache[ci]) return cache[ci];
+    auto kern = residual_tc<UT, PT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, cs, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cache[ci] = n;
+    return n;
+}
+
 template <int UT, int PT>
 cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
-    CUtensorMap tmA, tmB;
-    const int rpad = (a.R + kBM - 1) / kBM * kBM;
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)a.r, (cuuint64_t)rpad};
-        cuuint64_t str[1] = {(cuuint64_t)a.r * 2};
-        cuuint32_t box[2] = {64, kBM};
-        if (!draft_tc_make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.a_res, dims, str, box))
-            return cudaErrorInvalidValue;
+    constexpr int esu = UT == DSPARK_F32 ? 4 : 2, esp = PT == DSPARK_F32 ? 4 : 2;
+    const size_t smem = smem_bytes(a.r, esu, esp);
+    // M-groups per cluster: the largest of 4, 2, 1 dividing the number of groups
+    const int ng = (a.R + kBM - 1) / kBM;
+    int cs = ng % 4 == 0 ? 4 : (ng % 2 == 0 ? 2 : 1);
+    int ctas = num_sms();
+    if (cs > 1) {
+        const int nc = active_clusters<UT, PT>(cs, smem);
+        if (nc > 0)
+            ctas = nc * cs;
+        else
+            cs = 1;
     }
+    CUtensorMap tmB;
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
         cuuint64_t str[1] = {(cuuint64_t)a.V * 2};
-        cuuint32_t box[2] = {kBN, 64};
+        cuuint32_t box[2] = {kBN, (cuuint32_t)(64 / cs)};
         if (!draft_tc_make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
             return cudaErrorInvalidValue;
     }
     ResParams p;
+    p.a_res = a.a_res;
+    p.cs = cs;
     p.U = a.U;
     p.P = a.P;
     p.rej_count = a.rej_count;
@@ -379,19 +454,30 @@ cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     p.r = a.r;
     p.ntiles = (a.V + kBN - 1) / kBN;
     p.nch256 = a.nch256;
-    const int ng = (a.R + kBM - 1) / kBM;
-    int ns = num_sms() / ng;
+    int ns = ctas / ng;
     if (ns < 1) ns = 1;
     if (ns > a.nch256) ns = a.nch256;
     p.nslices = ns;
     p.c2 = 1.4426950408889634f / a.T;
-    constexpr int esu = UT == DSPARK_F32 ? 4 : 2, esp = PT == DSPARK_F32 ? 4 : 2;
-    const size_t smem = smem_bytes(a.r, esu, esp);
     auto kern = residual_tc<UT, PT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ns, ng, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)cs;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     prof_begin(kPVerifyResidualTc, s);
-    e = launch_kernel(kern, dim3(ns, ng), dim3(kThreads), smem, s, true, tmA, tmB, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmB, p);
     prof_end(s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

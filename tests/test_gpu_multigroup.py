@@ -47,13 +47,17 @@ def test_draft_parity_multigroup(name):
     np.testing.assert_array_equal(g["code"][m], o["code"][m].astype(np.float32))
 
 
-@pytest.mark.parametrize("name", ["mg2", "mg3"])
-def test_verify_parity_multigroup(name):
+@pytest.mark.parametrize("name,mode", [("mg2", "all"), ("mg3", "all"), ("mg4", "all"), ("mg4", "random")])
+def test_verify_parity_multigroup(name, mode):
+    """The residual pass runs one CTA per 128 rejecting requests and column
+    slice, clusters of 2 or 4 M-groups sharing W2; with random verify lengths
+    fewer requests reject and the last M-groups of a cluster may be empty."""
     w = MULTI[name]
     x = synth.gen_all(w)
     dr = oracle_draft(w, x, 8)
-    g = gpu_verify_on(w, x, dr, 8)
-    o = oracle_verify_on(w, x, dr, 8)
+    vl = None if mode == "all" else np.random.default_rng(5).integers(0, w.gamma + 1, w.R).astype(np.int32)
+    g = gpu_verify_on(w, x, dr, 8, verify_len=vl)
+    o = oracle_verify_on(w, x, dr, 8, verify_len=vl)
     n, nflag = compare_verify(g, o, np.ones(w.R, bool), tag=name)
     assert n + nflag == w.R and nflag <= max(2, w.R // 50)
 
