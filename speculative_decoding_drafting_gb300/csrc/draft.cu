@@ -74,39 +74,64 @@ __device__ int finish_greedy(const DraftArgs& A, int r, int kprev, const DraftPa
     return s_x;
 }
 
-// Block-wide argmax of (key, index), ties to the lower index; result in
-// thread 0's return value.
-__device__ void block_argmax(float& key, int& idx) {
-    __shared__ float sk[32];
-    __shared__ int si[32];
+// Warp-wide merge of (online log-sum-exp pair M, S with S = sum 2^(lm - M);
+// race winner key, index); every lane ends with the warp's result.
+__device__ __forceinline__ void merge_lse_race(float& M, float& S, float& key, int& idx) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
         const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
         const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (m2 != -INFINITY) {
+            if (M == -INFINITY) {
+                M = m2;
+                S = s2;
+            } else if (m2 > M) {
+                S = fmaf(S, ex2_approx(M - m2), s2);
+                M = m2;
+            } else {
+                S = fmaf(s2, ex2_approx(m2 - M), S);
+            }
+        }
         if (key_better(k2, i2, key, idx)) {
             key = k2;
             idx = i2;
         }
     }
+}
+
+// Block-wide argmax of (key, index), ties to the lower index, with a payload
+// that travels with the winner; thread 0 ends with the result.
+__device__ void block_argmax_with(float& key, int& idx, float& pay) {
+    __shared__ float sk[32], sp[32];
+    __shared__ int si[32];
+    auto warp_step = [&]() {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
+            const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+            const float p2 = __shfl_xor_sync(0xffffffffu, pay, o);
+            if (key_better(k2, i2, key, idx)) {
+                key = k2;
+                idx = i2;
+                pay = p2;
+            }
+        }
+    };
+    warp_step();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-    __syncthreads();
     if (lane == 0) {
         sk[warp] = key;
         si[warp] = idx;
+        sp[warp] = pay;
     }
     __syncthreads();
     if (warp == 0) {
         key = lane < nw ? sk[lane] : -INFINITY;
         idx = lane < nw ? si[lane] : INT_MAX;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
-            const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-            if (key_better(k2, i2, key, idx)) {
-                key = k2;
-                idx = i2;
-            }
-        }
+        pay = lane < nw ? sp[lane] : 0.f;
+        warp_step();
     }
 }
 
@@ -120,9 +145,11 @@ template <int UT, int WT>
 __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
     constexpr int NW = kPrepThreads / 32;
     __shared__ float e_sh[1024];
-    __shared__ float s_red[2 * NW];
+    __shared__ float s_M[NW], s_S[NW], s_k[NW];
+    __shared__ int s_ci[NW];
     __shared__ int s_c, s_x;
-    __shared__ float s_lse2, s_yx;
+    __shared__ float s_lseM, s_lseL;
+    __shared__ int s_lseE;
     const int V = A.V, NC = A.nchunk;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
@@ -183,26 +210,35 @@ __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
         const int i = threadIdx.x + t * kPrepThreads;
         if (i < A.r) e_sh[i] = ev[t];
     }
-    // log-sum-exp over the block
+    // one block reduction for the chunks' log-sum-exp (online pair M, S) and
+    // the chunk race; the log-sum-exp stays as M + e + log2(mant) with
+    // S = mant 2^e, so that nothing is rounded at the magnitude of M
     {
-        const float m = warp_max(M);
-        if (lane == 0) s_red[warp] = m;
-        __syncthreads();
-        float mb = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < NW; ++i) mb = fmaxf(mb, s_red[i]);
-        const float sv = warp_sum((M == -INFINITY) ? 0.f : S * ex2_approx(M - mb));
-        if (lane == 0) s_red[NW + warp] = sv;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double tot = 0.0;
-            for (int i = 0; i < NW; ++i) tot += (double)s_red[NW + i];
-            s_lse2 = mb + (float)log2(tot);
+        merge_lse_race(M, S, kbest, cbest);
+        if (lane == 0) {
+            s_M[warp] = M;
+            s_S[warp] = S;
+            s_k[warp] = kbest;
+            s_ci[warp] = cbest;
         }
+        __syncthreads();
+        if (warp == 0) {
+            M = lane < NW ? s_M[lane] : -INFINITY;
+            S = lane < NW ? s_S[lane] : 0.f;
+            kbest = lane < NW ? s_k[lane] : -INFINITY;
+            cbest = lane < NW ? s_ci[lane] : INT_MAX;
+            merge_lse_race(M, S, kbest, cbest);
+            if (lane == 0) {
+                int e = 0;
+                const float mant = frexpf(S, &e);           // S = mant 2^e, mant in [1/2, 1)
+                s_lseM = M;
+                s_lseE = e;
+                s_lseL = log2f(mant);
+                s_c = (cbest >= 0 && cbest < NC) ? cbest : 0;
+            }
+        }
+        __syncthreads();
     }
-    block_argmax(kbest, cbest);
-    if (threadIdx.x == 0) s_c = (cbest >= 0 && cbest < NC) ? cbest : 0;
-    __syncthreads();
     const int c = s_c;
     // level 2: rebuild the chosen chunk's logits, B = e W2 on its 256 columns.
     // Thread j < 256 owns column c 256 + j; its U value is fetched first so
@@ -252,23 +288,24 @@ __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
         ix = v;
         yx = y;
     }
-    const int ix_own = ix;
-    block_argmax(kx, ix);
-    if (threadIdx.x == 0) s_x = ix;
-    __syncthreads();
-    if (ix_own == s_x) s_yx = yx;                     // the thread that owns the winner
-    __syncthreads();
+    // the winner, its logit travelling with it
+    block_argmax_with(kx, ix, yx);
     if (threadIdx.x == 0) {
-        int x = s_x;
+        int x = ix;
         const size_t o = (size_t)r * A.gamma + (kprev - 1);
         if (x < 0 || x >= V) {
             raise_status(A.ws, kStatBadToken);
             x = 0;
-            s_x = 0;
         }
+        s_x = x;
         A.tokens[o] = x;
-        A.q_tok[o] = (float)exp2((double)s_yx - (double)s_lse2);
-        A.lse[o] = 0.69314718055994531 * (double)s_lse2;
+        // q(x) = 2^(y_x - lse2), lse2 = M + e + l: the exponent formed in
+        // double, then 2^hi (1 + lo ln 2) with hi + lo = the exponent
+        const double lse2 = ((double)s_lseM + (double)s_lseE) + (double)s_lseL;
+        const double d = (double)yx - lse2;
+        const float dh = (float)d;
+        A.q_tok[o] = exp2f(dh) * (1.f + (float)(d - (double)dh) * kLn2);
+        A.lse[o] = 0.69314718055994531 * lse2;
     }
     __syncthreads();
     return s_x;

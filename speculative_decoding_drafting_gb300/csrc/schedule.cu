@@ -34,6 +34,72 @@ __device__ __forceinline__ double sps_at(const double* sps, int n_sps, long long
     return (B >= 0 && B < n_sps) ? sps[B] : 0.0;
 }
 
+// One compare-exchange of a bitonic pass: `mine` and `theirs` sit at
+// positions p and p ^ stride; the lower position keeps the smaller key when
+// the block of `size` containing p sorts ascending.
+__device__ __forceinline__ unsigned long long cmpx(unsigned long long mine, unsigned long long theirs, bool lower,
+                                                  bool up) {
+    const bool keep_min = lower == up;
+    return keep_min ? (mine < theirs ? mine : theirs) : (mine < theirs ? theirs : mine);
+}
+
+// Ascending bitonic sort of keys[0 .. Np), Np <= 2 kSchedThreads a power of
+// two: thread t holds positions 2t and 2t + 1 in registers, so passes of
+// stride 1 stay in the thread and strides 2 .. 32 are warp shuffles with
+// thread t ^ (stride / 2); strides >= 64 go through shared memory.
+__device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
+    const int t = threadIdx.x;
+    const bool live = 2 * t < Np;
+    unsigned long long k0 = live ? keys[2 * t] : ~0ull, k1 = live ? keys[2 * t + 1] : ~0ull;
+    for (int size = 2; size <= Np; size <<= 1) {
+        const bool up = ((2 * t) & size) == 0;
+        int stride = size >> 1;
+        if (stride >= 64) {
+            // cross-warp strides in shared memory, one pair per thread
+            if (live) {
+                keys[2 * t] = k0;
+                keys[2 * t + 1] = k1;
+            }
+            __syncthreads();
+            for (; stride >= 64; stride >>= 1) {
+                const int ls = __ffs(stride) - 1;
+                if (t < Np / 2) {
+                    const int lo = ((t >> ls) << (ls + 1)) | (t & (stride - 1));
+                    const int hi = lo + stride;
+                    const bool upp = (lo & size) == 0;
+                    const unsigned long long a = keys[lo], b = keys[hi];
+                    if ((a > b) == upp) {
+                        keys[lo] = b;
+                        keys[hi] = a;
+                    }
+                }
+                __syncthreads();
+            }
+            if (live) {
+                k0 = keys[2 * t];
+                k1 = keys[2 * t + 1];
+            }
+        }
+        for (; stride >= 2; stride >>= 1) {
+            const int pt = stride >> 1;                      // partner thread t ^ pt
+            const bool lower = (t & pt) == 0;
+            const unsigned long long o0 = __shfl_xor_sync(0xffffffffu, k0, pt);
+            const unsigned long long o1 = __shfl_xor_sync(0xffffffffu, k1, pt);
+            k0 = cmpx(k0, o0, lower, up);
+            k1 = cmpx(k1, o1, lower, up);
+        }
+        // stride 1: the thread's own pair
+        const unsigned long long lo = k0 < k1 ? k0 : k1, hi = k0 < k1 ? k1 : k0;
+        k0 = up ? lo : hi;
+        k1 = up ? hi : lo;
+    }
+    __syncthreads();
+    if (live) {
+        keys[2 * t] = k0;
+        keys[2 * t + 1] = k1;
+    }
+}
+
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c, const double* sps, int n_sps,
                                                                  int R, int gamma, int Np, int32_t* len,
                                                                  double* theta, int32_t* nstar) {
@@ -74,6 +140,9 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     }
     for (int i = N + tid; i < Np; i += blockDim.x) keys[i] = ~0ull;
     __syncthreads();
+    if (Np <= 2 * kSchedThreads) {
+        bitonic_sort_regs(keys, Np);
+    } else {
     for (int ls = 1; (1 << ls) <= Np; ++ls) {
         const int size = 1 << ls;
         for (int lst = ls - 1; lst >= 0; --lst) {
@@ -96,6 +165,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
                 __syncwarp();
         }
     }
+    }
     __syncthreads();
     // 3: scan of the sorted a (double), sequential within a thread's run
     const int per = (Np + blockDim.x - 1) / blockDim.x;
@@ -112,7 +182,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
         run += a;
         val[i] = run;
     }
-    atomicAdd(&s_nvalid, nv);
+    nv = __reduce_add_sync(0xffffffffu, (unsigned)nv);
+    if ((tid & 31) == 0) atomicAdd(&s_nvalid, nv);
     // block exclusive scan of the per-thread totals
     const int lane = tid & 31, warp = tid >> 5;
     double x = run;
@@ -139,17 +210,20 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     __syncthreads();
     const int nvalid = s_nvalid;
     // 4: first non-improvement.  Theta(n) = (R + S_{n-1}) * SPS[R + n]
+    int first = INT_MAX;
 #pragma unroll
     for (int k = 0; k < kSchedMaxPer; ++k) {
         const int n = tid + k * kSchedThreads;
-        if (n < nvalid) {
+        if (n < nvalid && first == INT_MAX) {
             const double tn = (double)R + (n > 0 ? val[n - 1] : 0.0);
             const double tn1 = (double)R + val[n];
             const double th_n = tn * sp0[k];
             const double th_n1 = tn1 * sp1[k];
-            if (!(th_n1 > th_n)) atomicMin(&s_nstar, n);
+            if (!(th_n1 > th_n)) first = n;
         }
     }
+    first = (int)__reduce_min_sync(0xffffffffu, (unsigned)first);
+    if ((tid & 31) == 0 && first != INT_MAX) atomicMin(&s_nstar, first);
     __syncthreads();
     const int ns = s_nstar == INT_MAX ? nvalid : s_nstar;
     // 5: lengths

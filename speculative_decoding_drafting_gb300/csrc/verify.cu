@@ -196,7 +196,11 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
             }
             sum = warp_sum_d(sum);
             if (lane == 0) {
-                const double l = (double)m + log(sum);
+                // log(sum) = e ln 2 + log(mant), mant in [1/2, 1): only the
+                // mantissa's logarithm is taken, in float (error ~1e-7)
+                int e = 0;
+                const double mant = frexp(sum, &e);
+                const double l = ((double)m + (double)e * 0.69314718055994531) + (double)logf((float)mant);
                 s_lse[row] = l;
                 A.lsep_ws[(size_t)r * G1 + row] = l;
                 if (A.lse_p) A.lse_p[(size_t)r * G1 + row] = l;
