@@ -108,6 +108,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def rank_request_ids(R: int, rank: int) -> np.ndarray:
+    """Request ids of one rank: every rank drafts and verifies its own block of
+    R requests (weak scaling, no data-path exchange)."""
+    return (np.arange(R) + rank * R).astype(np.uint32)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks: the job takes as long as its
+    slowest rank.  CPU tensors with gloo, device tensors with NCCL."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(positions_per_rank_step: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job positions per second: every rank's positions over the slowest
+    rank's time."""
+    return positions_per_rank_step * world * steps / (max_ms / 1000.0)
+
+
 def algorithmic_bytes(w, n_rej: float, verify_rows: int):
     """Bytes the cycle must move (each input element once; the residual pass
     re-reads U_j and P_j of every rejecting request and W2 once)."""
@@ -211,7 +235,7 @@ def main(argv=None):
     if w.head != "markov":
         raise SystemExit("bench times the Markov-head cycle")
     x = synth.gen_all(w)
-    req_ids = (np.arange(w.R) + rank * w.R).astype(np.uint32)   # distinct requests on every rank
+    req_ids = rank_request_ids(w.R, rank)                       # distinct requests on every rank
 
     def to_dev(a):
         t = torch.from_numpy(np.ascontiguousarray(a))
@@ -269,13 +293,8 @@ def main(argv=None):
     # also keep consecutive kernels from overlapping, so this pass is slower)
     prof_ms, _, _, launches = timed(args.steps, 1000, True)
     clk = clocks.stop()
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], device=devc, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
-    positions = w.R * w.gamma * world * args.steps
-    value = positions / (tot_ms / 1000.0)
+    tot_ms = max_over_ranks(sum(step_ms), world, devc)
+    value = job_throughput(w.R * w.gamma, world, args.steps, tot_ms)
 
     # kernel table from the per-launch events
     table = {}
@@ -331,12 +350,8 @@ def main(argv=None):
                 e2e_ms.append(a0.elapsed_time(a1))
         h2d = int(hU.numel() * hU.element_size() + hP.numel() * hP.element_size() + hA.numel() * 4 + hC.numel() * 4)
         d2h = int(h_out.numel() * 4 + h_n.numel() * 4)
-        e2e_tot = sum(e2e_ms)
-        if world > 1:
-            t = torch.tensor([e2e_tot], device=devc, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_tot = float(t.item())
-        e2e_value = w.R * w.gamma * world * len(e2e_ms) / (e2e_tot / 1000.0)
+        e2e_tot = max_over_ranks(sum(e2e_ms), world, devc)
+        e2e_value = job_throughput(w.R * w.gamma, world, len(e2e_ms), e2e_tot)
         e2e = {"value": round(e2e_value, 1), "unit": "positions/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / len(e2e_ms), 3)}
 
