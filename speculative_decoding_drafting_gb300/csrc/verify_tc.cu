@@ -74,12 +74,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-
 template <int UT, int PT>
 __global__ void __launch_bounds__(kThreads, 1)
     residual_tc(const __grid_constant__ CUtensorMap tmB, ResParams p) {
@@ -124,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&b_empty[i], (uint32_t)p.cs);   // one release per CTA of the cluster
         }
         for (int i = 0; i < kNS; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], kEpiWarps);
+            mbar_init(&s_full[i], 32 * kEpiWarps);   // every epilogue thread, once its copies land
+            mbar_init(&s_empty[i], kEpiWarps);       // every epilogue warp, once it has read the stage
         }
         for (int i = 0; i < kNACC; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -248,56 +247,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lq_hi = (float)lq2, lq_lo = (float)(lq2 - (double)lq_hi);
         const float lp_hi = (float)lp2, lp_lo = (float)(lp2 - (double)lp_hi);
         float csum = 0.f;
-        // Each warp fetches U_j and P_j for its own 32 rows and 16 columns of a
-        // tile with cp.async (instruction i: lane l takes row 8i + l/4, 16-byte
-        // piece l%4), kNS tiles ahead, into padded rows of its stage slot.
-        const int fr_row = lane >> 2, fr_piece = lane & 3;
+        // The 16 epilogue warps fetch a tile's U_j and P_j rows together with
+        // cp.async: warp e takes rows 8e .. 8e + 7 of the M-group and whole
+        // 64-column segments of them (256 B per f32 row, 16 lanes a row), kNS
+        // tiles ahead, into padded rows of the stage.  A stage is full when all
+        // 512 threads' copies have landed (s_full) and free again when all 16
+        // warps have read it (s_empty).
+        constexpr int pcs_u = 4 * esu, pcs_p = 4 * esp;        // 16-byte pieces per row segment
+        constexpr int rpi_u = 32 / pcs_u, rpi_p = 32 / pcs_p;  // rows per instruction
+        const int e = warp - kEpiWarp0;
         const char* fsrcU[4];
         const char* fsrcP[4];
-        bool fok[4];
+        int frU[4], frP[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int rr = q * 32 + 8 * i + fr_row;            // row inside the group
-            fok[i] = rr < rows_here;
+            frU[i] = 8 * e + i * rpi_u + lane / pcs_u;
+            frP[i] = 8 * e + i * rpi_p + lane / pcs_p;
             fsrcU[i] = nullptr;
             fsrcP[i] = nullptr;
-            if (fok[i]) {
-                const int r2 = p.rej_list[mg * kBM + rr];
-                const int j2 = p.vstate[r2].y;
-                fsrcU[i] = static_cast<const char*>(p.U) + ((size_t)r2 * p.gamma + (j2 - 1)) * (size_t)p.V * esu;
-                fsrcP[i] = static_cast<const char*>(p.P) + ((size_t)r2 * (p.gamma + 1) + (j2 - 1)) * (size_t)p.V * esp;
+            if (i * rpi_u < 8 && frU[i] < rows_here) {
+                const int r2 = p.rej_list[mg * kBM + frU[i]];
+                fsrcU[i] = static_cast<const char*>(p.U) + ((size_t)r2 * p.gamma + (p.vstate[r2].y - 1)) * (size_t)p.V * esu;
+            }
+            if (i * rpi_p < 8 && frP[i] < rows_here) {
+                const int r2 = p.rej_list[mg * kBM + frP[i]];
+                fsrcP[i] = static_cast<const char*>(p.P) + ((size_t)r2 * (p.gamma + 1) + (p.vstate[r2].y - 1)) * (size_t)p.V * esp;
             }
         }
-        auto fetch = [&](int tt) {
+        const int pu_lane = lane % pcs_u, pp_lane = lane % pcs_p;
+        // fill number tt into stage tt % kNS; false if a wait gave up
+        auto fetch = [&](int tt) -> bool {
+            const int stf = tt % kNS;
+            if (!mbar_wait(&s_empty[stf], ((uint32_t)(tt / kNS) & 1u) ^ 1u, abort_flag)) return false;
             if (tt < nt) {
-                const int vv = (t_begin + tt) * kBN + wg * 16;          // first column of this warp's slice
-                uint8_t* stage = sS + (size_t)(tt % kNS) * stage_bytes(esu, esp);
+                const int vt = (t_begin + tt) * kBN;              // first column of the tile
+                uint8_t* stage = sS + (size_t)stf * stage_bytes(esu, esp);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int rr = q * 32 + 8 * i + fr_row;
-                    // 16 columns = 64 B (f32) or 32 B (bf16) per row; piece fr_piece of it
-                    if (fok[i] && fr_piece * 16 < 16 * esu && vv + fr_piece * (16 / esu) < p.V)
-                        cp_async16(stage + (size_t)rr * pu + wg * 16 * esu + fr_piece * 16,
-                                   fsrcU[i] + (size_t)vv * esu + fr_piece * 16);
-                    if (fok[i] && fr_piece * 16 < 16 * esp && vv + fr_piece * (16 / esp) < p.V)
-                        cp_async16(stage + (size_t)kBM * pu + (size_t)rr * pp + wg * 16 * esp + fr_piece * 16,
-                                   fsrcP[i] + (size_t)vv * esp + fr_piece * 16);
+                    const int vu = vt + pu_lane * (16 / esu), vp = vt + pp_lane * (16 / esp);
+                    if (fsrcU[i] && vu < p.V)
+                        cp_async16(stage + (size_t)frU[i] * pu + pu_lane * 16, fsrcU[i] + (size_t)vu * esu);
+                    if (fsrcP[i] && vp < p.V)
+                        cp_async16(stage + (size_t)kBM * pu + (size_t)frP[i] * pp + pp_lane * 16,
+                                   fsrcP[i] + (size_t)vp * esp);
                 }
             }
-            cp_async_commit();
+            cp_async_arrive(&s_full[stf]);
+            return true;
         };
+        bool fok = true;
 #pragma unroll
-        for (int tt = 0; tt < kNS; ++tt) fetch(tt);
+        for (int tt = 0; tt < kNS; ++tt) fok = fok && fetch(tt);
         for (int t = 0; t < nt; ++t) {
             const int tile = t_begin + t;
             const int v0 = tile * kBN + wg * 16;
             const int buf = t % kNACC;
             const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
             const int st = t % kNS;
-            bool ready = mbar_wait(&acc_full[buf], aph, abort_flag);
+            bool ready = fok && mbar_wait(&acc_full[buf], aph, abort_flag);
+            ready = ready && mbar_wait(&s_full[st], (uint32_t)(t / kNS) & 1u, abort_flag);   // every warp's copies
             if (!__all_sync(0xffffffffu, ready)) break;
-            cp_async_wait<kNS - 1>();       // this thread's pieces of tile t have landed
-            __syncwarp();                   // ... and the rest of the warp's
             tc_fence_after();
             float y[16];
             tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 16), y);
@@ -349,8 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();                   // every lane has read stage st and the accumulator
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            fetch(t + kNS);                 // refill this stage slot with tile t + kNS
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[buf]);
+                mbar_arrive(&s_empty[st]);
+            }
+            fok = fetch(t + kNS);           // refill this stage slot with tile t + kNS
             if (row_ok) {
                 const int ncols = min(16, p.V - v0);
 #pragma unroll
@@ -366,6 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 csum = 0.f;
             }
         }
+        // the arrivals of the last fills (past the final tile) land before the CTA leaves
+        if (fok && !*abort_flag)
+            for (int tt = nt; tt < nt + kNS; ++tt)
+                mbar_wait(&s_full[tt % kNS], (uint32_t)(tt / kNS) & 1u, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
