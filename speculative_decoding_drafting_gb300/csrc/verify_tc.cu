@@ -74,11 +74,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
                  : "memory");
 }
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the barrier's count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 template <int UT, int PT>
 __global__ void __launch_bounds__(kThreads, 1)
     residual_tc(const __grid_constant__ CUtensorMap tmB, ResParams p) {
