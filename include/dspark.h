@@ -170,6 +170,9 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int r);
  *   p_tok      [R, gamma]     float  p_k(x_k) for tested positions (may be NULL)
  *   lse_p      [R, gamma + 1] double log-sum-exp of P_k / T for rows read (may be NULL)
  * Rows the request never reads hold NaN in p_tok / lse_p.
+ * Requirements as for drafting, and V <= 2^18 when T > 0 (the sampling tree
+ * keeps at most 1024 top-level nodes of 256 words; greedy takes V <= 2^20);
+ * larger vocabularies return DSPARK_ERR_SHAPE before anything is enqueued.
  */
 int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype,
                   const void* W2, int w_dtype,

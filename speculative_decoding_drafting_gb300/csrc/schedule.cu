@@ -13,9 +13,11 @@
 // One CTA of 1024 threads does the whole batch in shared memory:
 //   1. a = running float32 product of c along each request
 //   2. 64-bit keys (~bits(a) << 32 | r * gamma + j) bitonic-sorted ascending,
-//      i.e. a descending, then r, then j ascending; a <= 0 sorts last.  A
-//      pass with stride <= 32 only touches the 64 keys of its warp, so block
-//      barriers are needed only around passes of stride >= 64.
+//      i.e. a descending, then r, then j ascending; a <= 0 sorts last.  Up to
+//      2048 keys sit eight per thread in registers (warp shuffles below
+//      stride 256); larger batches sort in shared memory, where a pass with
+//      stride <= 32 only touches the 64 keys of its warp, so block barriers
+//      are needed only around passes of stride >= 64.
 //   3. tau_n = R + inclusive scan of the sorted a (double)
 //   4. Theta(n) = tau_n * SPS[R + n]; n* = first n with Theta(n+1) <= Theta(n)
 //   5. l_r = number of the first n* candidates that belong to r
@@ -43,28 +45,48 @@ __device__ __forceinline__ unsigned long long cmpx(unsigned long long mine, unsi
     return keep_min ? (mine < theirs ? mine : theirs) : (mine < theirs ? theirs : mine);
 }
 
-// Ascending bitonic sort of keys[0 .. Np), Np <= 2 kSchedThreads a power of
-// two: thread t holds positions 2t and 2t + 1 in registers, so passes of
-// stride 1 stay in the thread and strides 2 .. 32 are warp shuffles with
-// thread t ^ (stride / 2); strides >= 64 go through shared memory.
+// One intra-thread pass of stride S (1, 2 or 4) over a thread's eight keys
+// at positions p0 .. p0 + 7 of a bitonic merge of blocks of `size`.
+template <int S>
+__device__ __forceinline__ void intra_pass(unsigned long long (&k)[8], int p0, int size) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (e & S) continue;
+        const int f = e | S;
+        const bool up = ((p0 + e) & size) == 0;
+        const unsigned long long a = k[e], b = k[f];
+        if ((a > b) == up) {
+            k[e] = b;
+            k[f] = a;
+        }
+    }
+}
+
+// Ascending bitonic sort of keys[0 .. Np), Np <= 2048 a power of two.
+// Threads 0 .. 255 hold eight keys each (positions 8t .. 8t + 7) in
+// registers: strides 1, 2, 4 stay inside a thread, strides 8 .. 128 are
+// warp shuffles with thread t ^ (stride / 8), strides >= 256 go through
+// shared memory (all threads).  Every thread of the block must call it.
+constexpr int kSortThreads = 256;
 __device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
     const int t = threadIdx.x;
-    const bool live = 2 * t < Np;
-    unsigned long long k0 = live ? keys[2 * t] : ~0ull, k1 = live ? keys[2 * t + 1] : ~0ull;
+    const bool active = t < kSortThreads;           // whole warps
+    const bool live = active && 8 * t < Np;
+    unsigned long long k[8];
+    // positions past Np (Np < 8) are padding: they only ever meet each other
+#pragma unroll
+    for (int e = 0; e < 8; ++e) k[e] = (live && 8 * t + e < Np) ? keys[8 * t + e] : ~0ull;
     for (int size = 2; size <= Np; size <<= 1) {
-        const bool up = ((2 * t) & size) == 0;
         int stride = size >> 1;
-        if (stride >= 64) {
-            // cross-warp strides in shared memory, one pair per thread
-            if (live) {
-                keys[2 * t] = k0;
-                keys[2 * t + 1] = k1;
-            }
+        if (stride >= 256) {
+            if (live)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) keys[8 * t + e] = k[e];
             __syncthreads();
-            for (; stride >= 64; stride >>= 1) {
+            for (; stride >= 256; stride >>= 1) {
                 const int ls = __ffs(stride) - 1;
-                if (t < Np / 2) {
-                    const int lo = ((t >> ls) << (ls + 1)) | (t & (stride - 1));
+                for (int i = t; i < Np / 2; i += blockDim.x) {
+                    const int lo = ((i >> ls) << (ls + 1)) | (i & (stride - 1));
                     const int hi = lo + stride;
                     const bool upp = (lo & size) == 0;
                     const unsigned long long a = keys[lo], b = keys[hi];
@@ -75,29 +97,28 @@ __device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
                 }
                 __syncthreads();
             }
-            if (live) {
-                k0 = keys[2 * t];
-                k1 = keys[2 * t + 1];
+            if (live)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) k[e] = keys[8 * t + e];
+        }
+        if (active) {
+            for (; stride >= 8; stride >>= 1) {
+                const int pt = stride >> 3;                  // partner thread t ^ pt, same warp
+                const bool lower = (t & pt) == 0;
+                const bool up = ((8 * t) & size) == 0;       // size >= 16 here: one direction per thread
+#pragma unroll
+                for (int e = 0; e < 8; ++e) k[e] = cmpx(k[e], __shfl_xor_sync(0xffffffffu, k[e], pt), lower, up);
             }
+            if (stride >= 4) intra_pass<4>(k, 8 * t, size);
+            if (stride >= 2) intra_pass<2>(k, 8 * t, size);
+            intra_pass<1>(k, 8 * t, size);
         }
-        for (; stride >= 2; stride >>= 1) {
-            const int pt = stride >> 1;                      // partner thread t ^ pt
-            const bool lower = (t & pt) == 0;
-            const unsigned long long o0 = __shfl_xor_sync(0xffffffffu, k0, pt);
-            const unsigned long long o1 = __shfl_xor_sync(0xffffffffu, k1, pt);
-            k0 = cmpx(k0, o0, lower, up);
-            k1 = cmpx(k1, o1, lower, up);
-        }
-        // stride 1: the thread's own pair
-        const unsigned long long lo = k0 < k1 ? k0 : k1, hi = k0 < k1 ? k1 : k0;
-        k0 = up ? lo : hi;
-        k1 = up ? hi : lo;
     }
     __syncthreads();
-    if (live) {
-        keys[2 * t] = k0;
-        keys[2 * t + 1] = k1;
-    }
+    if (live)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (8 * t + e < Np) keys[8 * t + e] = k[e];
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c, const double* sps, int n_sps,
@@ -113,12 +134,14 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     const int tid = threadIdx.x;
     const int N = R * gamma;
 
-    // the SPS values step 4 reads (candidate n = tid + k blockDim needs
-    // SPS[R + n] and SPS[R + n + 1]), fetched now so their latency hides
-    // behind the sort
-    double sp0[kSchedMaxPer], sp1[kSchedMaxPer];
+    // the SPS values step 4 reads for this thread's first two candidates
+    // (n = tid + k blockDim needs SPS[R + n] and SPS[R + n + 1]), fetched now
+    // so their latency hides behind the sort; larger batches fetch the rest
+    // when they get there
+    constexpr int kEarly = 2;
+    double sp0[kEarly], sp1[kEarly];
 #pragma unroll
-    for (int k = 0; k < kSchedMaxPer; ++k) {
+    for (int k = 0; k < kEarly; ++k) {
         const int n = tid + k * kSchedThreads;
         sp0[k] = n < N ? sps_at(sps, n_sps, (long long)R + n) : 0.0;
         sp1[k] = n < N ? sps_at(sps, n_sps, (long long)R + n + 1) : 0.0;
@@ -140,7 +163,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     }
     for (int i = N + tid; i < Np; i += blockDim.x) keys[i] = ~0ull;
     __syncthreads();
-    if (Np <= 2 * kSchedThreads) {
+    if (Np <= 8 * kSortThreads) {
         bitonic_sort_regs(keys, Np);
     } else {
     for (int ls = 1; (1 << ls) <= Np; ++ls) {
@@ -217,8 +240,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
         if (n < nvalid && first == INT_MAX) {
             const double tn = (double)R + (n > 0 ? val[n - 1] : 0.0);
             const double tn1 = (double)R + val[n];
-            const double th_n = tn * sp0[k];
-            const double th_n1 = tn1 * sp1[k];
+            const double s0 = k < kEarly ? sp0[k < kEarly ? k : 0] : sps_at(sps, n_sps, (long long)R + n);
+            const double s1 = k < kEarly ? sp1[k < kEarly ? k : 0] : sps_at(sps, n_sps, (long long)R + n + 1);
+            const double th_n = tn * s0;
+            const double th_n1 = tn1 * s1;
             if (!(th_n1 > th_n)) first = n;
         }
     }
