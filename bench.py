@@ -108,6 +108,55 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+CSRC = os.path.join(ROOT, "speculative_decoding_drafting_gb300", "csrc")
+# kernel (as the library's profiling names it) -> (ncu summary under profiles/, its source file)
+KERNEL_PROFILES = {
+    "draft_sweep_tc": ("draft_sweep_tc_headline.md", "draft_tc.cu"),
+    "verify_pass1": ("verify_pass1_headline.md", "verify.cu"),
+    "verify_residual_tc": ("residual_tc_headline.md", "verify_tc.cu"),
+}
+
+
+def source_digest(cu_file: str) -> str:
+    """sha256 over a kernel's .cu file and every header of the library: a
+    capture's counters stay valid only while this digest is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    files = [os.path.join(CSRC, cu_file)] + sorted(
+        os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
+    files.append(os.path.join(ROOT, "include", "dspark.h"))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes (read + write) of one launch of `kernel` from its committed
+    ncu summary, or None if there is none or the kernel changed since."""
+    ent = KERNEL_PROFILES.get(kernel)
+    if not ent:
+        return None
+    path = os.path.join(ROOT, "profiles", ent[0])
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    import re
+    m = re.search(r"source sha256: ([0-9a-f]{64})", text)
+    if not m or m.group(1) != source_digest(ent[1]):
+        return None
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    tot = 0.0
+    for key in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+        m = re.search(re.escape(key) + r" = ([0-9.]+) (byte|Kbyte|Mbyte|Gbyte)", text)
+        if not m:
+            return None
+        tot += float(m.group(1)) * scale[m.group(2)]
+    return int(tot)
+
+
 def rank_request_ids(R: int, rank: int) -> np.ndarray:
     """Request ids of one rank: every rank drafts and verifies its own block of
     R requests (weak scaling, no data-path exchange)."""
@@ -317,8 +366,9 @@ def main(argv=None):
     if dom_bytes:
         achieved = dom_bytes / (dom_ms / dom_n / 1000.0) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                    "frac": round(achieved / hbm_peak, 4), "traffic": None, "kernel": dom_name,
-                    "peak_source": f"{peak_src} hbm_gbs"}
+                    "frac": round(achieved / hbm_peak, 4), "traffic": measured_traffic(dom_name),
+                    "kernel": dom_name, "peak_source": f"{peak_src} hbm_gbs",
+                    "algorithmic_bytes_per_launch": int(dom_bytes)}
     cycle_gbs = ab["total"] / (tot_ms / args.steps / 1000.0) / 1e9 if world == 1 else None
 
     # end to end through the C ABI with host buffers
