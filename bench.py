@@ -254,6 +254,51 @@ def run_reference(args):
     return 0
 
 
+def measure_rnn_draft(steps: int, warmup: int, devc, flush):
+    """The RNN-head variant of the draft at its own workload (rnn: R = 256,
+    gamma = 8, V = 151936, r = 256, d = 2048): draft positions per second,
+    L2 flushed between calls, and the per-kernel table of a profiled pass."""
+    import torch
+    from speculative_decoding_drafting_gb300 import binding
+    w = synth.WORKLOADS["rnn"]
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(devc)
+
+    U, anchor = to_dev(synth.gen_U(w)), to_dev(synth.gen_anchor(w))
+    W1, W2, Wgco, H = to_dev(synth.gen_W1(w)), to_dev(synth.gen_W2(w)), to_dev(synth.gen_Wgco(w)), to_dev(synth.gen_H(w))
+    d = binding.draft_rnn(U, anchor, W1, W2, Wgco, H, w.T, 1)
+    for i in range(warmup):
+        binding.draft_rnn(U, anchor, W1, W2, Wgco, H, w.T, 2 + i, ws=d["ws"], out=d)
+    stream = torch.cuda.current_stream()
+    ms = []
+    for prof in (False, True):
+        binding.profile_enable(prof)
+        for i in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            binding.draft_rnn(U, anchor, W1, W2, Wgco, H, w.T, 100 + i, ws=d["ws"], out=d)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if not prof:
+                ms.append(a.elapsed_time(b))
+        binding.profile_enable(False)
+    table = {}
+    for name, t in binding.profile_collect():
+        e = table.setdefault(name, [0, 0.0])
+        e[0] += 1
+        e[1] += t
+    per = float(np.mean(ms))
+    return {"workload": f"{w.name}: R={w.R} gamma={w.gamma} V={w.V} r={w.r} d={w.d} T={w.T} U f32, W/H/Wgco bf16",
+            "metric": "draft positions/s", "value": round(w.R * w.gamma / (per / 1000.0), 1),
+            "ms_per_draft": round(per, 4),
+            "kernels_us_per_launch": {k: round(1000 * v / n, 2) for k, (n, v) in table.items()}}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -263,6 +308,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-variants", action="store_true", help="skip the RNN-head draft measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -405,6 +451,10 @@ def main(argv=None):
         e2e = {"value": round(e2e_value, 1), "unit": "positions/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / len(e2e_ms), 3)}
 
+    variants = None
+    if rank == 0 and world == 1 and not args.no_variants:
+        variants = {"rnn_draft": measure_rnn_draft(max(3, args.steps // 2), 3, devc, flush)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(w, x)
@@ -434,6 +484,7 @@ def main(argv=None):
             "wall_s_timed": round(t_wall, 3),
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "variants": variants,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -31,6 +31,10 @@ cudaError_t launch_draft_tc_sweep(DraftArgs& a, int k, cudaStream_t s);
 
 constexpr int kPrepThreads = 512;   // threads of a prep CTA (one request)
 
+// Leading dimension of the GRU input rows in the workspace: 2r + d rounded
+// up to a multiple of 4 floats (16-byte rows; the padding holds zeros).
+__host__ __device__ __forceinline__ int gru_ldz(int r, int d) { return (2 * r + d + 3) & ~3; }
+
 // ------------------------------------------------------------------ reduce
 // Block-wide reduction of n partials into thread 0's RowAcc.
 __device__ RowAcc reduce_partials(const DraftPartial* p, int n) {
@@ -336,13 +340,20 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits_rn(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Write e (float) for request r at step k into code and the bf16 hi/lo split.
+// Write e (float) for request r at step k into code and its three-way bf16
+// split e = hi + mid + lo (each term rounds the remainder of the previous
+// ones; 3 x 8 significand bits cover a float's 24, so the sum is e exactly
+// for the codes drafting produces).
 __device__ __forceinline__ void store_code(const DraftArgs& A, int r, int k, int i, float e) {
     A.code[((size_t)r * A.gamma + (k - 1)) * A.r + i] = e;
     const uint16_t hi = f32_to_bf16_bits_rn(e);
     const float rest = e - bf16_bits_to_float(hi);
+    const uint16_t mid = f32_to_bf16_bits_rn(rest);
+    const float rest2 = rest - bf16_bits_to_float(mid);
+    const size_t plane = (size_t)A.R * A.r;
     A.ebf[(size_t)r * A.r + i] = hi;
-    A.ebf[(size_t)A.R * A.r + (size_t)r * A.r + i] = f32_to_bf16_bits_rn(rest);
+    A.ebf[plane + (size_t)r * A.r + i] = mid;
+    A.ebf[2 * plane + (size_t)r * A.r + i] = f32_to_bf16_bits_rn(rest2);
 }
 
 // prep(k) for the Markov head: x_{k-1} then e_k = W1[x_{k-1}].
@@ -363,12 +374,11 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, i
         store_code(A, r, k, i, ld_elem(A.W1, A.w_dtype, (size_t)x * A.r + i));
 }
 
-// prep(k) for the RNN head (blog section 3.2 RNNHead.step):
-//   z = [s_{k-1}, W1[x_{k-1}], h_k];  G = z Wgco = (gate | cand | out)
-//   s_k = sigmoid(gate) s_{k-1} + (1 - sigmoid(gate)) tanh(cand);  e_k = tanh(out)
+// prep(k) for the RNN head (blog section 3.2 RNNHead.step), first half:
+// x_{k-1}, then the GRU input z = [s_{k-1}, W1[x_{k-1}], h_k] of the request
+// goes to the workspace; rnn_gru (below) forms G = z Wgco for all requests.
 template <int UT, int WT>
 __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int k) {
-    extern __shared__ float zin[];   // 2r + d
     pdl_launch_dependents();
     pdl_wait();
     const int r = blockIdx.x;
@@ -386,29 +396,128 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int 
         return;
     }
     if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
-    const int Kin = 2 * rr + A.d;
+    const int Kin = 2 * rr + A.d, ldz = gru_ldz(rr, A.d);
+    float* z = A.zbuf + (size_t)r * ldz;
     for (int i = threadIdx.x; i < rr; i += blockDim.x) {
-        zin[i] = (k == 1) ? 0.f : srow[i];
-        zin[rr + i] = ld_elem(A.W1, A.w_dtype, (size_t)x * rr + i);
+        z[i] = (k == 1) ? 0.f : srow[i];
+        z[rr + i] = ld_elem(A.W1, A.w_dtype, (size_t)x * rr + i);
     }
     const unsigned short* Hb = static_cast<const unsigned short*>(A.H);
     for (int i = threadIdx.x; i < A.d; i += blockDim.x)
-        zin[2 * rr + i] = bf16_bits_to_float(Hb[((size_t)r * A.gamma + (k - 1)) * A.d + i]);
-    __syncthreads();
-    for (int j = threadIdx.x; j < rr; j += blockDim.x) {
-        float g = 0.f, c = 0.f, o = 0.f;
-        for (int i = 0; i < Kin; ++i) {
-            const float zi = zin[i];
-            const size_t row = (size_t)i * 3 * rr;
-            g = fmaf(zi, ld_elem(A.Wgco, A.w_dtype, row + j), g);
-            c = fmaf(zi, ld_elem(A.Wgco, A.w_dtype, row + rr + j), c);
-            o = fmaf(zi, ld_elem(A.Wgco, A.w_dtype, row + 2 * rr + j), o);
+        z[2 * rr + i] = bf16_bits_to_float(Hb[((size_t)r * A.gamma + (k - 1)) * A.d + i]);
+    for (int i = Kin + threadIdx.x; i < ldz; i += blockDim.x) z[i] = 0.f;
+}
+
+// The GRU step for all requests (blog section 3.2 RNNHead.step):
+//   G = z Wgco = (gate | cand | out);
+//   s_k = sigmoid(gate) s_{k-1} + (1 - sigmoid(gate)) tanh(cand);  e_k = tanh(out).
+// One CTA = 16 requests x 32 state columns j, with the gate, candidate and
+// output columns of those j (96 columns of Wgco), so the update has all three
+// at hand.  Thread (m, n): request m of the tile, columns n, n + 1.  K runs in
+// tiles of 64 with the next tile's loads in flight during the current one;
+// the sum over z still runs in index order (f32 FMAs).  VEC: bf16 Wgco with
+// r % 8 == 0, loaded 8 values at a time; otherwise element by element.
+constexpr int kGruTM = 16, kGruTN = 32, kGruTK = 64;
+template <int WT, bool VEC>
+__global__ void __launch_bounds__(256) rnn_gru(DraftArgs A, int k) {
+    __shared__ __align__(16) float zs[kGruTK][kGruTM];
+    __shared__ __align__(16) float ws[kGruTK][3 * kGruTN];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int rr = A.r, Kin = 2 * rr + A.d, ldz = gru_ldz(rr, A.d);
+    const int j0 = blockIdx.x * kGruTN, m0 = blockIdx.y * kGruTM;
+    const int t = threadIdx.x;
+    const int m = t >> 4, n = (t & 15) * 2;
+    // this thread's loads of a K tile: z as one float4 (row t / 16, columns
+    // 4 (t % 16) ..), Wgco as three 8-value pieces (see below)
+    float4 zr[1];
+    uint4 wr[3];
+    float wsc[24];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int i = 0; i < 1; ++i) {
+            const int f = t + 256 * i, mm = f >> 4, c4 = f & 15, row = m0 + mm;
+            zr[i] = (row < A.R && k0 + 4 * c4 < ldz)
+                        ? *reinterpret_cast<const float4*>(A.zbuf + (size_t)row * ldz + k0 + 4 * c4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float sg = 1.f / (1.f + expf(-g));
-        const float sprev = zin[j];
-        const float snew = sg * sprev + (1.f - sg) * tanhf(c);
-        srow[j] = snew;
-        store_code(A, r, k, j, tanhf(o));
+        if (VEC) {
+            // piece p = t + 256 i (i < 3): tile row p / 12, gate (p % 12) / 4, columns 8 (p % 4) ..
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const int pc = t + 256 * i, kk = pc / 12, g = (pc % 12) >> 2, c8 = pc & 3;
+                const int col = j0 + 8 * c8;
+                wr[i] = (k0 + kk < Kin && col < rr)
+                            ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(A.Wgco) +
+                                                                   (size_t)(k0 + kk) * 3 * rr + (size_t)g * rr + col))
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 24; ++i) {
+                const int e = t + 256 * i, kk = e / 96, c = e % 96, g = c / kGruTN, jj = c % kGruTN;
+                wsc[i] = (k0 + kk < Kin && j0 + jj < rr)
+                             ? ld_elem(A.Wgco, WT, (size_t)(k0 + kk) * 3 * rr + (size_t)g * rr + j0 + jj)
+                             : 0.f;
+            }
+        }
+    };
+    auto store = [&]() {
+#pragma unroll
+        for (int i = 0; i < 1; ++i) {
+            const int f = t + 256 * i, mm = f >> 4, c4 = f & 15;
+            zs[4 * c4 + 0][mm] = zr[i].x;
+            zs[4 * c4 + 1][mm] = zr[i].y;
+            zs[4 * c4 + 2][mm] = zr[i].z;
+            zs[4 * c4 + 3][mm] = zr[i].w;
+        }
+        if (VEC) {
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const int pc = t + 256 * i, kk = pc / 12, g = (pc % 12) >> 2, c8 = pc & 3;
+                const uint32_t w4[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
+                float* dst = &ws[kk][g * kGruTN + 8 * c8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    dst[2 * e] = bf16_bits_to_float(w4[e] & 0xFFFFu);
+                    dst[2 * e + 1] = bf16_bits_to_float(w4[e] >> 16);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 24; ++i) {
+                const int e = t + 256 * i;
+                ws[e / 96][e % 96] = wsc[i];
+            }
+        }
+    };
+    float acc[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+    load(0);
+    for (int k0 = 0; k0 < Kin; k0 += kGruTK) {
+        __syncthreads();                  // the previous tile has been read
+        store();
+        __syncthreads();
+        if (k0 + kGruTK < Kin) load(k0 + kGruTK);
+#pragma unroll 8
+        for (int kk = 0; kk < kGruTK; ++kk) {
+            const float zv = zs[kk][m];
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {
+                acc[g][0] = fmaf(zv, ws[kk][g * kGruTN + n], acc[g][0]);
+                acc[g][1] = fmaf(zv, ws[kk][g * kGruTN + n + 1], acc[g][1]);
+            }
+        }
+    }
+    const int row = m0 + m;
+    if (row >= A.R) return;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int j = j0 + n + q;
+        if (j >= rr) continue;
+        const float sg = 1.f / (1.f + expf(-acc[0][q]));
+        const float sprev = A.zbuf[(size_t)row * ldz + j];      // s_{k-1}, the first block of z
+        A.rnn_state[(size_t)row * rr + j] = sg * sprev + (1.f - sg) * tanhf(acc[1][q]);
+        store_code(A, row, k, j, tanhf(acc[2][q]));
     }
 }
 
@@ -531,12 +640,12 @@ __global__ void __launch_bounds__(256) draft_sweep_generic(DraftArgs A, int k) {
 // ------------------------------------------------------------------ host
 size_t draft_workspace_bytes(int R, int gamma, int V, int r, int d) {
     (void)gamma;
-    (void)d;
     const int ns = (V + kGenericSlice - 1) / kGenericSlice;
     const int ns_max = ns > 1024 ? ns : 1024;
     size_t off = sizeof(WsHeader);
     off = align_up(off + 2ull * R * ns_max * sizeof(DraftPartial), 256);
-    off = align_up(off + 2ull * R * r * sizeof(uint16_t), 256);
+    off = align_up(off + (size_t)R * gru_ldz(r, d) * sizeof(float), 256);   // GRU input z (RNN head)
+    off = align_up(off + 3ull * R * r * sizeof(uint16_t), 256);
     off = align_up(off + (size_t)R * r * sizeof(float), 256);
     off = align_up(off + (size_t)R * sizeof(uint32_t), 256);
     off = align_up(off + (size_t)R * ((V + kRChunk - 1) / kRChunk) * 4 * sizeof(float2), 256);
@@ -553,8 +662,10 @@ int draft_carve(DraftArgs& a, size_t ws_bytes) {
     a.parts = reinterpret_cast<DraftPartial*>(base + off);
     a.parts_stride = a.R * ns_max;
     off = align_up(off + 2ull * a.R * ns_max * sizeof(DraftPartial), 256);
+    a.zbuf = reinterpret_cast<float*>(base + off);
+    off = align_up(off + (size_t)a.R * gru_ldz(a.r, a.d) * sizeof(float), 256);
     a.ebf = reinterpret_cast<uint16_t*>(base + off);
-    off = align_up(off + 2ull * a.R * a.r * sizeof(uint16_t), 256);
+    off = align_up(off + 3ull * a.R * a.r * sizeof(uint16_t), 256);
     a.rnn_state = reinterpret_cast<float*>(base + off);
     off = align_up(off + (size_t)a.R * a.r * sizeof(float), 256);
     a.best = reinterpret_cast<uint32_t*>(base + off);
@@ -594,7 +705,6 @@ cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
     a.rnn = rnn ? 1 : 0;
     const bool use_tc = draft_tc_supported(a);
     a.n_slices = use_tc ? draft_tc_slices(a) : (a.V + kGenericSlice - 1) / kGenericSlice;
-    const size_t rnn_smem = (size_t)(2 * a.r + a.d) * sizeof(float);
     void (*prep_m)(DraftArgs, int);
     void (*prep_r)(DraftArgs, int);
     switch (a.u_dtype * 2 + a.w_dtype) {
@@ -603,17 +713,21 @@ cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
         case 2: prep_m = draft_prep_markov<DSPARK_BF16, DSPARK_F32>; prep_r = draft_prep_rnn<DSPARK_BF16, DSPARK_F32>; break;
         default: prep_m = draft_prep_markov<DSPARK_BF16, DSPARK_BF16>; prep_r = draft_prep_rnn<DSPARK_BF16, DSPARK_BF16>; break;
     }
-    if (rnn && rnn_smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(prep_r, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rnn_smem);
-        if (e != cudaSuccess) return e;
-    }
+    void (*gru)(DraftArgs, int) = a.w_dtype == DSPARK_F32 ? rnn_gru<DSPARK_F32, false>
+                                  : (a.r % 8 == 0 ? rnn_gru<DSPARK_BF16, true> : rnn_gru<DSPARK_BF16, false>);
+    const dim3 gru_grid((a.r + kGruTN - 1) / kGruTN, (a.R + kGruTM - 1) / kGruTM);
     for (int k = 1; k <= a.gamma + 1; ++k) {
         // prep(1) waits for the caller's work; every later launch overlaps
         // the previous kernel's tail
         cudaError_t e;
         if (rnn) {
             prof_begin(kPDraftPrepRnn, s);
-            e = launch_kernel(prep_r, dim3(a.R), dim3(kPrepThreads), rnn_smem, s, k > 1, a, k);
+            e = launch_kernel(prep_r, dim3(a.R), dim3(kPrepThreads), 0, s, k > 1, a, k);
+            prof_end(s);
+            if (e == cudaSuccess && k <= a.gamma) {
+                prof_begin(kPDraftRnnGru, s);
+                e = launch_kernel(gru, gru_grid, dim3(256), 0, s, true, a, k);
+            }
         } else {
             prof_begin(kPDraftPrep, s);
             e = launch_kernel(prep_m, dim3(a.R), dim3(kPrepThreads), 0, s, k > 1, a, k);

@@ -45,13 +45,12 @@ constexpr int kBM = 128;           // requests per CTA (one M-group)
 constexpr int kBN = 128;           // vocabulary columns per tile
 constexpr int kNB = 6;             // W2 stages, each 128 columns x 64 rows of r (16 KB)
 constexpr int kNU = 2;             // U stages
-constexpr int kNACC = 2;           // TMEM accumulators
+constexpr int kNACC = 2;           // TMEM accumulators (at most; one when A needs the room)
 constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 32 of a tile's 128 columns
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kEpiWarp0 = 3;       // warps 0..2: U producer, MMA issuer, W2 producer
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol = kNACC * kBN;   // A: columns [256, 256 + r/2) of tensor memory
 constexpr int kUStageBytes = kBM * kBN * 4;   // 64 KB (f32); bf16 uses half
 constexpr int kBStageBytes = 16384;
 
@@ -65,7 +64,8 @@ struct TcParams {
     int R, V, r, k;          // k = 1-based step
     int ntiles, nslices;
     float c2;                // log2(e) / T
-    int cs;                  // CTAs per cluster (M-groups sharing each W2 stage): 1, 2 or 4
+    int nsplit;              // bf16 terms of the code: 1 (bf16-exact codes) or 3 (f32 codes, hi + mid + lo)
+    int nacc;                // TMEM accumulators: 2, or 1 when the split A needs the room
 };
 
 struct Smem {
@@ -104,7 +104,59 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     return s;
 }
 
-template <int UT, bool GREEDY>
+// MMA issuer of one CTA (one thread): for every tile, r/64 W2 stages of four
+// K=16 steps, each step one MMA per bf16 term of the code (NS = 1 or 3) into
+// the tile's accumulator.  Every stage is released to all CTAs of the cluster.
+template <int NS, int CS>
+__device__ __forceinline__ void issue_mma(const Smem& S, const TcParams& p, uint32_t tmem, uint32_t acol, int nt,
+                                          int kblocks) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
+    volatile int* abort_flag = S.abort_flag;
+    // two accumulators, or one when three A blocks take the room (NS = 3, r > 128)
+    const bool two = NS == 1 || p.nacc == 2;
+    bool ok = mbar_wait(S.a_full, 0, abort_flag);
+    tc_fence_after();
+    for (int t = 0; ok && t < nt; ++t) {
+        const int buf = two ? (t & 1) : 0;
+        const uint32_t aph = (uint32_t)(two ? (t >> 1) : t) & 1u;
+        if (!mbar_wait(&S.acc_empty[buf], aph ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * kBN);
+        for (int kb = 0; ok && kb < kblocks; ++kb) {
+            const int g = t * kblocks + kb;
+            const int bs = g % kNB;
+            const uint32_t bph = (uint32_t)(g / kNB) & 1u;
+            if (!mbar_wait(&S.b_full[bs], bph, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint8_t* bstage = S.B + (size_t)bs * kBStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                // B is MN-major: 8-row K groups 1 KB apart, 64-column atoms 8 KB apart
+                const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 8192, 1024);
+                // A: 16 K values = 8 tensor-memory columns per step; each
+                // bf16 term of the code adds its product into the same accumulator
+#pragma unroll
+                for (int sp = 0; sp < NS; ++sp) {
+                    const uint32_t at = tmem + acol + (uint32_t)(sp * (p.r / 2) + kb * 32 + kk * 8);
+                    umma_bf16_ts(d, at, bd, idesc, (kb | kk | sp) ? 1u : 0u);
+                }
+            }
+            if (CS > 1)
+                umma_commit_mc(&S.b_empty[bs], (1u << CS) - 1u);
+            else
+                umma_commit(&S.b_empty[bs]);
+        }
+        if (!ok) break;
+        umma_commit(&S.acc_full[buf]);
+    }
+}
+
+// CS: CTAs per cluster (1, 2 or 4), a template parameter so that the
+// multicast masks below are compile-time constants
+template <int UT, bool GREEDY, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     draft_sweep_tc(const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmU, TcParams p) {
@@ -124,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(S.a_full, kEpiWarps);
         for (int i = 0; i < kNB; ++i) {
             mbar_init(&S.b_full[i], 1);
-            mbar_init(&S.b_empty[i], (uint32_t)p.cs);   // one release per CTA of the cluster
+            mbar_init(&S.b_empty[i], (uint32_t)CS);   // one release per CTA of the cluster
         }
         for (int i = 0; i < kNU; ++i) {
             mbar_init(&S.u_full[i], 1);
@@ -144,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();   // the peers' barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *S.tmem_holder;
+    const uint32_t acol = (uint32_t)(p.nacc * kBN);   // A: columns [acol, acol + nsplit r/2)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -168,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (*abort_flag)   // wind down: let the copies this thread issued land
                 for (int t = (issued > kNU ? issued - kNU : 0); t < issued; ++t)
-                    mbar_wait_for(&S.u_full[t % kNU], (uint32_t)(t / kNU) & 1u, kWaitLimitNs);
+                    mbar_wait_for(&S.u_full[t % kNU], (uint32_t)(t / kNU) & 1u, kWaitLimitCycles);
         }
     } else if (warp == 2) {
         if (lane == 0) {
@@ -178,10 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // in a cluster of cs CTAs, CTA i loads piece i (atom i / (cs/2),
             // K rows (i % (cs/2)) * 128/cs ..) and multicasts it to all
             const uint32_t rank = cluster_ctarank();
-            const int per = p.cs > 1 ? p.cs / 2 : 1;
+            constexpr int per = CS > 1 ? CS / 2 : 1;
             const int prow = 64 / per;
             const int atom = (int)rank / per, ro = ((int)rank % per) * prow;
-            const uint16_t mask = (uint16_t)((1u << p.cs) - 1u);
+            constexpr uint32_t mask = (1u << CS) - 1u;
             const int ng = nt * kblocks;
             int issued = 0;
             for (int g = 0; g < ng; ++g) {
@@ -192,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_expect_tx(&S.b_full[bs], (uint32_t)kBStageBytes);
                 uint8_t* st = S.B + (size_t)bs * kBStageBytes;
                 const int v0 = (t_begin + t) * kBN;
-                if (p.cs == 1) {
+                if (CS == 1) {
                     tma_load_2d(st, &tmB, &S.b_full[bs], v0, kb * 64, pol_last);
                     tma_load_2d(st + 8192, &tmB, &S.b_full[bs], v0 + 64, kb * 64, pol_last);
                 } else {
@@ -207,47 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&S.b_empty[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag);
             if (*abort_flag) {
                 for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
-                    mbar_wait_for(&S.b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitNs);
+                    mbar_wait_for(&S.b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitCycles);
             }
         }
     } else if (warp == 1) {
+        // ---------------- MMA issuer (the split count picks a straight-line body)
         if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
-            bool ok = mbar_wait(S.a_full, 0, abort_flag);
-            tc_fence_after();
-            for (int t = 0; ok && t < nt; ++t) {
-                const int buf = t % kNACC;
-                const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
-                if (!mbar_wait(&S.acc_empty[buf], aph ^ 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(buf * kBN);
-                for (int kb = 0; ok && kb < kblocks; ++kb) {
-                    const int g = t * kblocks + kb;
-                    const int bs = g % kNB;
-                    const uint32_t bph = (uint32_t)(g / kNB) & 1u;
-                    if (!mbar_wait(&S.b_full[bs], bph, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint8_t* bstage = S.B + (size_t)bs * kBStageBytes;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // A: 16 K values = 8 tensor-memory columns per step
-                        const uint32_t at = tmem + kACol + (uint32_t)(kb * 32 + kk * 8);
-                        // B is MN-major: 8-row K groups 1 KB apart, 64-column atoms 8 KB apart
-                        const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 8192, 1024);
-                        umma_bf16_ts(d, at, bd, idesc, (kb | kk) ? 1u : 0u);
-                    }
-                    if (p.cs > 1)
-                        umma_commit_mc(&S.b_empty[bs], (uint16_t)((1u << p.cs) - 1u));
-                    else
-                        umma_commit(&S.b_empty[bs]);
-                }
-                if (!ok) break;
-                umma_commit(&S.acc_full[buf]);
-            }
+            if (p.nsplit == 1)
+                issue_mma<1, CS>(S, p, tmem, acol, nt, kblocks);
+            else
+                issue_mma<3, CS>(S, p, tmem, acol, nt, kblocks);
         }
     } else {
         // ---------------- epilogue: thread = (request row, 32 columns of each tile)
@@ -261,20 +283,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         {
             // A operand: this thread's share (r/8 columns, r/4 values) of its
-            // row's code goes to tensor memory; column j of the row holds the
-            // bf16 values 2j (low half) and 2j + 1 (high half)
+            // row's code goes to tensor memory, one block of r/2 columns per
+            // bf16 term; column j of a block holds the values 2j (low half)
+            // and 2j + 1 (high half)
             const int ncol = p.r / 8;
             const int c0 = wg * ncol;
-            for (int c = 0; c < ncol; c += 8) {
-                uint32_t v[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                if (row_ok) {
-                    const uint4* src = reinterpret_cast<const uint4*>(p.ebf + (size_t)row * p.r + 2 * (c0 + c));
-                    const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
-                    v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-                    v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+            for (int sp = 0; sp < p.nsplit; ++sp)
+                for (int c = 0; c < ncol; c += 8) {
+                    uint32_t v[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    if (row_ok) {
+                        const uint4* src = reinterpret_cast<const uint4*>(p.ebf + (size_t)sp * p.R * p.r +
+                                                                          (size_t)row * p.r + 2 * (c0 + c));
+                        const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
+                        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+                        v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+                    }
+                    tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + acol + (uint32_t)(sp * (p.r / 2) + c0 + c), v);
                 }
-                tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + kACol + (uint32_t)(c0 + c), v);
-            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -288,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ib = INT_MAX;
         for (int t = 0; t < nt; ++t) {
             const int tile = t_begin + t;
-            const int buf = t % kNACC;
-            const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
+            const int buf = p.nacc == 2 ? (t & 1) : 0;
+            const uint32_t aph = (uint32_t)(p.nacc == 2 ? (t >> 1) : t) & 1u;
             const int us = t % kNU;
             const uint32_t uph = (uint32_t)(t / kNU) & 1u;
             bool ready = mbar_wait(&S.acc_full[buf], aph, abort_flag);
@@ -402,9 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a peer's multicast copies or releases may still be on their way to
         // this CTA's shared memory: give them a millisecond before leaving
         if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 1000000ull) {
-        }
+        spin_about_1ms();
     }
     cluster_sync();   // no CTA leaves while a peer may still write into it
     if (warp == 1) {
@@ -455,7 +478,7 @@ int active_clusters(int cs, size_t smem) {
     static int cache[3][8] = {};   // [log2 cs][r / 64 - 1]
     const int ci = cs == 4 ? 2 : cs - 1, ri = (int)(smem / 16384) & 7;
     if (cache[ci][ri]) return cache[ci][ri];
-    auto kern = draft_sweep_tc<DSPARK_F32, false>;
+    auto kern = cs == 4 ? draft_sweep_tc<DSPARK_F32, false, 4> : draft_sweep_tc<DSPARK_F32, false, 2>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, cs, 1);
@@ -530,6 +553,9 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     }
     TcParams p;
     p.ebf = a.ebf;
+    // RNN codes tanh(out) are f32: three bf16 terms (exact); Markov codes are W1 rows
+    p.nsplit = a.rnn ? 3 : 1;
+    p.nacc = (p.nsplit * (a.r / 2) + kNACC * kBN <= (int)kTmemCols) ? kNACC : 1;
     p.parts = a.parts + (size_t)(k & 1) * a.parts_stride;
     p.cmass = a.cmass;
     p.nchunk = a.nchunk;
@@ -541,10 +567,10 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.k = k;
     p.ntiles = (a.V + kBN - 1) / kBN;
     p.nslices = pl.nslices;
-    p.cs = pl.cs;
     p.c2 = a.T > 0.f ? kLog2e / a.T : 1.f;
     const size_t smem = smem_bytes_for(a.r);
-    auto kern = draft_sweep_tc<UT, GREEDY>;
+    auto kern = pl.cs == 4 ? draft_sweep_tc<UT, GREEDY, 4>
+                : pl.cs == 2 ? draft_sweep_tc<UT, GREEDY, 2> : draft_sweep_tc<UT, GREEDY, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -578,7 +604,6 @@ bool draft_tc_make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* b
 }
 
 bool draft_tc_supported(const DraftArgs& a) {
-    if (a.rnn) return false;                       // e_k = tanh(out) is not bf16-exact
     if (a.w_dtype != DSPARK_BF16) return false;
     if (a.r % 64 != 0 || a.r > 256) return false;
     if (a.V % 8 != 0) return false;

@@ -38,8 +38,9 @@ struct DraftArgs {
     // workspace carve-up
     void* ws;
     DraftPartial* parts;      // [2][R][n_slices]
-    uint16_t* ebf;            // [2][R][r] bf16 bits (hi, lo) of e_k
+    uint16_t* ebf;            // [3][R][r] bf16 bits of e_k = hi + mid + lo (exact for f32 e_k)
     float* rnn_state;         // [R][r]
+    float* zbuf;              // RNN head: [R][2r + d] GRU input z of the current step
     uint32_t* best;           // [R] best race key of the current step (order-preserving bits)
     float2* cmass;            // [R][nchunk][4] (reference m, sum 2^(y - m)) per 256-column chunk
     int nchunk;               // ceil(V / 256)
@@ -79,7 +80,7 @@ struct VerifyArgs {
     float* rpart;       // [R][nch256][4] partial residual masses
     int* rej_count;     // number of requests that rejected a draft
     int* rej_list;      // [R] those requests, in arrival order
-    uint16_t* a_res;    // [R][r] bf16 codes e_j of the rejecting requests (compact order)
+    uint16_t* a_res;    // [3][rpad][r] bf16 terms hi, mid, lo of the rejecting requests' codes e_j (compact order; rpad = R rounded up to 128)
     uint32_t* vflags;   // bit 0: some rejecting code is not bf16-exact
     int tc;             // 1 if the tensor-core residual pass is launched
 };

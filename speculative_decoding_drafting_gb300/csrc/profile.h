@@ -15,7 +15,7 @@ enum ProfName : int {
     kPVerifySample = 7,
     kPSchedule = 8,
     kPDraftPrepRnn = 9,
-    kPRnnGatesTc = 10,
+    kPDraftRnnGru = 10,
 };
 
 void prof_begin(int name, cudaStream_t s);

@@ -13,11 +13,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
+// SM cycle counter: monotonic on the SM that reads it, unlike the global
+// nanosecond timer, which the driver may adjust (a forward step during a
+// wait would end it early).  Every wait limit below is in these cycles.
+__device__ __forceinline__ uint64_t sm_cycles() { return clock64(); }
 
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
     uint32_t v;
@@ -52,18 +51,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after `limit_ns` (or when another thread of the CTA already gave up) and
-// returns false; the caller then winds down without touching the pipeline.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// after kWaitLimitCycles SM cycles (2 to 4 s at 2 to 1 GHz; or at once when
+// another thread of the CTA already gave up) and returns false; the caller
+// then winds down without touching the pipeline.
+constexpr uint64_t kWaitLimitCycles = 1ull << 32;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const uint64_t t0 = sm_cycles();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (sm_cycles() - t0 > kWaitLimitCycles) {
                 *abort_flag = 1;
                 return false;
             }
@@ -73,11 +73,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Bounded wait that ignores the abort flag (used to drain copies in flight
 // after an abort).
-__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = global_timer_ns();
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_cycles) {
+    const uint64_t t0 = sm_cycles();
     while (!mbar_try_wait(bar, parity))
-        if (global_timer_ns() - t0 > limit_ns) return false;
+        if (sm_cycles() - t0 > limit_cycles) return false;
     return true;
+}
+
+// Spin for about a millisecond (2^21 SM cycles).
+__device__ __forceinline__ void spin_about_1ms() {
+    const uint64_t t0 = sm_cycles();
+    while (sm_cycles() - t0 < (1ull << 21)) {
+    }
 }
 
 // ---------------------------------------------------------------- TMA
@@ -114,12 +121,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
 // 2-d tile copy delivered to the same shared-memory offset of every CTA in
 // `cta_mask` (this cluster); each destination's mbarrier at the offset of
 // `bar` receives the bytes that land in that CTA.
+// The CTA mask is narrowed to .b16 inside the asm; callers pass a
+// compile-time constant (see umma_commit_mc).
 __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
-                                               uint16_t cta_mask, uint64_t policy) {
+                                               uint32_t cta_mask, uint64_t policy) {
     asm volatile(
+        "{\n\t.reg .b16 msk;\n\tcvt.u16.u32 msk, %5;\n\t"
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask), "l"(policy)
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], msk, %6;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(cta_mask), "l"(policy)
         : "memory");
 }
 
@@ -190,11 +200,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 
 // Arrive once on the mbarrier at the offset of `bar` in every CTA of
 // `cta_mask` when this thread's tensor-core operations issued so far complete.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+// Callers pass a compile-time constant mask (the cluster size is a template
+// parameter of every kernel that multicasts).  In one build of the draft sweep
+// whose MMA loop had a run-time trip count, a mask computed at run time (its
+// value checked in the kernel: all CTAs of the cluster) left the issuing CTA's
+// own barrier without its arrival on every stage, while its peer received
+// one; the same kernel with a constant mask completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint32_t cta_mask) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+        "{\n\t.reg .b16 msk;\n\tcvt.u16.u32 msk, %1;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], msk;\n\t}" ::"r"(
             smem_u32(bar)),
-        "h"(cta_mask)
+        "r"(cta_mask)
         : "memory");
 }
 

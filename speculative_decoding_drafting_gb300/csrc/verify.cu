@@ -245,7 +245,9 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
         A.n_out[r] = acc + 1;
     }
     if (GREEDY || !j) return;
-    // queue the rejecting request for the residual pass with its code e_j in bf16
+    // queue the rejecting request for the residual pass with its code e_j as
+    // three bf16 terms hi + mid + lo (exact for f32: each term takes the next
+    // 8 significand bits; mid = lo = 0 when e_j is bf16-exact)
     __shared__ int s_slot;
     if (tid == 0) {
         const int slot = atomicAdd(A.rej_count, 1);
@@ -255,26 +257,32 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
     __syncthreads();
     const int slot = s_slot;
     const float* e = A.code + ((size_t)r * A.gamma + (j - 1)) * A.r;
+    const size_t plane = (size_t)((A.R + 127) / 128) * 128 * A.r;
     bool inexact = false;
     for (int i = tid; i < A.r; i += blockDim.x) {
         const float v = e[i];
         const __nv_bfloat16 h = __float2bfloat16_rn(v);
-        A.a_res[(size_t)slot * A.r + i] = __bfloat16_as_ushort(h);
-        inexact |= __bfloat162float(h) != v;
+        const float r1 = v - __bfloat162float(h);
+        const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+        uint16_t* dst = A.a_res + (size_t)slot * A.r + i;
+        dst[0] = __bfloat16_as_ushort(h);
+        dst[plane] = __bfloat16_as_ushort(m);
+        dst[2 * plane] = __bfloat16_as_ushort(l);
+        inexact |= r1 != 0.f;
     }
     if (__syncthreads_or(inexact) && tid == 0) atomicOr(A.vflags, 1u);
 }
 
 // ------------------------------------------------------------------ residual (generic)
 // Rejecting requests only: w = max(p_j - q_j, 0) over the row, with
-// B = e_j W2 on CUDA cores.  One CTA task = (1024 columns, request); the mass
-// of each 256-column chunk goes to rpart[r][c][0].  When the tensor-core pass
-// ran and every code was bf16-exact, this kernel has nothing to do.
+// B = e_j W2 on CUDA cores, for the shapes the tensor-core pass does not take.
+// One CTA task = (1024 columns, request); the mass of each 256-column chunk
+// goes to rpart[r][c][0].
 template <int PT, int UT, int WT>
 __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
     pdl_launch_dependents();
     pdl_wait();
-    if (A.tc && !(*A.vflags & 1u)) return;
     extern __shared__ float e_sh[];
     __shared__ double sh[8];
     const int V = A.V, G1 = A.gamma + 1;
@@ -523,7 +531,7 @@ size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
     off = align_up(off + 256, 256);                                      // counters, flags
     off = align_up(off + (size_t)R * sizeof(int), 256);                 // rej_list
     const size_t rpad = (size_t)((R + 127) / 128) * 128;
-    off = align_up(off + rpad * r * sizeof(uint16_t), 256);              // a_res
+    off = align_up(off + 3 * rpad * r * sizeof(uint16_t), 256);          // a_res: hi, mid, lo planes
     return off;
 }
 
@@ -585,10 +593,8 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     if (a.tc) {
         e = launch_verify_tc_residual(a, s);
         if (e != cudaSuccess) return e;
-    }
-    {
-        // CUDA-core residual for codes that are not bf16-exact (or without the
-        // tensor-core pass); exits at once otherwise
+    } else {
+        // CUDA-core residual for the shapes the tensor-core pass does not take
         const long long rt = (long long)a.nch * a.R;
         const int g2 = (int)(rt < (long long)nsm * 8 ? rt : (long long)nsm * 8);
         prof_begin(kPVerifyResidualGeneric, s);
@@ -598,8 +604,11 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
         if (e == cudaSuccess) e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
+    // the sampling pass starts after the residual pass has finished: with
+    // programmatic overlap the whole cycle measured about 12 us slower on the
+    // 256-request, 151936-column workload
     prof_begin(kPVerifySample, s);
-    e = launch_kernel(verify_sample<PT, UT, WT>, dim3(a.R), dim3(256), 0, s, true, a);
+    e = launch_kernel(verify_sample<PT, UT, WT>, dim3(a.R), dim3(256), 0, s, false, a);
     prof_end(s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

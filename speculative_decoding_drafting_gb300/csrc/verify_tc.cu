@@ -42,8 +42,10 @@ constexpr int kEpiWG = 4;
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kEpiWarp0 = 3;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kACol = kNACC * kBN;   // A: columns [128, 128 + r/2) of tensor memory
+constexpr uint32_t kACol = kNACC * kBN;   // A: columns [128, 128 + nsplit r/2) of tensor memory
+// tensor-memory columns: two 64-column accumulators and nsplit blocks of r/2
+// A columns (r <= 256: 256 columns for one bf16 term, 512 for three)
+__host__ __device__ constexpr uint32_t tmem_cols_for(int nsplit) { return nsplit > 1 ? 512u : 256u; }
 
 __host__ __device__ constexpr int pitch_of(int es) { return kBN * es + 16; }   // padded row, bytes
 __host__ __device__ constexpr size_t stage_bytes(int esu, int esp) {
@@ -54,7 +56,8 @@ __host__ __device__ constexpr size_t smem_bytes(int /*r*/, int esu, int esp) {
 }
 
 struct ResParams {
-    const uint16_t* a_res;   // codes of the rejecting requests, compact order, [.][r] bf16 bits
+    const uint16_t* a_res;   // codes of the rejecting requests, compact order: [3][rpad][r] bf16 terms
+    int a_plane;             // elements between the hi, mid and lo planes of a_res (rpad r)
     const void* U;
     const void* P;
     const int* rej_count;
@@ -66,7 +69,6 @@ struct ResParams {
     float* rpart;            // [R][nch256][4]
     void* ws;
     int R, gamma, V, r, ntiles, nch256, nslices;
-    int cs;                  // CTAs per cluster (M-groups sharing each W2 stage)
     float c2;                // log2(e) / T
 };
 
@@ -74,7 +76,63 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src))
                  : "memory");
 }
-template <int UT, int PT>
+struct MmaBars {
+    uint64_t* a_full;
+    uint64_t* b_full;
+    uint64_t* b_empty;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+};
+
+// MMA issuer of one CTA (one thread): for every 64-column tile, r/64 W2
+// stages of four K=16 steps, each step one MMA per bf16 term of the code
+// (NS = 1 or 3) into the tile's accumulator.  Every stage is released to all
+// CTAs of the cluster.
+template <int NS, int CS>
+__device__ __forceinline__ void issue_mma(const MmaBars& mb, const uint8_t* sB, uint32_t tmem, int r, int nt,
+                                          int kblocks, volatile int* abort_flag) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
+    bool ok = mbar_wait(mb.a_full, 0, abort_flag);
+    tc_fence_after();
+    for (int t = 0; ok && t < nt; ++t) {
+        const int buf = t % kNACC;
+        const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
+        if (!mbar_wait(&mb.acc_empty[buf], aph ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * kBN);
+        for (int kb = 0; ok && kb < kblocks; ++kb) {
+            const int g = t * kblocks + kb;
+            const int bs = g % kNB;
+            if (!mbar_wait(&mb.b_full[bs], (uint32_t)(g / kNB) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint8_t* bstage = sB + (size_t)bs * 8192;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
+                // A: 16 K values = 8 tensor-memory columns per step, one
+                // block of r/2 columns per bf16 term of the code
+#pragma unroll
+                for (int sp = 0; sp < NS; ++sp) {
+                    const uint32_t at = tmem + kACol + (uint32_t)(sp * (r / 2) + kb * 32 + kk * 8);
+                    umma_bf16_ts(d, at, bd, idesc, (kb | kk | sp) ? 1u : 0u);
+                }
+            }
+            if (CS > 1)
+                umma_commit_mc(&mb.b_empty[bs], (1u << CS) - 1u);
+            else
+                umma_commit(&mb.b_empty[bs]);
+        }
+        if (!ok) break;
+        umma_commit(&mb.acc_full[buf]);
+    }
+}
+
+// CS: CTAs per cluster (1, 2 or 4), a template parameter so that the
+// multicast masks below are compile-time constants
+template <int UT, int PT, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     residual_tc(const __grid_constant__ CUtensorMap tmB, ResParams p) {
     pdl_launch_dependents();
@@ -84,8 +142,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int pu = pitch_of(esu), pp = pitch_of(esp);
     const int n_rej = *p.rej_count;
     const int mg = blockIdx.y, slice = blockIdx.x;
-    const int mg_first = mg - mg % p.cs;                      // first M-group of this cluster
-    if (mg_first * kBM >= n_rej || (*p.vflags & 1u)) return;  // nothing to do (cluster-uniform)
+    const int mg_first = mg - mg % CS;                         // first M-group of this cluster
+    if (mg_first * kBM >= n_rej) return;   // nothing to do (cluster-uniform)
+    // codes that are not bf16-exact (the RNN head's f32 tanh outputs) enter as
+    // three bf16 terms hi + mid + lo, each multiplied into the same accumulator
+    const int nsplit = (*p.vflags & 1u) ? 3 : 1;
+    const uint32_t tcols = tmem_cols_for(nsplit);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -115,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(a_full, kEpiWarps);
         for (int i = 0; i < kNB; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], (uint32_t)p.cs);   // one release per CTA of the cluster
+            mbar_init(&b_empty[i], (uint32_t)CS);   // one release per CTA of the cluster
         }
         for (int i = 0; i < kNS; ++i) {
             mbar_init(&s_full[i], 32 * kEpiWarps);   // every epilogue thread, once its copies land
@@ -129,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         prefetch_tmap(&tmB);
     }
-    if (warp == 1) tmem_alloc(tmem_holder, kTmemCols);
+    if (warp == 1) tmem_alloc(tmem_holder, tcols);
     tc_fence_before();
     cluster_sync();   // the peers' barriers are initialised before any multicast reaches them
     tc_fence_after();
@@ -142,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------- W2 producer: in a cluster of cs CTAs, CTA i loads
             // K rows [i 64/cs, (i + 1) 64/cs) of every stage and multicasts them
             const uint64_t pol_last = policy_evict_last();
-            const int prow = 64 / p.cs;
+            constexpr int prow = 64 / CS;
             const int ro = (int)cluster_ctarank() * prow;
-            const uint16_t mask = (uint16_t)((1u << p.cs) - 1u);
+            constexpr uint32_t mask = (1u << CS) - 1u;
             int issued = 0;
             for (int g = 0; g < nt * kblocks; ++g) {
                 const int t = g / kblocks, kb = g - t * kblocks;
@@ -152,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bph = (uint32_t)(g / kNB) & 1u;
                 if (!mbar_wait(&b_empty[bs], bph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&b_full[bs], 8192u);
-                if (p.cs == 1)
+                if (CS == 1)
                     tma_load_2d(sB + (size_t)bs * 8192, &tmB, &b_full[bs], (t_begin + t) * kBN, kb * 64, pol_last);
                 else
                     tma_load_2d_mc(sB + (size_t)bs * 8192 + ro * 128, &tmB, &b_full[bs], (t_begin + t) * kBN,
@@ -165,45 +227,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(&b_empty[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag);
             if (*abort_flag) {
                 for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
-                    mbar_wait_for(&b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitNs);
+                    mbar_wait_for(&b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitCycles);
             }
         }
     } else if (warp == 1) {
+        // ---------------- MMA issuer (the split count picks a straight-line body)
         if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
-            bool ok = mbar_wait(a_full, 0, abort_flag);
-            tc_fence_after();
-            for (int t = 0; ok && t < nt; ++t) {
-                const int buf = t % kNACC;
-                const uint32_t aph = (uint32_t)(t / kNACC) & 1u;
-                if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(buf * kBN);
-                for (int kb = 0; ok && kb < kblocks; ++kb) {
-                    const int g = t * kblocks + kb;
-                    const int bs = g % kNB;
-                    if (!mbar_wait(&b_full[bs], (uint32_t)(g / kNB) & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint8_t* bstage = sB + (size_t)bs * 8192;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        // A: 16 K values = 8 tensor-memory columns per step
-                        const uint32_t at = tmem + kACol + (uint32_t)(kb * 32 + kk * 8);
-                        const uint64_t bd = smem_desc_sw128(bstage + kk * 2048, 1024, 1024);
-                        umma_bf16_ts(d, at, bd, idesc, (kb | kk) ? 1u : 0u);
-                    }
-                    if (p.cs > 1)
-                        umma_commit_mc(&b_empty[bs], (uint16_t)((1u << p.cs) - 1u));
-                    else
-                        umma_commit(&b_empty[bs]);
-                }
-                if (!ok) break;
-                umma_commit(&acc_full[buf]);
-            }
+            const MmaBars mb{a_full, b_full, b_empty, acc_full, acc_empty};
+            if (nsplit == 1)
+                issue_mma<1, CS>(mb, sB, tmem, p.r, nt, kblocks, abort_flag);
+            else
+                issue_mma<3, CS>(mb, sB, tmem, p.r, nt, kblocks, abort_flag);
         }
     } else {
         // ---------------- epilogue: thread = (rejecting request, 16-column quarter)
@@ -213,21 +247,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = rit < rows_here;
         {
             // A operand: this thread's share (r/8 columns, r/4 values) of its
-            // row's code goes to tensor memory; column j of the row holds the
-            // bf16 values 2j (low half) and 2j + 1 (high half)
+            // row's code goes to tensor memory, one block of r/2 columns per
+            // bf16 term; column j of a block holds the values 2j (low half)
+            // and 2j + 1 (high half)
             const int ncol = p.r / 8;
             const int c0 = wg * ncol;
-            for (int c = 0; c < ncol; c += 8) {
-                uint32_t v[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                if (row_ok) {
-                    const uint4* src =
-                        reinterpret_cast<const uint4*>(p.a_res + (size_t)(mg * kBM + rit) * p.r + 2 * (c0 + c));
-                    const uint4 a0 = src[0], a1 = src[1];
-                    v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
-                    v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+            for (int sp = 0; sp < nsplit; ++sp)
+                for (int c = 0; c < ncol; c += 8) {
+                    uint32_t v[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    if (row_ok) {
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            p.a_res + (size_t)sp * p.a_plane + (size_t)(mg * kBM + rit) * p.r + 2 * (c0 + c));
+                        const uint4 a0 = src[0], a1 = src[1];
+                        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+                        v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+                    }
+                    tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + kACol + (uint32_t)(sp * (p.r / 2) + c0 + c), v);
                 }
-                tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + kACol + (uint32_t)(c0 + c), v);
-            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -384,14 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a peer's multicast copies or releases may still be on their way to
         // this CTA's shared memory: give them a millisecond before leaving
         if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 1000000ull) {
-        }
+        spin_about_1ms();
     }
     cluster_sync();   // no CTA leaves while a peer may still write into it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, tcols);
     }
 }
 
@@ -401,7 +435,7 @@ int active_clusters(int cs, size_t smem) {
     static int cache[3] = {0, 0, 0};
     const int ci = cs == 4 ? 2 : cs - 1;
     if (cache[ci]) return cache[ci];
-    auto kern = residual_tc<UT, PT>;
+    auto kern = cs == 4 ? residual_tc<UT, PT, 4> : residual_tc<UT, PT, 2>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, cs, 1);
@@ -448,7 +482,7 @@ cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     }
     ResParams p;
     p.a_res = a.a_res;
-    p.cs = cs;
+    p.a_plane = ((a.R + kBM - 1) / kBM) * kBM * a.r;
     p.U = a.U;
     p.P = a.P;
     p.rej_count = a.rej_count;
@@ -470,7 +504,7 @@ cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     if (ns > a.nch256) ns = a.nch256;
     p.nslices = ns;
     p.c2 = 1.4426950408889634f / a.T;
-    auto kern = residual_tc<UT, PT>;
+    auto kern = cs == 4 ? residual_tc<UT, PT, 4> : cs == 2 ? residual_tc<UT, PT, 2> : residual_tc<UT, PT, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
