@@ -70,6 +70,10 @@ def lib():
                                         u64, P, dbl, P, P, P, P, P, P, P, i32]
             L.oracle_verify.restype = i32
             L.oracle_prefix_survival.argtypes = [P, i32, i32, P]
+            L.oracle_confidence.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32, i32, P]
+            L.oracle_confidence.restype = i32
+            L.oracle_threshold_lengths.argtypes = [P, i32, i32, ctypes.c_float, i32, P]
+            L.oracle_threshold_lengths.restype = i32
             L.oracle_schedule_loop.argtypes = [P, P, i32, i32, i32, P, P]
             L.oracle_schedule_loop.restype = i32
             L.oracle_schedule_closed.argtypes = [P, P, i32, i32, i32, P, P, P]
@@ -206,6 +210,26 @@ def verify(P, U, W2, tokens, qx, lse, code, T: float, seed: int, verify_len=None
     return out
 
 
+# ---------------------------------------------------------------- confidence head
+def confidence(H, W1, w, anchor, tokens):
+    """c [R, gamma] (double) = sigmoid(w . [h_k, W1[x_{k-1}]]) (blog section 4.1).
+    H [R, gamma, d] and W1 [V, r] in storage dtype, w [d + r] float32,
+    anchor [R] = x_0, tokens [R, gamma] = the drafted x_1..x_gamma."""
+    H, W1 = _c(H), _c(W1)
+    w = _c(w, np.float32)
+    anchor = _c(anchor, np.int32)
+    tokens = _c(tokens, np.int32)
+    R, gamma, d = H.shape
+    V, r = W1.shape
+    assert w.shape == (d + r,) and anchor.shape == (R,) and tokens.shape == (R, gamma)
+    c = np.zeros((R, gamma))
+    st = lib().oracle_confidence(_ptr(H), _dt(H), _ptr(W1), _dt(W1), _ptr(w), _ptr(anchor), _ptr(tokens),
+                                 R, gamma, V, d, r, _ptr(c))
+    if st != 0:
+        raise RuntimeError(f"oracle_confidence failed: {st}")
+    return c
+
+
 # ---------------------------------------------------------------- scheduler
 def prefix_survival(c) -> np.ndarray:
     c = _c(c, np.float32)
@@ -237,3 +261,15 @@ def schedule_closed(c, sps):
     if n < 0:
         raise RuntimeError("oracle_schedule_closed failed")
     return L, float(th[0]), int(n), float(gap[0])
+
+
+def threshold_lengths(c, theta: float, mode: int = 0):
+    """Per-request verify lengths of the threshold filter: the longest prefix
+    with a_{r,j} >= theta (mode 0) or c_{r,j} >= theta (mode 1)."""
+    c = _c(c, np.float32)
+    R, gamma = c.shape
+    L = np.zeros(R, np.int32)
+    st = lib().oracle_threshold_lengths(_ptr(c), R, gamma, float(np.float32(theta)), int(mode), _ptr(L))
+    if st != 0:
+        raise RuntimeError(f"oracle_threshold_lengths failed: {st}")
+    return L

@@ -530,6 +530,30 @@ int oracle_verify(const void* P, int p_dtype, const void* U, int u_dtype,
 }
 
 /* ------------------------------------------------------------------ */
+/* Confidence head (blog section 4.1, ConfidenceHead).                  */
+/* ------------------------------------------------------------------ */
+int oracle_confidence(const void* H, int h_dtype, const void* W1, int w_dtype, const float* w,
+                      const int32_t* anchor, const int32_t* tokens,
+                      int R, int gamma, int V, int d, int r, double* c) {
+    if (R <= 0 || gamma <= 0 || V <= 0 || d < 0 || r <= 0) return -3;
+    for (int ri = 0; ri < R; ++ri) {
+        for (int k = 1; k <= gamma; ++k) {
+            /* the token before position k: x_0 = anchor, x_{k-1} = draft k-1 */
+            int prev = (k == 1) ? anchor[ri] : tokens[(size_t)ri * gamma + (size_t)(k - 2)];
+            if (prev < 0 || prev >= V) return -6;
+            /* logit = w . [h_k, W1[x_{k-1}]]: the first d weights meet h_k,
+             * the last r meet the previous token's rank-r embedding */
+            double t = 0.0;
+            const size_t hrow = ((size_t)ri * gamma + (size_t)(k - 1)) * (size_t)d;
+            for (int i = 0; i < d; ++i) t += (double)w[i] * ld(H, h_dtype, hrow + (size_t)i);
+            for (int i = 0; i < r; ++i) t += (double)w[d + i] * ld(W1, w_dtype, (size_t)prev * r + (size_t)i);
+            c[(size_t)ri * gamma + (size_t)(k - 1)] = sigmoid(t);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Scheduler (blog section 4.3; explainer section 04).                   */
 /* ------------------------------------------------------------------ */
 void oracle_prefix_survival(const float* c, int R, int gamma, float* a) {
@@ -637,4 +661,25 @@ int oracle_schedule_closed(const float* c, const double* sps, int n_sps, int R, 
     *theta = th[nstar];
     free(th); free(cand);
     return nstar;
+}
+
+/* Threshold filter (blog section 4.3, the confidence-threshold sweep; the
+ * explainer's section 04 contrasts it with the scheduler): every request
+ * verifies its longest prefix whose confidence clears one fixed threshold.
+ * mode 0: a_{r,j} = c_{r,1} ... c_{r,j} >= theta (float32 product in position
+ * order, as the scheduler forms it); mode 1: c_{r,j} >= theta itself, up to
+ * the first position that misses. */
+int oracle_threshold_lengths(const float* c, int R, int gamma, float theta, int mode, int32_t* lengths) {
+    if (R <= 0 || gamma <= 0 || (mode != 0 && mode != 1)) return -3;
+    float* a = (float*)malloc(sizeof(float) * (size_t)R * (size_t)gamma);
+    if (!a) return -1;
+    oracle_prefix_survival(c, R, gamma, a);
+    const float* score = mode == 0 ? a : c;
+    for (int ri = 0; ri < R; ++ri) {
+        int len = 0;
+        while (len < gamma && score[(size_t)ri * gamma + (size_t)len] >= theta) ++len;
+        lengths[ri] = len;
+    }
+    free(a);
+    return 0;
 }

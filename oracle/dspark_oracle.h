@@ -12,7 +12,8 @@
  * Sources (the pages are cited by title and section):
  *  - "DSpark: DeepSeek 线上跑的投机解码" (blog), section 3.2: Markov head
  *    B_k = W1[x_{k-1}] W2, RNN head step, and the sequential stage loop;
- *    section 4.3: prefix survival and the hardware-aware scheduler.
+ *    section 4.1: the confidence head; section 4.3: prefix survival, the
+ *    hardware-aware scheduler and the confidence-threshold sweep.
  *  - "DSpark explainer", section 03: q_k = softmax(U_k + B_k);
  *    section 04: a_j = c_1 ... c_j, B, tau, Theta = tau * SPS(B);
  *    section 05: alpha(x) = min(1, p(x)/q(x)) and
@@ -89,6 +90,20 @@ int oracle_verify(const void* P, int p_dtype, const void* U, int u_dtype,
                   int32_t* out_tokens, int32_t* accept_len, int32_t* n_out,
                   double* px, double* lse_p, double* min_gap, int32_t* gap_kind,
                   int n_threads);
+
+/* Confidence head (blog section 4.1): c[r,k-1] = sigmoid(w . [h_k, W1[x_{k-1}]])
+ * with no bias, x_0 = anchor[r] and x_{k-1} = tokens[r,k-2] for k >= 2.
+ * H is [R,gamma,d] in h_dtype, W1 [V,r] in w_dtype, w [d + r] float32 (the
+ * first d entries weigh h_k, the last r the embedding).  c is [R,gamma].
+ * Returns 0, or -6 for a token outside [0, V). */
+int oracle_confidence(const void* H, int h_dtype, const void* W1, int w_dtype, const float* w,
+                      const int32_t* anchor, const int32_t* tokens,
+                      int R, int gamma, int V, int d, int r, double* c);
+
+/* Threshold filter: lengths[r] = the longest prefix of positions whose score
+ * is >= theta; score = a[r,j] (mode 0, float32 prefix product) or c[r,j]
+ * (mode 1).  Returns 0 or a negative error. */
+int oracle_threshold_lengths(const float* c, int R, int gamma, float theta, int mode, int32_t* lengths);
 
 /* Prefix survival a[r,j] = c[r,0] * ... * c[r,j], float32 sequential
  * product (the decision precision of the scheduler's sort). */

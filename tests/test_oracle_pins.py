@@ -435,3 +435,127 @@ def test_scheduler_exact_ties_keep_prefix_order():
     np.testing.assert_array_equal(L, [3, 3])
     np.testing.assert_array_equal(L, L2)
     assert n == 6 and abs(th - (2 + 1 + 1 + 0.5 + 0.9 + 0.9 + 0.9)) < 1e-6
+
+
+# ------------------------------------------------------------------ confidence head
+def _bf16_bits(x):
+    """float32 values that bf16 holds exactly -> their bf16 bit patterns."""
+    b = np.ascontiguousarray(np.asarray(x, np.float32)).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0)
+    return (b >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("storage", ["f32", "bf16"])
+def test_confidence_head_hand_worked_two_steps(storage):
+    """Blog section 4.1: c_k = sigmoid(w . [h_k, W1[x_{k-1}]]), no bias.
+    d = 2, r = 2, V = 3, every value exact in bf16:
+      W1 rows: x=0 -> (3, -1), x=1 -> (1/2, 2), x=2 -> (-2, 1)
+      anchor x_0 = 0, drafted x_1 = 1, x_2 = 2
+      h_1 = (1, 2), h_2 = (-1, 1/2),  w = (1/2, 1/4 | 1/8, -1/4)
+      k = 1: 1/2 + 1/2 + 3/8 + 1/4 = 13/8
+      k = 2: -1/2 + 1/8 + 1/16 - 1/2 = -13/16
+    (the concatenation [e, h] would give 7/8 at k = 1; the embedding of x_1 at
+    k = 1 would give 9/16)."""
+    W1 = np.array([[3, -1], [0.5, 2], [-2, 1]], np.float32)
+    H = np.array([[[1, 2], [-1, 0.5]]], np.float32)
+    w = np.array([0.5, 0.25, 0.125, -0.25], np.float32)
+    if storage == "bf16":
+        W1, H = _bf16_bits(W1), _bf16_bits(H)
+    c = oracle.confidence(H, W1, w, np.array([0], np.int32), np.array([[1, 2]], np.int32))
+    np.testing.assert_allclose(c[0], special.expit([13 / 8, -13 / 16]), rtol=0, atol=1e-15)
+
+
+def _conf_case(seed, R=6, gamma=4, V=50, d=24, r=8):
+    rng = np.random.default_rng(seed)
+    H = rng.normal(0, 1, (R, gamma, d)).astype(np.float32)
+    W1 = rng.normal(0, 0.5, (V, r)).astype(np.float32)
+    w = rng.normal(0, 0.3, d + r).astype(np.float32)
+    anchor = rng.integers(0, V, R).astype(np.int32)
+    tokens = rng.integers(0, V, (R, gamma)).astype(np.int32)
+    return H, W1, w, anchor, tokens
+
+
+def test_confidence_head_special_cases():
+    H, W1, w, anchor, tokens = _conf_case(3)
+    d = H.shape[2]
+    # w = 0: sigmoid(0) = 1/2 everywhere
+    c0 = oracle.confidence(H, W1, np.zeros_like(w), anchor, tokens)
+    assert np.all(c0 == 0.5)
+    # no bias: negating w gives 1 - c
+    c = oracle.confidence(H, W1, w, anchor, tokens)
+    cn = oracle.confidence(H, W1, -w, anchor, tokens)
+    np.testing.assert_allclose(cn, 1.0 - c, rtol=0, atol=1e-15)
+    assert np.all((c > 0) & (c < 1))
+    # linear in w: the logits of a split w add up
+    wa = np.concatenate([w[:d], np.zeros_like(w[d:])])
+    wb = w - wa
+    lg = special.logit
+    ca = oracle.confidence(H, W1, wa, anchor, tokens)
+    cb = oracle.confidence(H, W1, wb, anchor, tokens)
+    np.testing.assert_allclose(lg(ca) + lg(cb), lg(c), rtol=0, atol=1e-12)
+    # the h part ignores the tokens; the embedding part sees only x_{k-1}
+    other = (tokens + 7) % W1.shape[0]
+    np.testing.assert_array_equal(ca, oracle.confidence(H, W1, wa, (anchor + 3) % W1.shape[0], other))
+    shifted = np.concatenate([anchor[:, None], tokens[:, :-1]], axis=1)      # x_0 .. x_{gamma-1}
+    for k in range(tokens.shape[1]):
+        for i in range(len(anchor)):
+            for j in range(len(anchor)):
+                if shifted[i, k] == shifted[j, k]:
+                    assert cb[i, k] == cb[j, k]
+    same = np.tile(shifted[:1], (len(anchor), 1))
+    cb_same = oracle.confidence(H, W1, wb, same[:, 0].copy(), np.concatenate([same[:, 1:], tokens[:, -1:]], 1))
+    assert np.all(cb_same == cb_same[:1])
+
+
+def test_confidence_head_rejects_out_of_range_tokens():
+    H, W1, w, anchor, tokens = _conf_case(4)
+    tokens[1, 2] = W1.shape[0]
+    with pytest.raises(RuntimeError):
+        oracle.confidence(H, W1, w, anchor, tokens)
+
+
+# ------------------------------------------------------------------ threshold filter
+def test_threshold_filter_worked_values():
+    """The explainer's section 04 numbers: c = 0.8 three times gives
+    a = (0.8, 0.64, 0.512).  Prefix-survival mode keeps the positions whose a
+    clears theta; per-token mode keeps all three while 0.8 >= theta."""
+    g = read_golden("prefix_survival.txt")
+    c = np.array([g["c"][0]], np.float32)
+    for theta, want in [(0.5, 3), (0.6, 2), (0.7, 1), (0.81, 0)]:
+        assert oracle.threshold_lengths(c, theta, 0)[0] == want
+    assert oracle.threshold_lengths(c, 0.8, 1)[0] == 3
+    assert oracle.threshold_lengths(c, 0.81, 1)[0] == 0
+
+
+def test_threshold_filter_modes_differ_on_a_dip():
+    """c = (0.9, 0.5, 0.95): a = (0.9, 0.45, 0.4275).  A per-token threshold of
+    0.6 stops at the dip (length 1) although 0.95 follows; the prefix-survival
+    threshold counts a >= theta."""
+    c = np.array([[0.9, 0.5, 0.95]], np.float32)
+    assert oracle.threshold_lengths(c, 0.6, 1)[0] == 1
+    assert oracle.threshold_lengths(c, 0.4, 1)[0] == 3
+    for theta, want in [(0.46, 1), (0.44, 2), (0.4, 3), (0.95, 0)]:
+        assert oracle.threshold_lengths(c, theta, 0)[0] == want
+
+
+def test_threshold_filter_invariants():
+    w = synth.WORKLOADS["toy"].scaled(R=64)
+    c = synth.gen_c(w)
+    c[3, 2] = 0.0
+    c[5, :] = 1.0
+    a = oracle.prefix_survival(c)
+    prev0 = prev1 = None
+    for theta in np.linspace(-0.1, 1.1, 49).astype(np.float32):
+        L0 = oracle.threshold_lengths(c, theta, 0)
+        L1 = oracle.threshold_lengths(c, theta, 1)
+        assert np.all((L0 >= 0) & (L0 <= w.gamma)) and np.all(L0 <= L1)
+        # a is non-increasing along a request, so the kept set is exactly {a >= theta}
+        assert L0.sum() == int((a >= theta).sum())
+        if prev0 is not None:
+            assert np.all(L0 <= prev0) and np.all(L1 <= prev1)
+        prev0, prev1 = L0, L1
+        if theta <= 0:
+            assert np.all(L0 == w.gamma)
+        if theta > 1:
+            assert np.all(L1 == 0)
+    assert oracle.threshold_lengths(c, 0.5, 0)[3] <= 2 and oracle.threshold_lengths(c, 1.0, 0)[5] == w.gamma
