@@ -299,6 +299,75 @@ def measure_rnn_draft(steps: int, warmup: int, devc, flush):
             "kernels_us_per_launch": {k: round(1000 * v / n, 2) for k, (n, v) in table.items()}}
 
 
+def measure_confidence_and_threshold(w, U, anchor, W1, W2, c, steps: int, devc, flush, d_conf: int = 2048):
+    """The fused confidence head and the threshold filter on the headline
+    workload.  The head: the Markov draft with and without a d = 2048 head
+    (alternating calls, L2 flushed before each), its extra time per draft and
+    per prep launch.  The threshold filter: one call on c [R, gamma]."""
+    import torch
+    from speculative_decoding_drafting_gb300 import binding
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(devc)
+
+    H, wc = to_dev(synth.gen_conf_H(w, d_conf)), to_dev(synth.gen_conf_w(w, d_conf))
+    base = binding.draft_markov(U, anchor, W1, W2, w.T, 1)
+    withc = binding.draft_markov(U, anchor, W1, W2, w.T, 1, conf_w=wc, conf_H=H)
+    stream = torch.cuda.current_stream()
+    ms = {False: [], True: []}
+    for i in range(3 + steps):
+        for on in (False, True):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if on:
+                binding.draft_markov(U, anchor, W1, W2, w.T, 50 + i, ws=withc["ws"], out=withc, conf_w=wc, conf_H=H)
+            else:
+                binding.draft_markov(U, anchor, W1, W2, w.T, 50 + i, ws=base["ws"], out=base)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ms[on].append(a.elapsed_time(b))
+    prep = {}
+    for on in (False, True):
+        binding.profile_enable(True)
+        for i in range(steps):
+            flush.zero_()
+            if on:
+                binding.draft_markov(U, anchor, W1, W2, w.T, 90 + i, ws=withc["ws"], out=withc, conf_w=wc, conf_H=H)
+            else:
+                binding.draft_markov(U, anchor, W1, W2, w.T, 90 + i, ws=base["ws"], out=base)
+        torch.cuda.synchronize()
+        binding.profile_enable(False)
+        t = [ms_ for name, ms_ in binding.profile_collect() if name == "draft_prep"]
+        prep[on] = 1000.0 * float(np.mean(t))
+    # threshold filter: one call per event pair (launch-bound: R * gamma floats)
+    out = torch.empty((w.R,), dtype=torch.int32, device=devc)
+    for i in range(5):
+        binding.schedule_threshold(c, 0.5, 0, out=out)
+    th = []
+    for i in range(max(10, steps)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.schedule_threshold(c, 0.5, 0, out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        th.append(a.elapsed_time(b))
+    m0, m1 = float(np.median(ms[False])), float(np.median(ms[True]))
+    return {
+        "confidence_head": {"workload": f"{w.name} draft with a d={d_conf} head (h bf16 [R, gamma, d], w f32 [d + r])",
+                            "ms_per_draft_without": round(m0, 4), "ms_per_draft_with": round(m1, 4),
+                            "extra_us_per_draft": round(1000 * (m1 - m0), 2),
+                            "prep_us_without": round(prep[False], 2), "prep_us_with": round(prep[True], 2),
+                            "h_bytes_per_draft": int(w.R * w.gamma * d_conf * 2)},
+        "threshold_filter": {"workload": f"c [{w.R}, {w.gamma}] float32, theta 0.5, prefix-survival mode",
+                             "us_per_call": round(1000 * float(np.median(th)), 2)},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -308,7 +377,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--no-variants", action="store_true", help="skip the RNN-head draft measurement")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the RNN-head draft, confidence-head and threshold-filter measurements")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -454,6 +524,8 @@ def main(argv=None):
     variants = None
     if rank == 0 and world == 1 and not args.no_variants:
         variants = {"rnn_draft": measure_rnn_draft(max(3, args.steps // 2), 3, devc, flush)}
+        variants.update(measure_confidence_and_threshold(w, U, anchor, W1, W2, c, max(5, args.steps // 2), devc,
+                                                         flush))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

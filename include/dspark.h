@@ -142,6 +142,55 @@ int dspark_draft_rnn(const void* U, int u_dtype, const int32_t* anchor,
                      float* state_out,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* -------------------------------------------------------- confidence head */
+
+/*
+ * Confidence head fused into drafting (blog section 4.1, ConfidenceHead):
+ *   c_k = sigmoid(w . [h_k, W1[x_{k-1}]])        no bias, x_0 = anchor
+ * evaluated inside draft step k from the h_k row and the W1 row that step
+ * gathers anyway, so c [R, gamma] is ready for dspark_schedule when the
+ * draft finishes.
+ *   H  [R, gamma, d]  bfloat16  backbone hidden states h_k (device).  NULL
+ *                               with the RNN head: the head's own H and d
+ *                               (the d below is then ignored); NULL with the
+ *                               Markov head requires d = 0.
+ *   w  [d + r]        float     weights: w[0, d) meet h_k, w[d, d + r) meet
+ *                               W1[x_{k-1}] (device)
+ *   d                 int       0 <= d <= 16384
+ *   c  [R, gamma]     float     output (device, caller-owned): the dot product
+ *                               in float32 (fixed summation order, so reruns
+ *                               agree bit for bit), then the sigmoid in float32
+ * The struct itself is read on the host during the call.  A null conf
+ * turns the head off (the plain entry points below pass null).  Errors:
+ * INVALID_ARG for a null w or c (or Markov H = NULL with d > 0), SHAPE for d
+ * outside [0, 16384].
+ */
+typedef struct {
+    const void* H;
+    const float* w;
+    int d;
+    float* c;
+} dspark_conf_t;
+
+/* dspark_draft_markov with the confidence head. */
+int dspark_draft_markov_conf(const void* U, int u_dtype, const int32_t* anchor,
+                             const void* W1, const void* W2, int w_dtype,
+                             int R, int gamma, int V, int r,
+                             uint64_t seed, const uint32_t* req_ids, float temperature,
+                             int32_t* tokens, float* q_tok, double* lse, float* code,
+                             const dspark_conf_t* conf,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* dspark_draft_rnn with the confidence head. */
+int dspark_draft_rnn_conf(const void* U, int u_dtype, const int32_t* anchor,
+                          const void* W1, const void* W2, const void* Wgco, int w_dtype,
+                          const void* H, int d,
+                          int R, int gamma, int V, int r,
+                          uint64_t seed, const uint32_t* req_ids, float temperature,
+                          int32_t* tokens, float* q_tok, double* lse, float* code,
+                          float* state_out, const dspark_conf_t* conf,
+                          void* ws, size_t ws_bytes, void* stream);
+
 /* ----------------------------------------------------------------- verify */
 
 size_t dspark_verify_workspace_size(int R, int gamma, int V, int r);
@@ -235,6 +284,23 @@ size_t dspark_schedule_workspace_size(int R, int gamma);
 int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gamma,
                     int32_t* verify_len, double* theta, int32_t* n_star,
                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Threshold filter (blog section 4.3, the confidence-threshold sweep; the
+ * explainer's section 04 sets the scheduler against one fixed threshold for
+ * every request): request r verifies its longest prefix of positions whose
+ * score is >= theta,
+ *   mode 0: score a_{r,j} = c_{r,1} ... c_{r,j} (float32 product in position
+ *           order, the scheduler's prefix survival)
+ *   mode 1: score c_{r,j}
+ * stopping at the first position that misses (a NaN score misses).
+ *   c          [R, gamma]  float   (device)
+ *   verify_len [R]         int32   output (device, caller-owned)
+ * No workspace.  Requirements: R >= 1, 1 <= gamma <= 64, mode 0 or 1
+ * (INVALID_ARG otherwise, or for a null pointer; SHAPE for the sizes).
+ */
+int dspark_schedule_threshold(const float* c, int R, int gamma, float theta, int mode,
+                              int32_t* verify_len, void* stream);
 
 /* -------------------------------------------------------------- profiling */
 

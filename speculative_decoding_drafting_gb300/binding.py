@@ -68,12 +68,18 @@ def load(build_if_missing: bool = True):
                                     P, P, P, P, P, P, sz, P]
         L.dspark_schedule_workspace_size.argtypes = [i32, i32]
         L.dspark_schedule_workspace_size.restype = sz
+        L.dspark_draft_markov_conf.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, u64, P, f32,
+                                               P, P, P, P, P, P, sz, P]
+        L.dspark_draft_rnn_conf.argtypes = [P, i32, P, P, P, P, i32, P, i32, i32, i32, i32, i32, u64, P, f32,
+                                            P, P, P, P, P, P, P, sz, P]
         L.dspark_schedule.argtypes = [P, P, i32, i32, i32, P, P, P, P, sz, P]
+        L.dspark_schedule_threshold.argtypes = [P, i32, i32, f32, i32, P, P]
         L.dspark_profile_enable.argtypes = [i32]
         L.dspark_profile_collect.argtypes = [P, P, i32]
         L.dspark_profile_kernel_name.argtypes = [i32]
         L.dspark_profile_kernel_name.restype = ctypes.c_char_p
-        for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_verify", "dspark_schedule",
+        for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_draft_markov_conf", "dspark_draft_rnn_conf",
+                     "dspark_verify", "dspark_schedule", "dspark_schedule_threshold",
                      "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
             getattr(L, name).restype = i32
         _lib = L
@@ -108,6 +114,25 @@ def _check(fn: str, code: int):
         raise DsparkError(fn, code)
 
 
+class _Conf(ctypes.Structure):
+    """dspark_conf_t: the confidence head's arguments."""
+    _fields_ = [("H", ctypes.c_void_p), ("w", ctypes.c_void_p), ("d", ctypes.c_int), ("c", ctypes.c_void_p)]
+
+
+def _conf(conf_w, conf_H, out, R, gamma, dev):
+    """Fill out["c"] and return a dspark_conf_t pointer (None: head off)."""
+    if conf_w is None:
+        return None, None
+    if conf_w.dtype != torch.float32:
+        raise TypeError("confidence weights must be float32")
+    if conf_H is not None and conf_H.dtype != torch.bfloat16:
+        raise TypeError("confidence-head H must be bfloat16")
+    if "c" not in out:
+        out["c"] = torch.empty((R, gamma), dtype=torch.float32, device=dev)
+    st = _Conf(_p(conf_H), _p(conf_w), 0 if conf_H is None else conf_H.shape[2], _p(out["c"]))
+    return st, ctypes.byref(st)
+
+
 def _workspace(nbytes: int, device) -> torch.Tensor:
     # torch's caching allocator returns 512-byte aligned blocks; the first
     # word (the device status word) must start at zero.
@@ -136,8 +161,11 @@ def schedule_workspace_bytes(R, gamma) -> int:
     return int(load().dspark_schedule_workspace_size(R, gamma))
 
 
-def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None, ws=None, out=None, stream=None):
-    """Markov-head drafting (``dspark_draft_markov``).  Returns a dict of outputs."""
+def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None, ws=None, out=None, stream=None,
+                 conf_w=None, conf_H=None):
+    """Markov-head drafting (``dspark_draft_markov``).  Returns a dict of outputs.
+    With ``conf_w`` ([d + r] float32) and ``conf_H`` ([R, gamma, d] bfloat16)
+    the fused confidence head (``dspark_draft_markov_conf``) adds ``c``."""
     L = load()
     R, gamma, V = U.shape
     r = W1.shape[1]
@@ -150,18 +178,20 @@ def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None,
     nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, 0)
     if ws is None:
         ws = _workspace(nbytes, dev)
-    code = L.dspark_draft_markov(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _dt(W1), R, gamma, V, r,
-                                 int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
-                                 _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
-                                 _p(ws), ws.numel(), _stream(stream))
+    keep, cp = _conf(conf_w, conf_H, out, R, gamma, dev)
+    code = L.dspark_draft_markov_conf(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _dt(W1), R, gamma, V, r,
+                                      int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
+                                      _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
+                                      cp, _p(ws), ws.numel(), _stream(stream))
     _check("dspark_draft_markov", code)
     out["ws"] = ws
     return out
 
 
 def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids=None, ws=None, out=None,
-              stream=None):
-    """RNN-head drafting (``dspark_draft_rnn``)."""
+              stream=None, conf_w=None, conf_H=None):
+    """RNN-head drafting (``dspark_draft_rnn``).  With ``conf_w`` the fused
+    confidence head adds ``c`` (``conf_H`` None: the head's own H)."""
     L = load()
     R, gamma, V = U.shape
     r = W1.shape[1]
@@ -178,10 +208,11 @@ def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids
     nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, d)
     if ws is None:
         ws = _workspace(nbytes, dev)
-    code = L.dspark_draft_rnn(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _p(Wgco), _dt(W1), _p(H), d,
-                              R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
-                              _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
-                              _p(out.get("state")), _p(ws), ws.numel(), _stream(stream))
+    keep, cp = _conf(conf_w, conf_H, out, R, gamma, dev)
+    code = L.dspark_draft_rnn_conf(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _p(Wgco), _dt(W1), _p(H), d,
+                                   R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
+                                   _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
+                                   _p(out.get("state")), cp, _p(ws), ws.numel(), _stream(stream))
     _check("dspark_draft_rnn", code)
     out["ws"] = ws
     return out
@@ -229,6 +260,19 @@ def schedule(c, sps, ws=None, out=None, stream=None):
                              _p(out["n_star"]), _p(ws), ws.numel(), _stream(stream))
     _check("dspark_schedule", code)
     out["ws"] = ws
+    return out
+
+
+def schedule_threshold(c, theta: float, mode: int = 0, out=None, stream=None):
+    """Threshold filter (``dspark_schedule_threshold``): per-request verify
+    lengths, the longest prefix with a_{r,j} >= theta (mode 0) or
+    c_{r,j} >= theta (mode 1)."""
+    L = load()
+    R, gamma = c.shape
+    if out is None:
+        out = torch.empty((R,), dtype=torch.int32, device=c.device)
+    code = L.dspark_schedule_threshold(_p(c), R, gamma, float(theta), int(mode), _p(out), _stream(stream))
+    _check("dspark_schedule_threshold", code)
     return out
 
 

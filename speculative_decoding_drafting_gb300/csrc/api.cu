@@ -89,6 +89,27 @@ size_t dspark_draft_workspace_size(int R, int gamma, int V, int r, int d) {
     return draft_workspace_bytes(R, gamma, V, r, d);
 }
 
+// Attach the confidence head's arguments (conf may be null: head off).
+static int attach_conf(DraftArgs& a, bool rnn, const dspark_conf_t* conf) {
+    if (!conf) return DSPARK_OK;
+    if (!conf->w || !conf->c) return DSPARK_ERR_INVALID_ARG;
+    if (conf->H) {
+        if (conf->d < 0 || conf->d > 16384) return DSPARK_ERR_SHAPE;
+        a.Hc = conf->H;
+        a.dc = conf->d;
+    } else if (rnn) {
+        a.Hc = a.H;   // the RNN head's own hidden states
+        a.dc = a.d;
+    } else {
+        if (conf->d != 0) return DSPARK_ERR_INVALID_ARG;
+        a.Hc = nullptr;
+        a.dc = 0;
+    }
+    a.wc = conf->w;
+    a.conf = conf->c;
+    return DSPARK_OK;
+}
+
 static int draft_entry(DraftArgs& a, bool rnn, size_t ws_bytes, void* stream) {
     int st = check_common(a.R, a.gamma, a.V, a.r, a.T, a.u_dtype, a.w_dtype);
     if (st) return st;
@@ -103,29 +124,50 @@ static int draft_entry(DraftArgs& a, bool rnn, size_t ws_bytes, void* stream) {
     return cuda_status(launch_draft(a, rnn, static_cast<cudaStream_t>(stream)));
 }
 
-int dspark_draft_markov(const void* U, int u_dtype, const int32_t* anchor, const void* W1, const void* W2,
-                        int w_dtype, int R, int gamma, int V, int r, uint64_t seed, const uint32_t* req_ids,
-                        float temperature, int32_t* tokens, float* q_tok, double* lse, float* code, void* ws,
-                        size_t ws_bytes, void* stream) {
+int dspark_draft_markov_conf(const void* U, int u_dtype, const int32_t* anchor, const void* W1, const void* W2,
+                             int w_dtype, int R, int gamma, int V, int r, uint64_t seed, const uint32_t* req_ids,
+                             float temperature, int32_t* tokens, float* q_tok, double* lse, float* code,
+                             const dspark_conf_t* conf, void* ws, size_t ws_bytes, void* stream) {
     DraftArgs a;
     std::memset(&a, 0, sizeof a);
     a.U = U; a.u_dtype = u_dtype; a.anchor = anchor; a.W1 = W1; a.W2 = W2; a.w_dtype = w_dtype;
     a.R = R; a.gamma = gamma; a.V = V; a.r = r; a.d = 0; a.seed = seed; a.req_ids = req_ids;
     a.T = temperature; a.tokens = tokens; a.q_tok = q_tok; a.lse = lse; a.code = code; a.ws = ws;
+    const int st = attach_conf(a, false, conf);
+    if (st) return st;
     return draft_entry(a, false, ws_bytes, stream);
 }
 
-int dspark_draft_rnn(const void* U, int u_dtype, const int32_t* anchor, const void* W1, const void* W2,
-                     const void* Wgco, int w_dtype, const void* H, int d, int R, int gamma, int V, int r,
-                     uint64_t seed, const uint32_t* req_ids, float temperature, int32_t* tokens, float* q_tok,
-                     double* lse, float* code, float* state_out, void* ws, size_t ws_bytes, void* stream) {
+int dspark_draft_markov(const void* U, int u_dtype, const int32_t* anchor, const void* W1, const void* W2,
+                        int w_dtype, int R, int gamma, int V, int r, uint64_t seed, const uint32_t* req_ids,
+                        float temperature, int32_t* tokens, float* q_tok, double* lse, float* code, void* ws,
+                        size_t ws_bytes, void* stream) {
+    return dspark_draft_markov_conf(U, u_dtype, anchor, W1, W2, w_dtype, R, gamma, V, r, seed, req_ids, temperature,
+                                    tokens, q_tok, lse, code, nullptr, ws, ws_bytes, stream);
+}
+
+int dspark_draft_rnn_conf(const void* U, int u_dtype, const int32_t* anchor, const void* W1, const void* W2,
+                          const void* Wgco, int w_dtype, const void* H, int d, int R, int gamma, int V, int r,
+                          uint64_t seed, const uint32_t* req_ids, float temperature, int32_t* tokens, float* q_tok,
+                          double* lse, float* code, float* state_out, const dspark_conf_t* conf, void* ws,
+                          size_t ws_bytes, void* stream) {
     DraftArgs a;
     std::memset(&a, 0, sizeof a);
     a.U = U; a.u_dtype = u_dtype; a.anchor = anchor; a.W1 = W1; a.W2 = W2; a.Wgco = Wgco; a.H = H;
     a.w_dtype = w_dtype; a.R = R; a.gamma = gamma; a.V = V; a.r = r; a.d = d; a.seed = seed;
     a.req_ids = req_ids; a.T = temperature; a.tokens = tokens; a.q_tok = q_tok; a.lse = lse; a.code = code;
     a.state_out = state_out; a.ws = ws;
+    const int st = attach_conf(a, true, conf);
+    if (st) return st;
     return draft_entry(a, true, ws_bytes, stream);
+}
+
+int dspark_draft_rnn(const void* U, int u_dtype, const int32_t* anchor, const void* W1, const void* W2,
+                     const void* Wgco, int w_dtype, const void* H, int d, int R, int gamma, int V, int r,
+                     uint64_t seed, const uint32_t* req_ids, float temperature, int32_t* tokens, float* q_tok,
+                     double* lse, float* code, float* state_out, void* ws, size_t ws_bytes, void* stream) {
+    return dspark_draft_rnn_conf(U, u_dtype, anchor, W1, W2, Wgco, w_dtype, H, d, R, gamma, V, r, seed, req_ids,
+                                 temperature, tokens, q_tok, lse, code, state_out, nullptr, ws, ws_bytes, stream);
 }
 
 size_t dspark_verify_workspace_size(int R, int gamma, int V, int r) {
@@ -172,6 +214,14 @@ int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gam
     if (ws_bytes < sizeof(WsHeader)) return DSPARK_ERR_WORKSPACE;
     return cuda_status(launch_schedule(c, sps, n_sps, R, gamma, verify_len, theta, n_star, ws,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_schedule_threshold(const float* c, int R, int gamma, float theta, int mode, int32_t* verify_len,
+                              void* stream) {
+    if (R < 1 || gamma < 1 || gamma > 64) return DSPARK_ERR_SHAPE;
+    if (!c || !verify_len || (mode != 0 && mode != 1)) return DSPARK_ERR_INVALID_ARG;
+    return cuda_status(launch_schedule_threshold(c, R, gamma, theta, mode, verify_len,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -356,7 +356,29 @@ __device__ __forceinline__ void store_code(const DraftArgs& A, int r, int k, int
     A.ebf[2 * plane + (size_t)r * A.r + i] = f32_to_bf16_bits_rn(rest2);
 }
 
-// prep(k) for the Markov head: x_{k-1} then e_k = W1[x_{k-1}].
+// Confidence head (blog section 4.1, ConfidenceHead) for request r at step k:
+// c_k = sigmoid(wc . [h_k, W1[x_{k-1}]]), no bias.  The block's threads take
+// strided shares of the d + r products (f32 FMAs), then the warps and the
+// block add them in a fixed order.
+__device__ void confidence_head(const DraftArgs& A, int r, int k, int x) {
+    __shared__ float s_part[kPrepThreads / 32];
+    const int d = A.dc, rr = A.r;
+    const unsigned short* h = static_cast<const unsigned short*>(A.Hc) + ((size_t)r * A.gamma + (k - 1)) * d;
+    float t = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) t = fmaf(A.wc[i], bf16_bits_to_float(h[i]), t);
+    for (int i = threadIdx.x; i < rr; i += blockDim.x)
+        t = fmaf(A.wc[d + i], ld_elem(A.W1, A.w_dtype, (size_t)x * rr + i), t);
+    t = warp_sum(t);
+    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float u = 0.f;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) u += s_part[w];
+        A.conf[(size_t)r * A.gamma + (k - 1)] = 1.f / (1.f + expf(-u));
+    }
+}
+
+// prep(k) for the Markov head: x_{k-1} then e_k = W1[x_{k-1}] (and c_k).
 template <int UT, int WT>
 __global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, int k) {
     pdl_launch_dependents();
@@ -372,11 +394,13 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, i
     if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
     for (int i = threadIdx.x; i < A.r; i += blockDim.x)
         store_code(A, r, k, i, ld_elem(A.W1, A.w_dtype, (size_t)x * A.r + i));
+    if (A.conf) confidence_head(A, r, k, x);
 }
 
 // prep(k) for the RNN head (blog section 3.2 RNNHead.step), first half:
 // x_{k-1}, then the GRU input z = [s_{k-1}, W1[x_{k-1}], h_k] of the request
-// goes to the workspace; rnn_gru (below) forms G = z Wgco for all requests.
+// goes to the workspace (and c_k); rnn_gru (below) forms G = z Wgco for all
+// requests.
 template <int UT, int WT>
 __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int k) {
     pdl_launch_dependents();
@@ -406,6 +430,7 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int 
     for (int i = threadIdx.x; i < A.d; i += blockDim.x)
         z[2 * rr + i] = bf16_bits_to_float(Hb[((size_t)r * A.gamma + (k - 1)) * A.d + i]);
     for (int i = Kin + threadIdx.x; i < ldz; i += blockDim.x) z[i] = 0.f;
+    if (A.conf) confidence_head(A, r, k, x);
 }
 
 // The GRU step for all requests (blog section 3.2 RNNHead.step):

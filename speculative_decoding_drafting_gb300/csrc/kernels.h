@@ -35,6 +35,11 @@ struct DraftArgs {
     double* lse;
     float* code;
     float* state_out;
+    // confidence head c_k = sigmoid(wc . [h_k, W1[x_{k-1}]]) (conf == nullptr: off)
+    const void* Hc;           // [R, gamma, dc] bf16
+    const float* wc;          // [dc + r]
+    int dc;
+    float* conf;              // [R, gamma]
     // workspace carve-up
     void* ws;
     DraftPartial* parts;      // [2][R][n_slices]
@@ -102,6 +107,8 @@ int verify_carve(VerifyArgs& a, size_t ws_bytes);
 cudaError_t launch_verify(VerifyArgs& a, cudaStream_t s);
 
 size_t schedule_smem_bytes(int R, int gamma);
+cudaError_t launch_schedule_threshold(const float* c, int R, int gamma, float theta, int mode, int32_t* len,
+                                      cudaStream_t s);
 cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,
                             double* theta, int32_t* nstar, void* ws, cudaStream_t s);
 

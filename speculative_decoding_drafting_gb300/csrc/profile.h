@@ -16,6 +16,7 @@ enum ProfName : int {
     kPSchedule = 8,
     kPDraftPrepRnn = 9,
     kPDraftRnnGru = 10,
+    kPScheduleThreshold = 11,
 };
 
 void prof_begin(int name, cudaStream_t s);

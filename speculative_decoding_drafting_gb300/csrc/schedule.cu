@@ -290,4 +290,33 @@ cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R,
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Threshold filter (blog section 4.3, the confidence-threshold sweep): one
+// thread per request walks its positions in order, forming the same float32
+// prefix product a_{r,j} as the scheduler, and stops at the first position
+// whose score (a in mode 0, c in mode 1) falls below theta (or is NaN).
+__global__ void __launch_bounds__(256) schedule_threshold_kernel(const float* c, int R, int gamma, float theta,
+                                                                 int mode, int32_t* len) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= R) return;
+    const float* cr = c + (size_t)r * gamma;
+    float a = 1.f;
+    int n = 0;
+    for (int j = 0; j < gamma; ++j) {
+        const float cj = cr[j];
+        a = __fmul_rn(a, cj);
+        if (!((mode == 0 ? a : cj) >= theta)) break;
+        ++n;
+    }
+    len[r] = n;
+}
+
+cudaError_t launch_schedule_threshold(const float* c, int R, int gamma, float theta, int mode, int32_t* len,
+                                      cudaStream_t s) {
+    prof_begin(kPScheduleThreshold, s);
+    cudaError_t e = launch_kernel(schedule_threshold_kernel, dim3((R + 255) / 256), dim3(256), 0, s, false, c, R,
+                                  gamma, theta, mode, len);
+    prof_end(s);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace dspark

@@ -15,6 +15,9 @@ Shapes and value distributions follow the workloads of the DSpark pages:
 * target logits ``P[R, gamma+1, V]``: ``U`` with its last position repeated
   once more (the bonus row), plus normal noise;
 * confidences ``c[R, gamma] = sigmoid(N(mu, s^2))``;
+* confidence-head inputs (DSpark blog, section 4.1 ``ConfidenceHead``):
+  backbone states ``h[R, gamma, d]`` (bf16, N(0, sigma_h^2)) and the head's
+  weight vector ``w[d + r]`` (float32, N(0, sigma_w^2));
 * the steps-per-second table ``SPS[B] = 1000 / T(B)`` of the explainer's toy
   cost curve ``T(B) = 20 + (0.05 + 1.15 rho) B + (0.002 + 0.10 rho) B^2`` ms
   (DSpark explainer, section 04 "algorithm details"), tabulated for
@@ -112,7 +115,7 @@ def _child(seed: int, tag: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag])))
 
 
-_TAG = {"anchor": 1, "U": 2, "W1": 3, "W2": 4, "Pnoise": 5, "c": 6, "h": 7, "Wgco": 8}
+_TAG = {"anchor": 1, "U": 2, "W1": 3, "W2": 4, "Pnoise": 5, "c": 6, "h": 7, "Wgco": 8, "hconf": 9, "wconf": 10}
 
 
 def gen_anchor(w: Workload) -> np.ndarray:
@@ -172,6 +175,23 @@ def gen_H(w: Workload, rows=None) -> np.ndarray:
 def gen_Wgco(w: Workload) -> np.ndarray:
     g = _child(w.seed, _TAG["Wgco"])
     return _store(g.standard_normal((2 * w.r + w.d, 3 * w.r), dtype=np.float32) * np.float32(w.sigma_w), w.w_dtype)
+
+
+def gen_conf_H(w: Workload, d: int, rows=None) -> np.ndarray:
+    """Backbone states [R, gamma, d] (bf16) for the confidence head of a
+    Markov-head workload (an RNN-head workload uses its own ``gen_H``)."""
+    idx = np.arange(w.R) if rows is None else np.asarray(rows)
+    out = np.empty((len(idx), w.gamma, d), dtype=np.float32)
+    for n, i in enumerate(idx):
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, _TAG["hconf"], int(i)])))
+        out[n] = g.standard_normal((w.gamma, d), dtype=np.float32) * np.float32(w.sigma_h)
+    return f32_to_bf16_bits(out)
+
+
+def gen_conf_w(w: Workload, d: int) -> np.ndarray:
+    """Confidence-head weights [d + r] (float32): w[:d] meet h_k, w[d:] meet W1[x_{k-1}]."""
+    g = _child(w.seed, _TAG["wconf"])
+    return g.standard_normal(d + w.r, dtype=np.float32) * np.float32(w.sigma_w)
 
 
 def gen_c(w: Workload) -> np.ndarray:

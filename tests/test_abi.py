@@ -64,3 +64,32 @@ def test_invalid_arguments_rejected_before_any_device_work():
                            0.0, null, null, null, null, null, null, 0, null) == -1
     assert L.dspark_schedule(null, null, 10, 4, 5, null, null, null, null, 0, null) == -1
     assert L.dspark_schedule(null, null, 10, 1000, 16, null, null, null, null, 0, null) == -3
+
+
+def test_confidence_head_and_threshold_arguments_rejected_on_the_host():
+    L = binding.load()
+    null = None
+    fake = ctypes.c_void_p(4096)   # never dereferenced: every call below fails its host checks
+
+    def markov_conf(conf):
+        return L.dspark_draft_markov_conf(null, 0, null, null, null, 1, 4, 5, 4096, 32, 0, null, 1.0,
+                                          null, null, null, null, conf, null, 0, null)
+
+    # null weights or output
+    assert markov_conf(ctypes.byref(binding._Conf(fake, None, 8, fake))) == -1
+    assert markov_conf(ctypes.byref(binding._Conf(fake, fake, 8, None))) == -1
+    # d out of range; Markov head without H but d > 0
+    assert markov_conf(ctypes.byref(binding._Conf(fake, fake, 16385, fake))) == -3
+    assert markov_conf(ctypes.byref(binding._Conf(None, fake, 8, fake))) == -1
+    # a valid head still needs the draft's own inputs
+    assert markov_conf(ctypes.byref(binding._Conf(fake, fake, 8, fake))) == -1
+    assert markov_conf(None) == -1
+    st = L.dspark_draft_rnn_conf(null, 0, null, null, null, null, 1, null, 16, 4, 5, 4096, 32, 0, null, 1.0,
+                                 null, null, null, null, null, ctypes.byref(binding._Conf(None, None, 0, fake)),
+                                 null, 0, null)
+    assert st == -1
+    # threshold filter: mode, sizes, null pointers
+    assert L.dspark_schedule_threshold(fake, 4, 5, ctypes.c_float(0.5), 2, fake, null) == -1
+    assert L.dspark_schedule_threshold(fake, 4, 65, ctypes.c_float(0.5), 0, fake, null) == -3
+    assert L.dspark_schedule_threshold(fake, 0, 5, ctypes.c_float(0.5), 0, fake, null) == -3
+    assert L.dspark_schedule_threshold(null, 4, 5, ctypes.c_float(0.5), 0, fake, null) == -1
