@@ -358,14 +358,19 @@ __device__ __forceinline__ void store_code(const DraftArgs& A, int r, int k, int
 
 // Confidence head (blog section 4.1, ConfidenceHead) for request r at step k:
 // c_k = sigmoid(wc . [h_k, W1[x_{k-1}]]), no bias.  The block's threads take
-// strided shares of the d + r products (f32 FMAs), then the warps and the
-// block add them in a fixed order.
-__device__ void confidence_head(const DraftArgs& A, int r, int k, int x) {
-    __shared__ float s_part[kPrepThreads / 32];
-    const int d = A.dc, rr = A.r;
+// strided shares of the d + r products (f32 FMAs; the h_k terms first, from
+// confidence_h_part), then the warps and the block add them in a fixed order.
+__device__ __forceinline__ float confidence_h_part(const DraftArgs& A, int r, int k) {
+    const int d = A.dc;
     const unsigned short* h = static_cast<const unsigned short*>(A.Hc) + ((size_t)r * A.gamma + (k - 1)) * d;
     float t = 0.f;
     for (int i = threadIdx.x; i < d; i += blockDim.x) t = fmaf(A.wc[i], bf16_bits_to_float(h[i]), t);
+    return t;
+}
+
+__device__ void confidence_head(const DraftArgs& A, int r, int k, int x, float t) {
+    __shared__ float s_part[kPrepThreads / 32];
+    const int d = A.dc, rr = A.r;
     for (int i = threadIdx.x; i < rr; i += blockDim.x)
         t = fmaf(A.wc[d + i], ld_elem(A.W1, A.w_dtype, (size_t)x * rr + i), t);
     t = warp_sum(t);
@@ -382,6 +387,9 @@ __device__ void confidence_head(const DraftArgs& A, int r, int k, int x) {
 template <int UT, int WT>
 __global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, int k) {
     pdl_launch_dependents();
+    // the head's h_k half reads only the caller's inputs, so it runs before
+    // the wait, under the previous kernel's tail
+    const float th = (A.conf && k <= A.gamma) ? confidence_h_part(A, blockIdx.x, k) : 0.f;
     pdl_wait();
     const int r = blockIdx.x;
     int x;
@@ -394,7 +402,7 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, i
     if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
     for (int i = threadIdx.x; i < A.r; i += blockDim.x)
         store_code(A, r, k, i, ld_elem(A.W1, A.w_dtype, (size_t)x * A.r + i));
-    if (A.conf) confidence_head(A, r, k, x);
+    if (A.conf) confidence_head(A, r, k, x, th);
 }
 
 // prep(k) for the RNN head (blog section 3.2 RNNHead.step), first half:
@@ -404,6 +412,7 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_markov(DraftArgs A, i
 template <int UT, int WT>
 __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int k) {
     pdl_launch_dependents();
+    const float th = (A.conf && k <= A.gamma) ? confidence_h_part(A, blockIdx.x, k) : 0.f;
     pdl_wait();
     const int r = blockIdx.x;
     int x;
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int 
     for (int i = threadIdx.x; i < A.d; i += blockDim.x)
         z[2 * rr + i] = bf16_bits_to_float(Hb[((size_t)r * A.gamma + (k - 1)) * A.d + i]);
     for (int i = Kin + threadIdx.x; i < ldz; i += blockDim.x) z[i] = 0.f;
-    if (A.conf) confidence_head(A, r, k, x);
+    if (A.conf) confidence_head(A, r, k, x, th);
 }
 
 // The GRU step for all requests (blog section 3.2 RNNHead.step):
