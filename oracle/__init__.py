@@ -74,6 +74,11 @@ def lib():
             L.oracle_confidence.restype = i32
             L.oracle_threshold_lengths.argtypes = [P, i32, i32, ctypes.c_float, i32, P]
             L.oracle_threshold_lengths.restype = i32
+            L.oracle_ece.argtypes = [P, P, i32, i32]
+            L.oracle_ece.restype = dbl
+            L.oracle_sts_fit.argtypes = [P, P, i32, i32, P, i32, i32, P, P, P, P]
+            L.oracle_sts_fit.restype = i32
+            L.oracle_sts_apply.argtypes = [P, i32, i32, P, P]
             L.oracle_schedule_loop.argtypes = [P, P, i32, i32, i32, P, P]
             L.oracle_schedule_loop.restype = i32
             L.oracle_schedule_closed.argtypes = [P, P, i32, i32, i32, P, P, P]
@@ -273,3 +278,36 @@ def threshold_lengths(c, theta: float, mode: int = 0):
     if st != 0:
         raise RuntimeError(f"oracle_threshold_lengths failed: {st}")
     return L
+
+
+# ---------------------------------------------------------------- STS
+def ece(pred, y, M: int) -> float:
+    """Expected calibration error over M equal-width bins (Guo et al. 2017)."""
+    pred = _c(pred, np.float64)
+    y = _c(y, np.int32)
+    return float(lib().oracle_ece(_ptr(pred), _ptr(y), int(pred.size), int(M)))
+
+
+def sts_fit(c, accept_len, grid, M: int = 15):
+    """Sequential Temperature Scaling (blog section 4.2).  c [N, gamma] raw
+    confidences (float32), accept_len [N] accepted drafts per block, grid [G]
+    candidate temperatures.  Returns dict(t, g, ece, gap), one entry per position."""
+    c = _c(c, np.float32)
+    al = _c(accept_len, np.int32)
+    grid = _c(grid, np.float64)
+    N, gamma = c.shape
+    out = dict(t=np.zeros(gamma), g=np.zeros(gamma, np.int32), ece=np.zeros(gamma), gap=np.zeros(gamma))
+    st = lib().oracle_sts_fit(_ptr(c), _ptr(al), N, gamma, _ptr(grid), int(grid.size), int(M),
+                              _ptr(out["t"]), _ptr(out["g"]), _ptr(out["ece"]), _ptr(out["gap"]))
+    if st != 0:
+        raise RuntimeError(f"oracle_sts_fit failed: {st}")
+    return out
+
+
+def sts_apply(c, t):
+    """c'[n, k] = sigmoid(logit(c[n, k]) / t[k])."""
+    c = _c(c, np.float32)
+    t = _c(t, np.float64)
+    out = np.zeros(c.shape)
+    lib().oracle_sts_apply(_ptr(c), c.shape[0], c.shape[1], _ptr(t), _ptr(out))
+    return out

@@ -683,3 +683,82 @@ int oracle_threshold_lengths(const float* c, int R, int gamma, float theta, int 
     free(a);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Sequential Temperature Scaling (blog section 4.2).                   */
+/* ------------------------------------------------------------------ */
+
+/* Expected calibration error (Guo, Pleiss, Sun, Weinberger, "On
+ * Calibration of Modern Neural Networks", ICML 2017, section 2): the
+ * predictions fall into M equal-width bins over [0, 1] (bin b holds
+ * b/M <= p < (b+1)/M; p = 1 goes to the last bin), and
+ *   ECE = sum_b |B_b|/N * |mean of y over B_b - mean of p over B_b|. */
+double oracle_ece(const double* pred, const int32_t* y, int N, int M) {
+    if (N <= 0 || M <= 0) return 0.0;
+    double* sp = (double*)calloc((size_t)M, sizeof(double));
+    double* sy = (double*)calloc((size_t)M, sizeof(double));
+    long* cnt = (long*)calloc((size_t)M, sizeof(long));
+    if (!sp || !sy || !cnt) { free(sp); free(sy); free(cnt); return NAN; }
+    for (int n = 0; n < N; ++n) {
+        int b = (int)floor(pred[n] * (double)M);
+        if (b < 0) b = 0;
+        if (b > M - 1) b = M - 1;
+        cnt[b] += 1;
+        sp[b] += pred[n];
+        sy[b] += (double)(y[n] != 0);
+    }
+    double ece = 0.0;
+    for (int b = 0; b < M; ++b) {
+        if (cnt[b] == 0) continue;
+        const double acc = sy[b] / (double)cnt[b], conf = sp[b] / (double)cnt[b];
+        ece += ((double)cnt[b] / (double)N) * fabs(acc - conf);
+    }
+    free(sp); free(sy); free(cnt);
+    return ece;
+}
+
+/* Temperature scaling of one confidence: sigmoid(logit(c) / t), with
+ * logit(c) = ln c - ln(1 - c) (c = 0 and c = 1 stay where they are). */
+static double temper(double c, double t) {
+    const double z = log(c) - log1p(-c);
+    return sigmoid(z / t);
+}
+
+int oracle_sts_fit(const float* c, const int32_t* accept_len, int N, int gamma,
+                   const double* grid, int G, int M,
+                   double* t_out, int32_t* g_out, double* ece_out, double* gap_out) {
+    if (N <= 0 || gamma <= 0 || G <= 0 || M <= 0) return -3;
+    double* a_prev = (double*)malloc(sizeof(double) * (size_t)N);   /* prefix survival of positions < k */
+    double* pred = (double*)malloc(sizeof(double) * (size_t)N);
+    int32_t* y = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    if (!a_prev || !pred || !y) { free(a_prev); free(pred); free(y); return -1; }
+    for (int n = 0; n < N; ++n) a_prev[n] = 1.0;
+    for (int k = 1; k <= gamma; ++k) {
+        /* outcome at position k: the first k drafts were all accepted */
+        for (int n = 0; n < N; ++n) y[n] = accept_len[n] >= k;
+        double best = INFINITY, second = INFINITY;
+        int gbest = 0;
+        for (int g = 0; g < G; ++g) {
+            for (int n = 0; n < N; ++n)
+                pred[n] = a_prev[n] * temper((double)c[(size_t)n * gamma + (size_t)(k - 1)], grid[g]);
+            const double e = oracle_ece(pred, y, N, M);
+            if (e < best) { second = best; best = e; gbest = g; }   /* ties keep the lowest index */
+            else if (e < second) { second = e; }
+        }
+        t_out[k - 1] = grid[gbest];
+        g_out[k - 1] = gbest;
+        ece_out[k - 1] = best;
+        gap_out[k - 1] = second - best;
+        /* fix this position's temperature before the next one */
+        for (int n = 0; n < N; ++n)
+            a_prev[n] *= temper((double)c[(size_t)n * gamma + (size_t)(k - 1)], grid[gbest]);
+    }
+    free(a_prev); free(pred); free(y);
+    return 0;
+}
+
+void oracle_sts_apply(const float* c, int N, int gamma, const double* t, double* c_out) {
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < gamma; ++k)
+            c_out[(size_t)n * gamma + k] = temper((double)c[(size_t)n * gamma + k], t[k]);
+}

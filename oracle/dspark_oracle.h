@@ -12,7 +12,8 @@
  * Sources (the pages are cited by title and section):
  *  - "DSpark: DeepSeek 线上跑的投机解码" (blog), section 3.2: Markov head
  *    B_k = W1[x_{k-1}] W2, RNN head step, and the sequential stage loop;
- *    section 4.1: the confidence head; section 4.3: prefix survival, the
+ *    section 4.1: the confidence head; section 4.2: sequential temperature
+ *    scaling; section 4.3: prefix survival, the
  *    hardware-aware scheduler and the confidence-threshold sweep.
  *  - "DSpark explainer", section 03: q_k = softmax(U_k + B_k);
  *    section 04: a_j = c_1 ... c_j, B, tau, Theta = tau * SPS(B);
@@ -20,6 +21,8 @@
  *    r(v) = max(p(v) - q(v), 0) / sum_u max(p(u) - q(u), 0).
  *  - Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers:
  *    As Easy as 1, 2, 3", SC'11.
+ *  - Expected calibration error: Guo, Pleiss, Sun, Weinberger, "On
+ *    Calibration of Modern Neural Networks", ICML 2017, section 2.
  */
 #ifndef DSPARK_ORACLE_H
 #define DSPARK_ORACLE_H
@@ -120,6 +123,25 @@ int oracle_schedule_loop(const float* c, const double* sps, int n_sps, int R, in
  * comparisons n = 0..n* the stop rule made (+inf if none).  Returns n*. */
 int oracle_schedule_closed(const float* c, const double* sps, int n_sps, int R, int gamma,
                            int32_t* lengths, double* theta, double* min_rel_gap);
+
+/* Expected calibration error (Guo et al., ICML 2017, section 2) of
+ * predictions pred[N] against outcomes y[N] (nonzero = 1) over M
+ * equal-width bins of [0, 1]; p = 1 falls in the last bin. */
+double oracle_ece(const double* pred, const int32_t* y, int N, int M);
+
+/* Sequential Temperature Scaling (blog section 4.2): per position k = 1..gamma,
+ * left to right, the grid temperature t minimising the ECE of the calibrated
+ * prefix survival a'_k = prod_{i<=k} sigmoid(logit(c_i) / t_i) (t_i fixed for
+ * i < k, t_k = t) against the outcome accept_len >= k; ties keep the lowest
+ * grid index.  c [N,gamma] float32 raw confidences, accept_len [N], grid [G].
+ * Outputs per position: t_out, g_out (grid index), ece_out (the minimum) and
+ * gap_out (second-smallest ECE minus the minimum, +inf if G = 1). */
+int oracle_sts_fit(const float* c, const int32_t* accept_len, int N, int gamma,
+                   const double* grid, int G, int M,
+                   double* t_out, int32_t* g_out, double* ece_out, double* gap_out);
+
+/* c_out[n,k] = sigmoid(logit(c[n,k]) / t[k]). */
+void oracle_sts_apply(const float* c, int N, int gamma, const double* t, double* c_out);
 
 #ifdef __cplusplus
 }

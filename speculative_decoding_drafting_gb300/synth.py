@@ -18,6 +18,11 @@ Shapes and value distributions follow the workloads of the DSpark pages:
 * confidence-head inputs (DSpark blog, section 4.1 ``ConfidenceHead``):
   backbone states ``h[R, gamma, d]`` (bf16, N(0, sigma_h^2)) and the head's
   weight vector ``w[d + r]`` (float32, N(0, sigma_w^2));
+* an STS calibration set (DSpark blog, section 4.2): per block n and
+  position k a latent acceptance probability ``alpha = sigmoid(u)``,
+  ``u ~ N(mu, s^2)``, outcomes drawn position by position (``accept_len`` =
+  the leading successes), and raw confidences ``sigmoid(tau u)`` that are
+  overconfident by a known factor ``tau``;
 * the steps-per-second table ``SPS[B] = 1000 / T(B)`` of the explainer's toy
   cost curve ``T(B) = 20 + (0.05 + 1.15 rho) B + (0.002 + 0.10 rho) B^2`` ms
   (DSpark explainer, section 04 "algorithm details"), tabulated for
@@ -115,7 +120,8 @@ def _child(seed: int, tag: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag])))
 
 
-_TAG = {"anchor": 1, "U": 2, "W1": 3, "W2": 4, "Pnoise": 5, "c": 6, "h": 7, "Wgco": 8, "hconf": 9, "wconf": 10}
+_TAG = {"anchor": 1, "U": 2, "W1": 3, "W2": 4, "Pnoise": 5, "c": 6, "h": 7, "Wgco": 8, "hconf": 9, "wconf": 10,
+        "sts": 11}
 
 
 def gen_anchor(w: Workload) -> np.ndarray:
@@ -198,6 +204,25 @@ def gen_c(w: Workload) -> np.ndarray:
     g = _child(w.seed, _TAG["c"])
     x = g.normal(w.c_mu, w.c_sigma, size=(w.R, w.gamma))
     return (1.0 / (1.0 + np.exp(-x))).astype(np.float32)
+
+
+def gen_sts_set(N: int, gamma: int, tau: float = 2.0, mu: float = 1.5, s: float = 1.0, seed: int = 0):
+    """STS calibration set: raw confidences c [N, gamma] (float32) and
+    accept_len [N] (int32).  u ~ N(mu, s^2); position k of block n is accepted
+    with probability sigmoid(u[n, k]) (a uniform below it), accept_len counts
+    the leading acceptances, and c = sigmoid(tau u)."""
+    g = _child(seed, _TAG["sts"])
+    u = g.normal(mu, s, size=(N, gamma))
+    v = g.random(size=(N, gamma))
+    ok = v < 1.0 / (1.0 + np.exp(-u))
+    accept_len = np.where(ok.all(axis=1), gamma, np.argmin(ok, axis=1)).astype(np.int32)
+    c = (1.0 / (1.0 + np.exp(-tau * u))).astype(np.float32)
+    return c, accept_len
+
+
+def sts_grid(G: int = 256, lo: float = 0.1, hi: float = 10.0) -> np.ndarray:
+    """Candidate temperatures, log-spaced over [lo, hi] (float64)."""
+    return np.geomspace(lo, hi, G)
 
 
 def toy_cost_ms(B: np.ndarray, rho: float) -> np.ndarray:

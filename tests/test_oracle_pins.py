@@ -559,3 +559,78 @@ def test_threshold_filter_invariants():
         if theta > 1:
             assert np.all(L1 == 0)
     assert oracle.threshold_lengths(c, 0.5, 0)[3] <= 2 and oracle.threshold_lengths(c, 1.0, 0)[5] == w.gamma
+
+
+# ------------------------------------------------------------------ STS
+def test_ece_hand_worked():
+    """Guo et al. 2017, section 2, by hand: M = 10, predictions 0.1, 0.1, 0.9,
+    0.9 with outcomes 0, 1, 1, 1: bin 1 has accuracy 1/2 and confidence 0.1,
+    bin 9 accuracy 1 and confidence 0.9, so ECE = 1/2 (0.4) + 1/2 (0.1) = 0.25."""
+    assert abs(oracle.ece([0.1, 0.1, 0.9, 0.9], [0, 1, 1, 1], 10) - 0.25) < 1e-15
+    # bin edges, M = 4: p = 0.25 opens bin 1, so 0.25 and 0.24 sit apart
+    # (1/2 (0.75) + 1/2 (0.24), not one bin's |1/2 - 0.245|); p = 1 shares
+    # bin 3 with 0.75 and 0.8 (|2/3 - 0.85|, not 1/3 + 2/3 |1 - 0.775|)
+    assert abs(oracle.ece([0.25, 0.24], [1, 0], 4) - (0.5 * 0.75 + 0.5 * 0.24)) < 1e-15
+    assert abs(oracle.ece([1.0, 0.75, 0.8], [0, 1, 1], 4) - abs(2 / 3 - 2.55 / 3)) < 1e-15
+    # calibrated in the bins: 30% positives at p = 0.3 gives 0
+    assert oracle.ece([0.3] * 10, [1, 1, 1] + [0] * 7, 10) < 1e-15
+
+
+def test_sts_apply_closed_forms():
+    c = np.array([[0.5, special.expit(2.0), 0.0, 1.0]], np.float32)
+    out = oracle.sts_apply(c, np.array([3.0, 2.0, 0.5, 0.5]))
+    assert out[0, 0] == 0.5                                  # logit 0 is fixed by every t
+    # sigmoid(2) stored in float32, then tempered by 2: sigmoid(logit(float32 value) / 2)
+    z = math.log(float(c[0, 1])) - math.log1p(-float(c[0, 1]))
+    assert abs(out[0, 1] - special.expit(z / 2)) < 1e-15 and abs(out[0, 1] - special.expit(1.0)) < 1e-7
+    assert out[0, 2] == 0.0 and out[0, 3] == 1.0
+    # t = 1 is the identity; order inside a position is preserved for any t
+    cc = np.sort(np.random.default_rng(1).random((50, 1)).astype(np.float32), axis=0)
+    np.testing.assert_allclose(oracle.sts_apply(cc, [1.0]), cc.astype(np.float64), rtol=1e-12)
+    for t in (0.3, 4.0):
+        assert np.all(np.diff(oracle.sts_apply(cc, [t])[:, 0]) >= 0)
+
+
+@pytest.mark.parametrize("tau", [2.0, 1.0, 0.5])
+def test_sts_recovers_a_known_overconfidence(tau):
+    """Raw confidences sigmoid(tau u) of events with probability sigmoid(u):
+    sigmoid(logit(c) / tau) is exactly calibrated, so the left-to-right search
+    should settle near t = tau at every position (sampling noise and the grid
+    step of 1.8% aside), and lower the ECE it was given."""
+    c, al = synth.gen_sts_set(20000, 5, tau=tau, seed=3)
+    grid = synth.sts_grid(256, 0.1, 10.0)
+    r = oracle.sts_fit(c, al, grid, 15)
+    assert np.all(np.abs(np.log(r["t"] / tau)) < 0.15), r["t"]
+    raw = np.cumprod(c.astype(np.float64), axis=1)
+    for k in range(5):
+        e_raw = oracle.ece(raw[:, k], (al >= k + 1).astype(np.int32), 15)
+        assert r["ece"][k] <= e_raw + 1e-12
+        if tau != 1.0:
+            assert r["ece"][k] < 0.6 * e_raw
+
+
+def test_sts_is_sequential():
+    """Position k's temperature depends only on outcomes up to k: changing
+    accept_len among values above k leaves t_1..t_k unchanged; a one-point
+    grid returns that point everywhere."""
+    c, al = synth.gen_sts_set(3000, 4, tau=2.0, seed=5)
+    grid = synth.sts_grid(64, 0.2, 8.0)
+    r = oracle.sts_fit(c, al, grid, 10)
+    al2 = al.copy()
+    al2[al2 >= 3] = 4 - (al2[al2 >= 3] - 3)          # swap 3 <-> 4 above position 2
+    r2 = oracle.sts_fit(c, al2, grid, 10)
+    np.testing.assert_array_equal(r["g"][:2], r2["g"][:2])
+    one = oracle.sts_fit(c, al, np.array([1.7]), 10)
+    assert np.all(one["t"] == 1.7) and np.all(np.isinf(one["gap"]))
+
+
+def test_sts_first_position_is_a_plain_grid_search():
+    """At k = 1 nothing is fixed yet: t_1 is the grid point whose tempered
+    c_1 has the smallest ECE against accept_len >= 1, found here by
+    evaluating every grid point with the ECE pinned above."""
+    c, al = synth.gen_sts_set(2000, 3, tau=1.5, seed=9)
+    grid = synth.sts_grid(40, 0.3, 5.0)
+    r = oracle.sts_fit(c, al, grid, 12)
+    y = (al >= 1).astype(np.int32)
+    e = [oracle.ece(oracle.sts_apply(c[:, :1], [t])[:, 0], y, 12) for t in grid]
+    assert r["g"][0] == int(np.argmin(e)) and abs(r["ece"][0] - min(e)) < 1e-15
