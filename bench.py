@@ -368,6 +368,47 @@ def measure_confidence_and_threshold(w, U, anchor, W1, W2, c, steps: int, devc, 
     }
 
 
+def measure_sts(steps: int, devc):
+    """Sequential Temperature Scaling fit on a calibration set of 65536 draft
+    blocks (gamma = 8, 256 log-spaced temperatures in [0.1, 10], 15 bins):
+    fits per second and the per-kernel table.  Each fit evaluates
+    N gamma G calibrated prefix-survival values."""
+    import torch
+    from speculative_decoding_drafting_gb300 import binding
+    N, gamma, G, M = 65536, 8, 256, 15
+    c, al = synth.gen_sts_set(N, gamma, tau=2.0, seed=1)
+    cd = torch.from_numpy(c).to(devc)
+    ad = torch.from_numpy(al).to(devc)
+    grid = torch.from_numpy(synth.sts_grid(G, 0.1, 10.0)).to(devc)
+    out = binding.sts_fit(cd, ad, grid, M)
+    for _ in range(3):
+        binding.sts_fit(cd, ad, grid, M, ws=out["ws"], out=out)
+    stream = torch.cuda.current_stream()
+    ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        binding.sts_fit(cd, ad, grid, M, ws=out["ws"], out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    binding.profile_enable(True)
+    for _ in range(steps):
+        binding.sts_fit(cd, ad, grid, M, ws=out["ws"], out=out)
+    torch.cuda.synchronize()
+    binding.profile_enable(False)
+    table = {}
+    for name, t in binding.profile_collect():
+        e = table.setdefault(name, [0, 0.0])
+        e[0] += 1
+        e[1] += t
+    per = float(np.median(ms))
+    return {"workload": f"calibration set N={N} gamma={gamma}, G={G} temperatures, M={M} bins",
+            "ms_per_fit": round(per, 4), "evaluations_per_s": round(N * gamma * G / (per / 1000.0), 1),
+            "t": [round(float(v), 4) for v in out["t"].cpu().numpy()],
+            "kernels_us_per_launch": {k: round(1000 * v / n, 2) for k, (n, v) in table.items()}}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,7 +419,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the RNN-head draft, confidence-head and threshold-filter measurements")
+                    help="skip the RNN-head draft, confidence-head, threshold-filter and STS measurements")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -526,6 +567,7 @@ def main(argv=None):
         variants = {"rnn_draft": measure_rnn_draft(max(3, args.steps // 2), 3, devc, flush)}
         variants.update(measure_confidence_and_threshold(w, U, anchor, W1, W2, c, max(5, args.steps // 2), devc,
                                                          flush))
+        variants["sts_fit"] = measure_sts(max(5, args.steps // 2), devc)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -164,12 +164,18 @@ int dspark_draft_rnn(const void* U, int u_dtype, const int32_t* anchor,
  * turns the head off (the plain entry points below pass null).  Errors:
  * INVALID_ARG for a null w or c (or Markov H = NULL with d > 0), SHAPE for d
  * outside [0, 16384].
+ *   t  [gamma]        double    per-position temperatures of Sequential
+ *                               Temperature Scaling (blog section 4.2; for
+ *                               example dspark_sts_fit's t_out), device, may be
+ *                               NULL: c_k = sigmoid(w . [h_k, W1[x_{k-1}]] / t_k)
+ *                               (the division in float32 by (float)(1 / t_k))
  */
 typedef struct {
     const void* H;
     const float* w;
     int d;
     float* c;
+    const double* t;
 } dspark_conf_t;
 
 /* dspark_draft_markov with the confidence head. */
@@ -301,6 +307,48 @@ int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gam
  */
 int dspark_schedule_threshold(const float* c, int R, int gamma, float theta, int mode,
                               int32_t* verify_len, void* stream);
+
+/* -------------------------------------------------------------------- STS */
+
+/*
+ * Sequential Temperature Scaling (blog section 4.2): fit one temperature per
+ * draft position on a calibration set, left to right.  The calibrated
+ * confidence is c' = sigmoid(logit(c) / t_k), logit(c) = ln c - ln(1 - c).
+ * Position k takes, from the grid, the t whose calibrated prefix survival
+ * a'_{n,k} = c'_{n,1} ... c'_{n,k} (t_1 .. t_{k-1} already fixed) has the
+ * smallest expected calibration error against the outcome accept_len[n] >= k
+ * (Guo et al., ICML 2017, section 2: M equal-width bins over [0, 1], p = 1 in
+ * the last bin, ECE = sum_b |B_b|/N |mean y - mean a'|); ties keep the lowest
+ * grid index.
+ *   c          [N, gamma]  float   raw confidences in [0, 1] (device)
+ *   accept_len [N]         int32   accepted drafts of each calibration block
+ *                                  (verification of all gamma positions)
+ *   grid       [G]         double  candidate temperatures, positive (device)
+ * Outputs (device, caller-owned), per position: t_out [gamma] double,
+ * g_out [gamma] int32 (grid index), ece_out [gamma] double (the minimum),
+ * gap_out [gamma] double (second-smallest ECE minus the minimum; +inf if G = 1).
+ * Precision: the calibrated prefix survival is formed in float32, except that
+ * a value within 1e-4 bin widths of a bin edge is formed again in double
+ * (which bin it joins is decided as in double arithmetic); the prefix
+ * survival carried between positions is double; per-bin sums are exact
+ * (sums of p as integers of 2^-32).  The ECE values are accurate to about
+ * 1e-7; a position whose gap is below that may pick either neighbour.
+ * Requirements: 1 <= N <= 2^24, 1 <= gamma <= 64, 1 <= G <= 4096, 1 <= M <= 32
+ * (SHAPE otherwise), workspace of dspark_sts_workspace_size bytes (256-byte
+ * aligned).
+ */
+size_t dspark_sts_workspace_size(int N, int gamma, int G, int M);
+int dspark_sts_fit(const float* c, const int32_t* accept_len, int N, int gamma,
+                   const double* grid, int G, int M,
+                   double* t_out, int32_t* g_out, double* ece_out, double* gap_out,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Apply per-position temperatures: out[n,k] = sigmoid(logit(c[n,k]) / t[k])
+ * in float32 (c = 0 and c = 1 stay put).  c, out [N, gamma] float, t [gamma]
+ * double, all device.  No workspace.
+ */
+int dspark_sts_apply(const float* c, int N, int gamma, const double* t, float* out, void* stream);
 
 /* -------------------------------------------------------------- profiling */
 

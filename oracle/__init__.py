@@ -70,7 +70,7 @@ def lib():
                                         u64, P, dbl, P, P, P, P, P, P, P, i32]
             L.oracle_verify.restype = i32
             L.oracle_prefix_survival.argtypes = [P, i32, i32, P]
-            L.oracle_confidence.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32, i32, P]
+            L.oracle_confidence.argtypes = [P, i32, P, i32, P, P, P, i32, i32, i32, i32, i32, P, P]
             L.oracle_confidence.restype = i32
             L.oracle_threshold_lengths.argtypes = [P, i32, i32, ctypes.c_float, i32, P]
             L.oracle_threshold_lengths.restype = i32
@@ -216,10 +216,11 @@ def verify(P, U, W2, tokens, qx, lse, code, T: float, seed: int, verify_len=None
 
 
 # ---------------------------------------------------------------- confidence head
-def confidence(H, W1, w, anchor, tokens):
+def confidence(H, W1, w, anchor, tokens, temps=None):
     """c [R, gamma] (double) = sigmoid(w . [h_k, W1[x_{k-1}]]) (blog section 4.1).
     H [R, gamma, d] and W1 [V, r] in storage dtype, w [d + r] float32,
-    anchor [R] = x_0, tokens [R, gamma] = the drafted x_1..x_gamma."""
+    anchor [R] = x_0, tokens [R, gamma] = the drafted x_1..x_gamma; temps
+    [gamma] (optional): per-position temperatures, sigmoid(logit / t_k)."""
     H, W1 = _c(H), _c(W1)
     w = _c(w, np.float32)
     anchor = _c(anchor, np.int32)
@@ -228,8 +229,9 @@ def confidence(H, W1, w, anchor, tokens):
     V, r = W1.shape
     assert w.shape == (d + r,) and anchor.shape == (R,) and tokens.shape == (R, gamma)
     c = np.zeros((R, gamma))
+    tt = None if temps is None else _c(temps, np.float64)
     st = lib().oracle_confidence(_ptr(H), _dt(H), _ptr(W1), _dt(W1), _ptr(w), _ptr(anchor), _ptr(tokens),
-                                 R, gamma, V, d, r, _ptr(c))
+                                 R, gamma, V, d, r, _ptr(tt), _ptr(c))
     if st != 0:
         raise RuntimeError(f"oracle_confidence failed: {st}")
     return c

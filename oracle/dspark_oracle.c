@@ -534,7 +534,7 @@ int oracle_verify(const void* P, int p_dtype, const void* U, int u_dtype,
 /* ------------------------------------------------------------------ */
 int oracle_confidence(const void* H, int h_dtype, const void* W1, int w_dtype, const float* w,
                       const int32_t* anchor, const int32_t* tokens,
-                      int R, int gamma, int V, int d, int r, double* c) {
+                      int R, int gamma, int V, int d, int r, const double* temps, double* c) {
     if (R <= 0 || gamma <= 0 || V <= 0 || d < 0 || r <= 0) return -3;
     for (int ri = 0; ri < R; ++ri) {
         for (int k = 1; k <= gamma; ++k) {
@@ -547,6 +547,8 @@ int oracle_confidence(const void* H, int h_dtype, const void* W1, int w_dtype, c
             const size_t hrow = ((size_t)ri * gamma + (size_t)(k - 1)) * (size_t)d;
             for (int i = 0; i < d; ++i) t += (double)w[i] * ld(H, h_dtype, hrow + (size_t)i);
             for (int i = 0; i < r; ++i) t += (double)w[d + i] * ld(W1, w_dtype, (size_t)prev * r + (size_t)i);
+            /* with sequential temperature scaling (section 4.2): sigmoid(t / t_k) */
+            if (temps) t /= temps[k - 1];
             c[(size_t)ri * gamma + (size_t)(k - 1)] = sigmoid(t);
         }
     }

@@ -98,10 +98,12 @@ int oracle_verify(const void* P, int p_dtype, const void* U, int u_dtype,
  * with no bias, x_0 = anchor[r] and x_{k-1} = tokens[r,k-2] for k >= 2.
  * H is [R,gamma,d] in h_dtype, W1 [V,r] in w_dtype, w [d + r] float32 (the
  * first d entries weigh h_k, the last r the embedding).  c is [R,gamma].
+ * temps [gamma] (may be NULL): per-position temperatures of section 4.2,
+ * c = sigmoid(w . [h_k, W1[x_{k-1}]] / temps[k-1]).
  * Returns 0, or -6 for a token outside [0, V). */
 int oracle_confidence(const void* H, int h_dtype, const void* W1, int w_dtype, const float* w,
                       const int32_t* anchor, const int32_t* tokens,
-                      int R, int gamma, int V, int d, int r, double* c);
+                      int R, int gamma, int V, int d, int r, const double* temps, double* c);
 
 /* Threshold filter: lengths[r] = the longest prefix of positions whose score
  * is >= theta; score = a[r,j] (mode 0, float32 prefix product) or c[r,j]

@@ -74,12 +74,17 @@ def load(build_if_missing: bool = True):
                                             P, P, P, P, P, P, P, sz, P]
         L.dspark_schedule.argtypes = [P, P, i32, i32, i32, P, P, P, P, sz, P]
         L.dspark_schedule_threshold.argtypes = [P, i32, i32, f32, i32, P, P]
+        L.dspark_sts_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.dspark_sts_workspace_size.restype = sz
+        L.dspark_sts_fit.argtypes = [P, P, i32, i32, P, i32, i32, P, P, P, P, P, sz, P]
+        L.dspark_sts_apply.argtypes = [P, i32, i32, P, P, P]
         L.dspark_profile_enable.argtypes = [i32]
         L.dspark_profile_collect.argtypes = [P, P, i32]
         L.dspark_profile_kernel_name.argtypes = [i32]
         L.dspark_profile_kernel_name.restype = ctypes.c_char_p
         for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_draft_markov_conf", "dspark_draft_rnn_conf",
-                     "dspark_verify", "dspark_schedule", "dspark_schedule_threshold",
+                     "dspark_verify", "dspark_schedule", "dspark_schedule_threshold", "dspark_sts_fit",
+                     "dspark_sts_apply",
                      "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
             getattr(L, name).restype = i32
         _lib = L
@@ -116,10 +121,11 @@ def _check(fn: str, code: int):
 
 class _Conf(ctypes.Structure):
     """dspark_conf_t: the confidence head's arguments."""
-    _fields_ = [("H", ctypes.c_void_p), ("w", ctypes.c_void_p), ("d", ctypes.c_int), ("c", ctypes.c_void_p)]
+    _fields_ = [("H", ctypes.c_void_p), ("w", ctypes.c_void_p), ("d", ctypes.c_int), ("c", ctypes.c_void_p),
+                ("t", ctypes.c_void_p)]
 
 
-def _conf(conf_w, conf_H, out, R, gamma, dev):
+def _conf(conf_w, conf_H, out, R, gamma, dev, conf_t=None):
     """Fill out["c"] and return a dspark_conf_t pointer (None: head off)."""
     if conf_w is None:
         return None, None
@@ -129,7 +135,9 @@ def _conf(conf_w, conf_H, out, R, gamma, dev):
         raise TypeError("confidence-head H must be bfloat16")
     if "c" not in out:
         out["c"] = torch.empty((R, gamma), dtype=torch.float32, device=dev)
-    st = _Conf(_p(conf_H), _p(conf_w), 0 if conf_H is None else conf_H.shape[2], _p(out["c"]))
+    if conf_t is not None and conf_t.dtype != torch.float64:
+        raise TypeError("per-position temperatures must be float64")
+    st = _Conf(_p(conf_H), _p(conf_w), 0 if conf_H is None else conf_H.shape[2], _p(out["c"]), _p(conf_t))
     return st, ctypes.byref(st)
 
 
@@ -162,7 +170,7 @@ def schedule_workspace_bytes(R, gamma) -> int:
 
 
 def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None, ws=None, out=None, stream=None,
-                 conf_w=None, conf_H=None):
+                 conf_w=None, conf_H=None, conf_t=None):
     """Markov-head drafting (``dspark_draft_markov``).  Returns a dict of outputs.
     With ``conf_w`` ([d + r] float32) and ``conf_H`` ([R, gamma, d] bfloat16)
     the fused confidence head (``dspark_draft_markov_conf``) adds ``c``."""
@@ -178,7 +186,7 @@ def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None,
     nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, 0)
     if ws is None:
         ws = _workspace(nbytes, dev)
-    keep, cp = _conf(conf_w, conf_H, out, R, gamma, dev)
+    keep, cp = _conf(conf_w, conf_H, out, R, gamma, dev, conf_t)
     code = L.dspark_draft_markov_conf(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _dt(W1), R, gamma, V, r,
                                       int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
                                       _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
@@ -189,7 +197,7 @@ def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None,
 
 
 def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids=None, ws=None, out=None,
-              stream=None, conf_w=None, conf_H=None):
+              stream=None, conf_w=None, conf_H=None, conf_t=None):
     """RNN-head drafting (``dspark_draft_rnn``).  With ``conf_w`` the fused
     confidence head adds ``c`` (``conf_H`` None: the head's own H)."""
     L = load()
@@ -208,7 +216,7 @@ def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids
     nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, d)
     if ws is None:
         ws = _workspace(nbytes, dev)
-    keep, cp = _conf(conf_w, conf_H, out, R, gamma, dev)
+    keep, cp = _conf(conf_w, conf_H, out, R, gamma, dev, conf_t)
     code = L.dspark_draft_rnn_conf(_p(U), _dt(U), _p(anchor), _p(W1), _p(W2), _p(Wgco), _dt(W1), _p(H), d,
                                    R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
                                    _p(out["tokens"]), _p(out["q_tok"]), _p(out["lse"]), _p(out["code"]),
@@ -273,6 +281,40 @@ def schedule_threshold(c, theta: float, mode: int = 0, out=None, stream=None):
         out = torch.empty((R,), dtype=torch.int32, device=c.device)
     code = L.dspark_schedule_threshold(_p(c), R, gamma, float(theta), int(mode), _p(out), _stream(stream))
     _check("dspark_schedule_threshold", code)
+    return out
+
+
+def sts_fit(c, accept_len, grid, M: int = 15, ws=None, out=None, stream=None):
+    """Sequential Temperature Scaling (``dspark_sts_fit``): per-position
+    temperatures t, grid indices g, minimum ECE and the gap to the second."""
+    L = load()
+    N, gamma = c.shape
+    G = grid.numel()
+    dev = c.device
+    if grid.dtype != torch.float64 or accept_len.dtype != torch.int32:
+        raise TypeError("grid must be float64 and accept_len int32")
+    if out is None:
+        out = dict(t=torch.empty((gamma,), dtype=torch.float64, device=dev),
+                   g=torch.empty((gamma,), dtype=torch.int32, device=dev),
+                   ece=torch.empty((gamma,), dtype=torch.float64, device=dev),
+                   gap=torch.empty((gamma,), dtype=torch.float64, device=dev))
+    if ws is None:
+        ws = _workspace(L.dspark_sts_workspace_size(N, gamma, G, M), dev)
+    code = L.dspark_sts_fit(_p(c), _p(accept_len), N, gamma, _p(grid), G, M, _p(out["t"]), _p(out["g"]),
+                            _p(out["ece"]), _p(out["gap"]), _p(ws), ws.numel(), _stream(stream))
+    _check("dspark_sts_fit", code)
+    out["ws"] = ws
+    return out
+
+
+def sts_apply(c, t, out=None, stream=None):
+    """out = sigmoid(logit(c) / t[k]) per position (``dspark_sts_apply``)."""
+    L = load()
+    N, gamma = c.shape
+    if out is None:
+        out = torch.empty_like(c)
+    code = L.dspark_sts_apply(_p(c), N, gamma, _p(t), _p(out), _stream(stream))
+    _check("dspark_sts_apply", code)
     return out
 
 

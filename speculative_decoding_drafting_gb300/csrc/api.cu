@@ -107,6 +107,7 @@ static int attach_conf(DraftArgs& a, bool rnn, const dspark_conf_t* conf) {
     }
     a.wc = conf->w;
     a.conf = conf->c;
+    a.tc = conf->t;
     return DSPARK_OK;
 }
 
@@ -214,6 +215,28 @@ int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gam
     if (ws_bytes < sizeof(WsHeader)) return DSPARK_ERR_WORKSPACE;
     return cuda_status(launch_schedule(c, sps, n_sps, R, gamma, verify_len, theta, n_star, ws,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+size_t dspark_sts_workspace_size(int N, int gamma, int G, int M) {
+    if (N < 1 || N > (1 << 24) || gamma < 1 || gamma > 64 || G < 1 || G > 4096 || M < 1 || M > 32) return 0;
+    return sts_workspace_bytes(N, gamma, G, M);
+}
+
+int dspark_sts_fit(const float* c, const int32_t* accept_len, int N, int gamma, const double* grid, int G, int M,
+                   double* t_out, int32_t* g_out, double* ece_out, double* gap_out, void* ws, size_t ws_bytes,
+                   void* stream) {
+    if (N < 1 || N > (1 << 24) || gamma < 1 || gamma > 64 || G < 1 || G > 4096 || M < 1 || M > 32)
+        return DSPARK_ERR_SHAPE;
+    if (!c || !accept_len || !grid || !t_out || !g_out || !ece_out || !gap_out) return DSPARK_ERR_INVALID_ARG;
+    if (!ws || !aligned256(ws) || ws_bytes < sts_workspace_bytes(N, gamma, G, M)) return DSPARK_ERR_WORKSPACE;
+    return cuda_status(launch_sts_fit(c, accept_len, N, gamma, grid, G, M, t_out, g_out, ece_out, gap_out, ws,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_sts_apply(const float* c, int N, int gamma, const double* t, float* out, void* stream) {
+    if (N < 1 || gamma < 1 || gamma > 64 || (long long)N * gamma > (1ll << 31)) return DSPARK_ERR_SHAPE;
+    if (!c || !t || !out) return DSPARK_ERR_INVALID_ARG;
+    return cuda_status(launch_sts_apply(c, N, gamma, t, out, static_cast<cudaStream_t>(stream)));
 }
 
 int dspark_schedule_threshold(const float* c, int R, int gamma, float theta, int mode, int32_t* verify_len,

@@ -357,7 +357,8 @@ __device__ __forceinline__ void store_code(const DraftArgs& A, int r, int k, int
 }
 
 // Confidence head (blog section 4.1, ConfidenceHead) for request r at step k:
-// c_k = sigmoid(wc . [h_k, W1[x_{k-1}]]), no bias.  The block's threads take
+// c_k = sigmoid(wc . [h_k, W1[x_{k-1}]] / t_k), no bias, t_k = 1 unless
+// per-position temperatures (blog section 4.2) are given.  The block's threads take
 // strided shares of the d + r products (f32 FMAs; the h_k terms first, from
 // confidence_h_part), then the warps and the block add them in a fixed order.
 __device__ __forceinline__ float confidence_h_part(const DraftArgs& A, int r, int k) {
@@ -379,6 +380,7 @@ __device__ void confidence_head(const DraftArgs& A, int r, int k, int x, float t
     if (threadIdx.x == 0) {
         float u = 0.f;
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) u += s_part[w];
+        if (A.tc) u *= (float)(1.0 / A.tc[k - 1]);   // sequential temperature scaling of position k
         A.conf[(size_t)r * A.gamma + (k - 1)] = 1.f / (1.f + expf(-u));
     }
 }

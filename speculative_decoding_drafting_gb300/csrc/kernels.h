@@ -40,6 +40,7 @@ struct DraftArgs {
     const float* wc;          // [dc + r]
     int dc;
     float* conf;              // [R, gamma]
+    const double* tc;         // [gamma] per-position temperatures (STS), nullptr: none
     // workspace carve-up
     void* ws;
     DraftPartial* parts;      // [2][R][n_slices]
@@ -107,6 +108,11 @@ int verify_carve(VerifyArgs& a, size_t ws_bytes);
 cudaError_t launch_verify(VerifyArgs& a, cudaStream_t s);
 
 size_t schedule_smem_bytes(int R, int gamma);
+size_t sts_workspace_bytes(int N, int gamma, int G, int M);
+cudaError_t launch_sts_fit(const float* c, const int32_t* accept_len, int N, int gamma, const double* grid, int G,
+                           int M, double* t_out, int32_t* g_out, double* ece_out, double* gap_out, void* ws,
+                           cudaStream_t s);
+cudaError_t launch_sts_apply(const float* c, int N, int gamma, const double* t, float* out, cudaStream_t s);
 cudaError_t launch_schedule_threshold(const float* c, int R, int gamma, float theta, int mode, int32_t* len,
                                       cudaStream_t s);
 cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,

@@ -21,7 +21,8 @@ int g_open = -1;
 const char* const kNames[] = {"draft_prep",      "draft_sweep_generic", "draft_sweep_tc",   "verify_pass1",
                               "verify_accept",   "verify_residual_generic", "verify_residual_tc",
                               "verify_sample",   "schedule",            "draft_prep_rnn",   "draft_rnn_gru",
-                              "schedule_threshold"};
+                              "schedule_threshold", "sts_hist",           "sts_ece",          "sts_advance",
+                              "sts_apply",          "sts_fix"};
 
 cudaEvent_t take() {
     if (!g_pool.empty()) {

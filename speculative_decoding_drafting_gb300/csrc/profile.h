@@ -17,6 +17,11 @@ enum ProfName : int {
     kPDraftPrepRnn = 9,
     kPDraftRnnGru = 10,
     kPScheduleThreshold = 11,
+    kPStsHist = 12,
+    kPStsEce = 13,
+    kPStsAdvance = 14,
+    kPStsApply = 15,
+    kPStsFix = 16,
 };
 
 void prof_begin(int name, cudaStream_t s);

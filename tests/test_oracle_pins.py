@@ -463,6 +463,9 @@ def test_confidence_head_hand_worked_two_steps(storage):
         W1, H = _bf16_bits(W1), _bf16_bits(H)
     c = oracle.confidence(H, W1, w, np.array([0], np.int32), np.array([[1, 2]], np.int32))
     np.testing.assert_allclose(c[0], special.expit([13 / 8, -13 / 16]), rtol=0, atol=1e-15)
+    # with per-position temperatures (section 4.2): the logits divided by t_k
+    ct = oracle.confidence(H, W1, w, np.array([0], np.int32), np.array([[1, 2]], np.int32), temps=[2.0, 0.5])
+    np.testing.assert_allclose(ct[0], special.expit([13 / 16, -13 / 8]), rtol=0, atol=1e-15)
 
 
 def _conf_case(seed, R=6, gamma=4, V=50, d=24, r=8):
