@@ -15,7 +15,9 @@
 //               count), then lane b adds bin b over the 32 lanes.  p is formed
 //               in float32 (no double arithmetic on this path: GB300's FP64
 //               rate is a small fraction of its FP32 rate).  A value within
-//               the float error band of an interior bin edge is left out and
+//               twice its float error bound (tracked per sample and position
+//               from the ulp limits of logf, log1pf and expf) of an interior
+//               bin edge is left out and
 //               queued (sample, grid point): first in the CTA's shared memory,
 //               then copied to the workspace with one reservation per CTA.
 //   sts_fix     the queued values, one warp each: lane i forms position i's
@@ -24,10 +26,10 @@
 //               value is added to that bin's sums with integer atomics (exact,
 //               so the order does not matter).  Bin membership therefore never
 //               depends on float rounding.
-//   sts_ece     one CTA per 32 grid points: per (bin, grid point) the chunks'
-//               sums in a fixed order, the ECE in double; the last CTA to
-//               finish takes the smallest ECE (lowest grid index on ties) and
-//               the gap to the second smallest.
+//   sts_ece     one CTA per (32 grid points, bin): the chunks' sums in a fixed
+//               order, |sum y - sum p| in double; the last CTA to finish adds
+//               the bins of every grid point in order (the ECE) and takes the
+//               smallest (lowest grid index on ties) and the gap to the second.
 //   sts_advance the float32 prefix survival of every sample with the chosen
 //               temperature (the same expression sts_hist evaluated).
 #include <math.h>
@@ -40,9 +42,9 @@ namespace dspark {
 
 namespace {
 
-constexpr int kStsChunk = 2048;          // samples per CTA of sts_hist
+constexpr int kStsChunk = 1024;          // samples per CTA of sts_hist
 constexpr int kStsWarps = 8;             // grid points per CTA (one per warp)
-constexpr float kStsEdge = 1e-4f;        // bin-edge band (in bins) decided in double
+constexpr float kUlp = 1.1920929e-7f;    // 2^-23
 constexpr double kStsScale = 4294967296.0;
 constexpr int kStsLocalQ = 256;          // near-edge entries a CTA of sts_hist holds before flushing
 
@@ -57,9 +59,10 @@ struct StsArgs {
     double* ece_out;
     double* gap_out;
     float* a_prev;                 // [N] calibrated prefix survival of the positions before k (float32)
+    float* e_prev;                 // [N] bound on the relative error of a_prev against the double value
     unsigned long long* psum;      // [nchunk][M][G] sum of p, integers of 2^-32
     uint32_t* ysum;                // [nchunk][M][G] number of outcomes y = 1
-    double* ece;                   // [G] ECE of each grid point at the current position
+    double* ece;                   // [M][G] |sum y - sum p| of each bin and grid point at the current position
     unsigned int* done;            // CTAs of sts_ece finished (the last one resets it and qcount)
     unsigned int* qcount;          // entries appended to the near-edge queue at this position
     uint2* queue;                  // [qcap] (sample, grid point) of values near a bin edge
@@ -68,6 +71,24 @@ struct StsArgs {
 };
 
 __device__ __forceinline__ float logit_f(float c) { return logf(c) - log1pf(-c); }
+
+// logit in float32 and a bound on its absolute error: logf and log1pf are
+// within 1 ulp and the difference rounds once, so the error is below
+// 2.5 ulp of the largest of |ln c|, |ln(1 - c)| and |z|.
+__device__ __forceinline__ float logit_f_err(float c, float* dz) {
+    const float l0 = logf(c), l1 = log1pf(-c);
+    const float z = l0 - l1;
+    *dz = 2.5f * kUlp * fmaxf(fmaxf(fabsf(l0), fabsf(l1)), fabsf(z));
+    return z;
+}
+
+// Bound on the relative error of the float32 tempered confidence
+// 1 / (1 + expf(x)), x = -z inv_t, against the double value: the error of x
+// (from z and the two roundings of the product) moves the result by (1 - s)
+// times it, expf adds 2 ulp and the sum and the division one rounding each.
+__device__ __forceinline__ float tempered_rel_err(float x, float s, float dz, float inv_t) {
+    return (1.f - s) * (dz * inv_t + fabsf(x) * kUlp + 2.f * kUlp) + kUlp;
+}
 __device__ __forceinline__ double logit_d(float c) {
     const double cd = (double)c;
     return log(cd) - log1p(-cd);
@@ -86,7 +107,7 @@ __device__ __forceinline__ unsigned long long fixed32(float p) {
 // The calibrated prefix survival of sample n through position k in double,
 // as the oracle forms it: a = 1, then a *= sigmoid(logit(c_i) / t_i) for
 // i = 1 .. k with t_i the chosen temperatures and t_k = tk.
-__device__ double survival_exact(const StsArgs& A, int n, int k, double tk) {
+__device__ __noinline__ double survival_exact(const StsArgs& A, int n, int k, double tk) {
     double a = 1.0;
     for (int i = 1; i <= k; ++i) {
         const double t = i < k ? A.t_out[i - 1] : tk;
@@ -97,25 +118,27 @@ __device__ double survival_exact(const StsArgs& A, int n, int k, double tk) {
 
 // One warp of sts_hist: grid point g over the chunk's samples.
 __device__ __forceinline__ void hist_warp(const StsArgs& A, int k, int g, int n0, int nn, unsigned long long* lp,
-                                          uint32_t* ly, const float* sa, const float* sz, const unsigned char* sy,
-                                          uint2* s_q, unsigned int* s_nq) {
+                                          uint32_t* ly, const float* sa, const float* sz, const float* sdz,
+                                          const float* se, const unsigned char* sy, uint2* s_q, unsigned int* s_nq) {
     const int M = A.M;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const double tg = A.grid[g];
     const float inv_t = (float)(1.0 / tg);
     const float fM = (float)M;
-    // float error of p relative to the double value: a few ulp per position
-    const float rel_err = 4e-7f * (float)k;
     unsigned long long* mp = lp + (size_t)warp * M * 32 + lane;
     uint32_t* my = ly + (size_t)warp * M * 32 + lane;
     for (int i = lane; i < nn; i += 32) {
-        const float p = sa[i] * (1.f / (1.f + expf(-sz[i] * inv_t)));
+        const float x = -sz[i] * inv_t;
+        const float sg = 1.f / (1.f + expf(x));
+        const float p = sa[i] * sg;
         const float q = p * fM;
-        // only the interior edges 1 .. M-1 separate bins (0 and M are clamped)
+        // only the interior edges 1 .. M-1 separate bins (0 and M are clamped);
+        // a value whose error bound (doubled) reaches an edge is decided in double
         const float edge = rintf(q);
         int b;
         unsigned long long pi;
-        if (edge >= 1.f && edge <= fM - 1.f && fabsf(q - edge) < kStsEdge + q * rel_err) {
+        if (edge >= 1.f && edge <= fM - 1.f &&
+            fabsf(q - edge) < 2.f * q * (se[i] + tempered_rel_err(x, sg, sdz[i], inv_t) + kUlp)) {
             // near a bin edge: the oracle's double arithmetic decides, in
             // sts_fix; here only when the CTA's queue is full
             const unsigned int slot = atomicAdd(s_nq, 1u);
@@ -159,7 +182,9 @@ __global__ void __launch_bounds__(256) sts_hist(StsArgs A, int k) {
     uint32_t* ly = reinterpret_cast<uint32_t*>(lp + kStsWarps * M * 32);  // [warp][M][32]
     float* sa = reinterpret_cast<float*>(ly + kStsWarps * M * 32);        // [chunk] a_prev
     float* sz = sa + kStsChunk;                                            // [chunk] logit of c_k
-    unsigned char* sy = reinterpret_cast<unsigned char*>(sz + kStsChunk); // [chunk] outcome
+    float* sdz = sz + kStsChunk;                                           // [chunk] its error bound
+    float* se = sdz + kStsChunk;                                           // [chunk] a_prev's relative error bound
+    unsigned char* sy = reinterpret_cast<unsigned char*>(se + kStsChunk); // [chunk] outcome
     __shared__ uint2 s_q[kStsLocalQ];
     __shared__ unsigned int s_nq, s_base;
     if (threadIdx.x == 0) s_nq = 0u;
@@ -167,8 +192,11 @@ __global__ void __launch_bounds__(256) sts_hist(StsArgs A, int k) {
     const int nn = min(kStsChunk, A.N - n0);
     for (int i = threadIdx.x; i < nn; i += blockDim.x) {
         const int n = n0 + i;
-        sz[i] = logit_f(A.c[(size_t)n * A.gamma + (k - 1)]);
+        float dz;
+        sz[i] = logit_f_err(A.c[(size_t)n * A.gamma + (k - 1)], &dz);
+        sdz[i] = dz;
         sa[i] = k > 1 ? A.a_prev[n] : 1.f;
+        se[i] = k > 1 ? A.e_prev[n] : 0.f;
         sy[i] = A.accept_len[n] >= k ? 1 : 0;
     }
     for (int i = threadIdx.x; i < kStsWarps * M * 32; i += blockDim.x) {
@@ -178,7 +206,7 @@ __global__ void __launch_bounds__(256) sts_hist(StsArgs A, int k) {
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y * kStsWarps + warp;
-    if (g < A.G) hist_warp(A, k, g, n0, nn, lp, ly, sa, sz, sy, s_q, &s_nq);
+    if (g < A.G) hist_warp(A, k, g, n0, nn, lp, ly, sa, sz, sdz, se, sy, s_q, &s_nq);
     // the CTA's queued entries go to the workspace queue (one reservation)
     __syncthreads();
     const unsigned int nq = min(s_nq, (unsigned int)kStsLocalQ);
@@ -246,41 +274,57 @@ __device__ __forceinline__ Best merge(Best x, Best y) {
     return r;
 }
 
-// One CTA per 32 grid points, thread (b, j) = bin b of grid point 32 blockIdx + j.
+// One CTA per (32 grid points, bin b = blockIdx.y): thread (l, j) adds the
+// chunks l, l + 32, ... of grid point 32 blockIdx.x + j, then the 32 partial
+// sums of each grid point are added in order and |sum y - sum p| is stored.
+// The last CTA to finish forms every grid point's ECE (bins in order) and
+// picks the temperature.
 __global__ void __launch_bounds__(1024) sts_ece(StsArgs A, int k) {
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ double s_bin[32][33];
+    __shared__ unsigned long long s_p[32][33];
+    __shared__ unsigned int s_y[32][33];
     __shared__ Best s_w[32];
     __shared__ bool s_last;
-    const int M = A.M;
-    const int j = threadIdx.x & 31, b = threadIdx.x >> 5;
+    const int M = A.M, b = blockIdx.y;
+    const int j = threadIdx.x & 31, l = threadIdx.x >> 5;
     const int g = blockIdx.x * 32 + j;
-    if (b < M && g < A.G) {
-        unsigned long long sp = 0ull, sy = 0ull;
-        for (int ch = 0; ch < A.nchunk; ++ch) {
+    unsigned long long sp = 0ull;
+    unsigned int sy = 0u;
+    if (g < A.G) {
+#pragma unroll 4
+        for (int ch = l; ch < A.nchunk; ch += 32) {
             const size_t o = ((size_t)ch * M + b) * A.G + g;
             sp += A.psum[o];
             sy += A.ysum[o];
         }
-        s_bin[b][j] = fabs((double)sy - (double)sp / kStsScale);
     }
+    s_p[l][j] = sp;
+    s_y[l][j] = sy;
     __syncthreads();
-    if (threadIdx.x < 32 && g < A.G) {
-        double e = 0.0;
-        for (int bb = 0; bb < M; ++bb) e += s_bin[bb][j];
-        A.ece[g] = e / (double)A.N;
+    if (l == 0 && g < A.G) {
+        unsigned long long tp = 0ull;
+        unsigned int ty = 0u;
+        for (int ll = 0; ll < 32; ++ll) {
+            tp += s_p[ll][j];
+            ty += s_y[ll][j];
+        }
+        A.ece[(size_t)b * A.G + g] = fabs((double)ty - (double)tp / kStsScale);
     }
     // the last CTA to finish picks the temperature
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(A.done, 1u) == gridDim.x - 1;
+    if (threadIdx.x == 0) s_last = atomicAdd(A.done, 1u) == gridDim.x * gridDim.y - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     Best mine{INFINITY, INT_MAX, INFINITY};
-    const volatile double* ece = A.ece;
-    for (int gg = threadIdx.x; gg < A.G; gg += blockDim.x) mine = merge(mine, Best{ece[gg], gg, INFINITY});
+    const volatile double* eb = A.ece;
+    for (int gg = threadIdx.x; gg < A.G; gg += blockDim.x) {
+        double e = 0.0;
+        for (int bb = 0; bb < M; ++bb) e += eb[(size_t)bb * A.G + gg];
+        mine = merge(mine, Best{e / (double)A.N, gg, INFINITY});
+    }
     for (int o = 16; o > 0; o >>= 1) {
         Best other;
         other.b = __shfl_xor_sync(0xffffffffu, mine.b, o);
@@ -309,7 +353,12 @@ __global__ void __launch_bounds__(256) sts_advance(StsArgs A, int k) {
     if (n >= A.N) return;
     const float inv_t = (float)(1.0 / A.t_out[k - 1]);
     const float a = k > 1 ? A.a_prev[n] : 1.f;
-    A.a_prev[n] = a * (1.f / (1.f + expf(-logit_f(A.c[(size_t)n * A.gamma + (k - 1)]) * inv_t)));
+    const float e = k > 1 ? A.e_prev[n] : 0.f;
+    float dz;
+    const float x = -logit_f_err(A.c[(size_t)n * A.gamma + (k - 1)], &dz) * inv_t;
+    const float sg = 1.f / (1.f + expf(x));
+    A.a_prev[n] = a * sg;
+    A.e_prev[n] = e + tempered_rel_err(x, sg, dz, inv_t) + kUlp;
 }
 
 // c_out = sigmoid(logit(c) / t_k), float32.
@@ -330,7 +379,7 @@ unsigned int sts_queue_cap(int N, int G) {
 }
 
 size_t hist_smem(int M) {
-    return (size_t)kStsWarps * M * 32 * (8 + 4) + (size_t)kStsChunk * (4 + 4 + 1);
+    return (size_t)kStsWarps * M * 32 * (8 + 4) + (size_t)kStsChunk * (4 + 4 + 4 + 4 + 1);
 }
 
 }  // namespace
@@ -342,7 +391,8 @@ size_t sts_workspace_bytes(int N, int gamma, int G, int M) {
     off = align_up(off + 256, 256);                                          // done, qcount
     off = align_up(off + (size_t)sts_queue_cap(N, G) * sizeof(uint2), 256);  // near-edge queue
     off = align_up(off + (size_t)N * sizeof(float), 256);                    // a_prev
-    off = align_up(off + (size_t)G * sizeof(double), 256);                   // ece
+    off = align_up(off + (size_t)N * sizeof(float), 256);                    // e_prev
+    off = align_up(off + (size_t)M * G * sizeof(double), 256);               // ece per bin
     off = align_up(off + nchunk * M * G * sizeof(unsigned long long), 256);  // psum
     off = align_up(off + nchunk * M * G * sizeof(uint32_t), 256);            // ysum
     return off;
@@ -374,8 +424,10 @@ cudaError_t launch_sts_fit(const float* c, const int32_t* accept_len, int N, int
     off = align_up(off + (size_t)A.qcap * sizeof(uint2), 256);
     A.a_prev = reinterpret_cast<float*>(base + off);
     off = align_up(off + (size_t)N * sizeof(float), 256);
+    A.e_prev = reinterpret_cast<float*>(base + off);
+    off = align_up(off + (size_t)N * sizeof(float), 256);
     A.ece = reinterpret_cast<double*>(base + off);
-    off = align_up(off + (size_t)G * sizeof(double), 256);
+    off = align_up(off + (size_t)M * G * sizeof(double), 256);
     A.psum = reinterpret_cast<unsigned long long*>(base + off);
     off = align_up(off + (size_t)A.nchunk * M * G * sizeof(unsigned long long), 256);
     A.ysum = reinterpret_cast<uint32_t*>(base + off);
@@ -395,7 +447,7 @@ cudaError_t launch_sts_fit(const float* c, const int32_t* accept_len, int N, int
         prof_end(s);
         if (e != cudaSuccess) return e;
         prof_begin(kPStsEce, s);
-        e = launch_kernel(sts_ece, dim3((G + 31) / 32), dim3(32 * M), 0, s, true, A, k);
+        e = launch_kernel(sts_ece, dim3((G + 31) / 32, M), dim3(1024), 0, s, true, A, k);
         prof_end(s);
         if (e != cudaSuccess) return e;
         if (k < gamma) {
