@@ -431,16 +431,35 @@ __global__ void __launch_bounds__(kPrepThreads) draft_prep_rnn(DraftArgs A, int 
         return;
     }
     if (threadIdx.x == 0) A.best[r] = kOrderNegInf;
-    const int Kin = 2 * rr + A.d, ldz = gru_ldz(rr, A.d);
-    float* z = A.zbuf + (size_t)r * ldz;
-    for (int i = threadIdx.x; i < rr; i += blockDim.x) {
-        z[i] = (k == 1) ? 0.f : srow[i];
-        z[rr + i] = ld_elem(A.W1, A.w_dtype, (size_t)x * rr + i);
+    const unsigned short* Hb = static_cast<const unsigned short*>(A.H) + ((size_t)r * A.gamma + (k - 1)) * A.d;
+    if (A.gru_tc) {
+        // bf16 row [s_hi | s_mid | s_lo | W1[x] | h | 0] for the tensor-core GRU
+        // (the three terms of s add up to s exactly; W1 and h are bf16 already)
+        const int ldzb = gru_ldzb(rr, A.d);
+        uint16_t* zr = A.zb + (size_t)r * ldzb;
+        const uint16_t* w1 = static_cast<const uint16_t*>(A.W1) + (size_t)x * rr;
+        for (int i = threadIdx.x; i < rr; i += blockDim.x) {
+            const float sv = (k == 1) ? 0.f : srow[i];
+            const uint16_t hi = f32_to_bf16_bits_rn(sv);
+            const float rest = sv - bf16_bits_to_float(hi);
+            const uint16_t mid = f32_to_bf16_bits_rn(rest);
+            zr[i] = hi;
+            zr[rr + i] = mid;
+            zr[2 * rr + i] = f32_to_bf16_bits_rn(rest - bf16_bits_to_float(mid));
+            zr[3 * rr + i] = w1[i];
+        }
+        for (int i = threadIdx.x; i < A.d; i += blockDim.x) zr[4 * rr + i] = Hb[i];
+        for (int i = 4 * rr + A.d + threadIdx.x; i < ldzb; i += blockDim.x) zr[i] = 0;
+    } else {
+        const int Kin = 2 * rr + A.d, ldz = gru_ldz(rr, A.d);
+        float* z = A.zbuf + (size_t)r * ldz;
+        for (int i = threadIdx.x; i < rr; i += blockDim.x) {
+            z[i] = (k == 1) ? 0.f : srow[i];
+            z[rr + i] = ld_elem(A.W1, A.w_dtype, (size_t)x * rr + i);
+        }
+        for (int i = threadIdx.x; i < A.d; i += blockDim.x) z[2 * rr + i] = bf16_bits_to_float(Hb[i]);
+        for (int i = Kin + threadIdx.x; i < ldz; i += blockDim.x) z[i] = 0.f;
     }
-    const unsigned short* Hb = static_cast<const unsigned short*>(A.H);
-    for (int i = threadIdx.x; i < A.d; i += blockDim.x)
-        z[2 * rr + i] = bf16_bits_to_float(Hb[((size_t)r * A.gamma + (k - 1)) * A.d + i]);
-    for (int i = Kin + threadIdx.x; i < ldz; i += blockDim.x) z[i] = 0.f;
     if (A.conf) confidence_head(A, r, k, x, th);
 }
 
@@ -555,6 +574,30 @@ __global__ void __launch_bounds__(256) rnn_gru(DraftArgs A, int k) {
         A.rnn_state[(size_t)row * rr + j] = sg * sprev + (1.f - sg) * tanhf(acc[1][q]);
         store_code(A, row, k, j, tanhf(acc[2][q]));
     }
+}
+
+// The end of the tensor-core GRU step (gru_tc.cu computes G in K parts):
+// one thread per (request, j) adds the parts in order and applies the update
+//   s_k = sigmoid(gate) s_{k-1} + (1 - sigmoid(gate)) tanh(cand),  e_k = tanh(out).
+__global__ void __launch_bounds__(256) gru_finish(DraftArgs A, int k) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int rr = A.r;
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)A.R * rr) return;
+    const int row = (int)(idx / rr), j = (int)(idx % rr);
+    float gate = 0.f, cand = 0.f, out = 0.f;
+    for (int s = 0; s < A.gru_parts; ++s) {
+        const float* gp = A.gpart + ((size_t)s * A.R + row) * 3 * rr;
+        gate += gp[j];
+        cand += gp[rr + j];
+        out += gp[2 * rr + j];
+    }
+    const float sg = 1.f / (1.f + expf(-gate));
+    float* srow = A.rnn_state + (size_t)row * rr;
+    const float sprev = k == 1 ? 0.f : srow[j];
+    srow[j] = sg * sprev + (1.f - sg) * tanhf(cand);
+    store_code(A, row, k, j, tanhf(out));
 }
 
 // ------------------------------------------------------------------ generic sweep
@@ -681,6 +724,10 @@ size_t draft_workspace_bytes(int R, int gamma, int V, int r, int d) {
     size_t off = sizeof(WsHeader);
     off = align_up(off + 2ull * R * ns_max * sizeof(DraftPartial), 256);
     off = align_up(off + (size_t)R * gru_ldz(r, d) * sizeof(float), 256);   // GRU input z (RNN head)
+    if (d > 0) {
+        off = align_up(off + (size_t)R * gru_ldzb(r, d) * sizeof(uint16_t), 256);               // bf16 z
+        off = align_up(off + (size_t)gru_tc_parts(R, r, d) * R * 3 * r * sizeof(float), 256);  // partial G
+    }
     off = align_up(off + 3ull * R * r * sizeof(uint16_t), 256);
     off = align_up(off + (size_t)R * r * sizeof(float), 256);
     off = align_up(off + (size_t)R * sizeof(uint32_t), 256);
@@ -700,6 +747,16 @@ int draft_carve(DraftArgs& a, size_t ws_bytes) {
     off = align_up(off + 2ull * a.R * ns_max * sizeof(DraftPartial), 256);
     a.zbuf = reinterpret_cast<float*>(base + off);
     off = align_up(off + (size_t)a.R * gru_ldz(a.r, a.d) * sizeof(float), 256);
+    a.zb = nullptr;
+    a.gpart = nullptr;
+    a.gru_parts = 0;
+    if (a.d > 0) {
+        a.zb = reinterpret_cast<uint16_t*>(base + off);
+        off = align_up(off + (size_t)a.R * gru_ldzb(a.r, a.d) * sizeof(uint16_t), 256);
+        a.gpart = reinterpret_cast<float*>(base + off);
+        a.gru_parts = gru_tc_parts(a.R, a.r, a.d);
+        off = align_up(off + (size_t)a.gru_parts * a.R * 3 * a.r * sizeof(float), 256);
+    }
     a.ebf = reinterpret_cast<uint16_t*>(base + off);
     off = align_up(off + 3ull * a.R * a.r * sizeof(uint16_t), 256);
     a.rnn_state = reinterpret_cast<float*>(base + off);
@@ -739,6 +796,7 @@ static cudaError_t launch_sweep(DraftArgs& a, int k, bool use_tc, cudaStream_t s
 
 cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
     a.rnn = rnn ? 1 : 0;
+    a.gru_tc = (rnn && gru_tc_supported(a)) ? 1 : 0;
     const bool use_tc = draft_tc_supported(a);
     a.n_slices = use_tc ? draft_tc_slices(a) : (a.V + kGenericSlice - 1) / kGenericSlice;
     void (*prep_m)(DraftArgs, int);
@@ -761,8 +819,17 @@ cudaError_t launch_draft(DraftArgs& a, bool rnn, cudaStream_t s) {
             e = launch_kernel(prep_r, dim3(a.R), dim3(kPrepThreads), 0, s, k > 1, a, k);
             prof_end(s);
             if (e == cudaSuccess && k <= a.gamma) {
-                prof_begin(kPDraftRnnGru, s);
-                e = launch_kernel(gru, gru_grid, dim3(256), 0, s, true, a, k);
+                if (a.gru_tc) {
+                    e = launch_gru_tc(a, k, s);
+                    if (e == cudaSuccess) {
+                        const size_t n = (size_t)a.R * a.r;
+                        prof_begin(kPDraftRnnGruFinish, s);
+                        e = launch_kernel(gru_finish, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, true, a, k);
+                    }
+                } else {
+                    prof_begin(kPDraftRnnGru, s);
+                    e = launch_kernel(gru, gru_grid, dim3(256), 0, s, true, a, k);
+                }
             }
         } else {
             prof_begin(kPDraftPrep, s);

@@ -46,7 +46,11 @@ struct DraftArgs {
     DraftPartial* parts;      // [2][R][n_slices]
     uint16_t* ebf;            // [3][R][r] bf16 bits of e_k = hi + mid + lo (exact for f32 e_k)
     float* rnn_state;         // [R][r]
-    float* zbuf;              // RNN head: [R][2r + d] GRU input z of the current step
+    float* zbuf;              // RNN head: [R][2r + d] GRU input z of the current step (CUDA-core GRU)
+    uint16_t* zb;             // RNN head: [R][ldzb] bf16 z = [s_hi | s_mid | s_lo | W1[x] | h | 0] (tensor-core GRU)
+    float* gpart;             // RNN head: [parts][R][3r] partial G of the K parts (tensor-core GRU)
+    int gru_tc;               // 1: the GRU step runs on the tensor cores
+    int gru_parts;            // K parts of the tensor-core GRU
     uint32_t* best;           // [R] best race key of the current step (order-preserving bits)
     float2* cmass;            // [R][nchunk][4] (reference m, sum 2^(y - m)) per 256-column chunk
     int nchunk;               // ceil(V / 256)
@@ -119,6 +123,13 @@ cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R,
                             double* theta, int32_t* nstar, void* ws, cudaStream_t s);
 
 int num_sms();
+
+// Row length of the tensor-core GRU's bf16 input [s_hi | s_mid | s_lo | W1[x] | h]
+// (4r + d values) rounded up to a whole 64-value K block.
+__host__ __device__ inline int gru_ldzb(int r, int d) { return (4 * r + d + 63) / 64 * 64; }
+int gru_tc_parts(int R, int r, int d);
+bool gru_tc_supported(const DraftArgs& a);
+cudaError_t launch_gru_tc(DraftArgs& a, int k, cudaStream_t s);
 
 // Launch `kern` on `s`.  With `pdl` set the launch may begin while the
 // previous kernel in the stream is still running (programmatic dependent

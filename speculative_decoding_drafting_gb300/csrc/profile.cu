@@ -22,7 +22,8 @@ const char* const kNames[] = {"draft_prep",      "draft_sweep_generic", "draft_s
                               "verify_accept",   "verify_residual_generic", "verify_residual_tc",
                               "verify_sample",   "schedule",            "draft_prep_rnn",   "draft_rnn_gru",
                               "schedule_threshold", "sts_hist",           "sts_ece",          "sts_advance",
-                              "sts_apply",          "sts_fix"};
+                              "sts_apply",          "sts_fix",
+                              "draft_rnn_gru_finish"};
 
 cudaEvent_t take() {
     if (!g_pool.empty()) {

@@ -22,6 +22,7 @@ enum ProfName : int {
     kPStsAdvance = 14,
     kPStsApply = 15,
     kPStsFix = 16,
+    kPDraftRnnGruFinish = 17,
 };
 
 void prof_begin(int name, cudaStream_t s);
