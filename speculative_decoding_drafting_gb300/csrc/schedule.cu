@@ -30,6 +30,12 @@
 namespace dspark {
 
 constexpr int kSchedThreads = 1024;
+
+// Key p lives at p + p / 8 in shared memory: one spare slot per eight keys,
+// so the eight consecutive keys of a sorting thread start 72 bytes after its
+// neighbour's and a warp's register <-> shared transfers do not pile onto two
+// banks.
+__host__ __device__ __forceinline__ int kslot(int p) { return p + (p >> 3); }
 constexpr int kSchedMaxPer = 8;    // candidates per thread at the largest batch (R gamma <= 8192)
 
 __device__ __forceinline__ double sps_at(const double* sps, int n_sps, long long B) {
@@ -75,13 +81,13 @@ __device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
     unsigned long long k[8];
     // positions past Np (Np < 8) are padding: they only ever meet each other
 #pragma unroll
-    for (int e = 0; e < 8; ++e) k[e] = (live && 8 * t + e < Np) ? keys[8 * t + e] : ~0ull;
+    for (int e = 0; e < 8; ++e) k[e] = (live && 8 * t + e < Np) ? keys[kslot(8 * t + e)] : ~0ull;
     for (int size = 2; size <= Np; size <<= 1) {
         int stride = size >> 1;
         if (stride >= 256) {
             if (live)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) keys[8 * t + e] = k[e];
+                for (int e = 0; e < 8; ++e) keys[kslot(8 * t + e)] = k[e];
             __syncthreads();
             for (; stride >= 256; stride >>= 1) {
                 const int ls = __ffs(stride) - 1;
@@ -89,17 +95,17 @@ __device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
                     const int lo = ((i >> ls) << (ls + 1)) | (i & (stride - 1));
                     const int hi = lo + stride;
                     const bool upp = (lo & size) == 0;
-                    const unsigned long long a = keys[lo], b = keys[hi];
+                    const unsigned long long a = keys[kslot(lo)], b = keys[kslot(hi)];
                     if ((a > b) == upp) {
-                        keys[lo] = b;
-                        keys[hi] = a;
+                        keys[kslot(lo)] = b;
+                        keys[kslot(hi)] = a;
                     }
                 }
                 __syncthreads();
             }
             if (live)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) k[e] = keys[8 * t + e];
+                for (int e = 0; e < 8; ++e) k[e] = keys[kslot(8 * t + e)];
         }
         if (active) {
             for (; stride >= 8; stride >>= 1) {
@@ -118,7 +124,7 @@ __device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
     if (live)
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            if (8 * t + e < Np) keys[8 * t + e] = k[e];
+            if (8 * t + e < Np) keys[kslot(8 * t + e)] = k[e];
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c, const double* sps, int n_sps,
@@ -127,9 +133,11 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     pdl_launch_dependents();
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
-    double* val = reinterpret_cast<double*>(smem + (size_t)Np * 8);
-    int* cnt = reinterpret_cast<int*>(smem + (size_t)Np * 16);
+    const int Nk = kslot(Np);                       // key slots
+    double* val = reinterpret_cast<double*>(smem + (size_t)Nk * 8);
+    int* cnt = reinterpret_cast<int*>(smem + (size_t)Nk * 8 + (size_t)Np * 8);
     __shared__ double wsum[kSchedThreads / 32];
+    __shared__ int s_wfirst[kSchedThreads / 32];
     __shared__ int s_nvalid, s_nstar;
     const int tid = threadIdx.x;
     const int N = R * gamma;
@@ -156,12 +164,12 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
         for (int j = 0; j < gamma; ++j) {
             const int idx = r * gamma + j;
             prod = __fmul_rn(prod, c_sh[idx]);
-            keys[idx] = (prod > 0.0f) ? (((unsigned long long)(~__float_as_uint(prod)) << 32) | (unsigned)idx)
-                                      : ~0ull;
+            keys[kslot(idx)] = (prod > 0.0f) ? (((unsigned long long)(~__float_as_uint(prod)) << 32) | (unsigned)idx)
+                                             : ~0ull;
         }
         cnt[r] = 0;
     }
-    for (int i = N + tid; i < Np; i += blockDim.x) keys[i] = ~0ull;
+    for (int i = N + tid; i < Np; i += blockDim.x) keys[kslot(i)] = ~0ull;
     __syncthreads();
     if (Np <= 8 * kSortThreads) {
         bitonic_sort_regs(keys, Np);
@@ -174,10 +182,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
                 const int lo = ((i >> lst) << (lst + 1)) | (i & (stride - 1));
                 const int hi = lo + stride;
                 const bool up = ((lo & size) == 0);
-                const unsigned long long a = keys[lo], b = keys[hi];
+                const unsigned long long a = keys[kslot(lo)], b = keys[kslot(hi)];
                 if ((a > b) == up) {
-                    keys[lo] = b;
-                    keys[hi] = a;
+                    keys[kslot(lo)] = b;
+                    keys[kslot(hi)] = a;
                 }
             }
             // the next pass: stride / 2 within this size, else the next size's first
@@ -194,19 +202,17 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     const int per = (Np + blockDim.x - 1) / blockDim.x;
     const int b0 = tid * per;
     double run = 0.0;
-    int nv = 0;
     for (int i = b0; i < b0 + per && i < Np; ++i) {
-        const unsigned long long k = keys[i];
+        const unsigned long long k = keys[kslot(i)];
         double a = 0.0;
         if (k != ~0ull) {
             a = (double)__uint_as_float(~(unsigned)(k >> 32));
-            ++nv;
+            // the valid candidates sort first: the last valid one gives their count
+            if (i + 1 == Np || keys[kslot(i + 1)] == ~0ull) s_nvalid = i + 1;
         }
         run += a;
         val[i] = run;
     }
-    nv = __reduce_add_sync(0xffffffffu, (unsigned)nv);
-    if ((tid & 31) == 0) atomicAdd(&s_nvalid, nv);
     // block exclusive scan of the per-thread totals
     const int lane = tid & 31, warp = tid >> 5;
     double x = run;
@@ -248,12 +254,18 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
         }
     }
     first = (int)__reduce_min_sync(0xffffffffu, (unsigned)first);
-    if ((tid & 31) == 0 && first != INT_MAX) atomicMin(&s_nstar, first);
+    if ((tid & 31) == 0) s_wfirst[tid >> 5] = first;
+    __syncthreads();
+    if (tid < 32) {
+        int f = tid < (int)(blockDim.x >> 5) ? s_wfirst[tid] : INT_MAX;
+        f = (int)__reduce_min_sync(0xffffffffu, (unsigned)f);
+        if (tid == 0) s_nstar = f;
+    }
     __syncthreads();
     const int ns = s_nstar == INT_MAX ? nvalid : s_nstar;
     // 5: lengths
     for (int i = tid; i < ns; i += blockDim.x) {
-        const int idx = (int)(unsigned)(keys[i] & 0xFFFFFFFFull);
+        const int idx = (int)(unsigned)(keys[kslot(i)] & 0xFFFFFFFFull);
         atomicAdd(&cnt[idx / gamma], 1);
     }
     __syncthreads();
@@ -273,7 +285,7 @@ static int next_pow2(int n) {
 
 size_t schedule_smem_bytes(int R, int gamma) {
     const int Np = next_pow2(R * gamma < 2 ? 2 : R * gamma);
-    return (size_t)Np * 16 + (size_t)R * sizeof(int);
+    return (size_t)kslot(Np) * 8 + (size_t)Np * 8 + (size_t)R * sizeof(int);
 }
 
 cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,
