@@ -93,3 +93,24 @@ def test_confidence_head_and_threshold_arguments_rejected_on_the_host():
     assert L.dspark_schedule_threshold(fake, 4, 65, ctypes.c_float(0.5), 0, fake, null) == -3
     assert L.dspark_schedule_threshold(fake, 0, 5, ctypes.c_float(0.5), 0, fake, null) == -3
     assert L.dspark_schedule_threshold(null, 4, 5, ctypes.c_float(0.5), 0, fake, null) == -1
+
+
+def test_sts_arguments_rejected_on_the_host():
+    L = binding.load()
+    null = None
+    fake = ctypes.c_void_p(4096)   # never dereferenced: every call below fails its host checks
+    assert L.dspark_sts_workspace_size(65536, 8, 256, 15) > 0
+    for bad in [(0, 8, 256, 15), (10, 0, 256, 15), (10, 65, 256, 15), (10, 8, 0, 15), (10, 8, 4097, 15),
+                (10, 8, 256, 0), (10, 8, 256, 33), ((1 << 24) + 1, 8, 256, 15)]:
+        assert L.dspark_sts_workspace_size(*bad) == 0
+    fit = lambda c, al, N, g, grid, G, M, out, ws, wsb: L.dspark_sts_fit(  # noqa: E731
+        c, al, N, g, grid, G, M, out, out, out, out, ws, wsb, null)
+    assert fit(fake, fake, 10, 8, fake, 256, 33, fake, fake, 1 << 20) == -3
+    assert fit(null, fake, 10, 8, fake, 256, 15, fake, fake, 1 << 20) == -1
+    assert fit(fake, fake, 10, 8, fake, 256, 15, null, fake, 1 << 20) == -1
+    assert fit(fake, fake, 10, 8, fake, 256, 15, fake, null, 1 << 20) == -8
+    assert fit(fake, fake, 10, 8, fake, 256, 15, fake, ctypes.c_void_p(4096 + 8), 1 << 20) == -8   # misaligned
+    assert fit(fake, fake, 10, 8, fake, 256, 15, fake, fake, 64) == -8                            # too small
+    assert L.dspark_sts_apply(fake, 0, 8, fake, fake, null) == -3
+    assert L.dspark_sts_apply(fake, 10, 65, fake, fake, null) == -3
+    assert L.dspark_sts_apply(null, 10, 8, fake, fake, null) == -1
