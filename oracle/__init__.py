@@ -83,6 +83,8 @@ def lib():
             L.oracle_schedule_loop.restype = i32
             L.oracle_schedule_closed.argtypes = [P, P, i32, i32, i32, P, P, P]
             L.oracle_schedule_closed.restype = i32
+            L.oracle_schedule_budget.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
+            L.oracle_schedule_budget.restype = i32
             _lib = L
     return _lib
 
@@ -313,3 +315,20 @@ def sts_apply(c, t):
     out = np.zeros(c.shape)
     lib().oracle_sts_apply(_ptr(c), c.shape[0], c.shape[1], _ptr(t), _ptr(out))
     return out
+
+
+def schedule_budget(c, sps, budget: int):
+    """Production-style scheduler: the capacity (budget) decided two steps
+    back, the current candidates ranked into it.  Returns (lengths, theta,
+    places filled, this step's synchronous n*)."""
+    c = _c(c, np.float32)
+    sps = _c(sps, np.float64)
+    R, gamma = c.shape
+    L = np.zeros(R, np.int32)
+    th = np.zeros(1)
+    ns = np.zeros(1, np.int32)
+    n = lib().oracle_schedule_budget(_ptr(c), _ptr(sps), int(sps.size), R, gamma, int(budget), _ptr(L), _ptr(th),
+                                     _ptr(ns))
+    if n < 0:
+        raise RuntimeError("oracle_schedule_budget failed")
+    return L, float(th[0]), int(n), int(ns[0])

@@ -665,6 +665,35 @@ int oracle_schedule_closed(const float* c, const double* sps, int n_sps, int R, 
     return nstar;
 }
 
+/* Production-style scheduler (explainer section 04): the capacity comes
+ * from the prediction made two steps back, and the current candidates are
+ * ranked into it.  Reading: budget = the n* the synchronous rule gave two
+ * steps earlier (negative: none yet, use this step's n*); the current
+ * candidates, in the order of the synchronous scheduler, fill min(budget,
+ * count) places; theta = tau * SPS at that batch.  *n_star receives this
+ * step's own synchronous n*, the capacity for two steps later.  Returns the
+ * number of places filled. */
+int oracle_schedule_budget(const float* c, const double* sps, int n_sps, int R, int gamma, int budget,
+                           int32_t* lengths, double* theta, int32_t* n_star) {
+    int n;
+    cand_t* cand = sorted_candidates(c, R, gamma, &n);
+    if (!cand) return -1;
+    double th_sync;
+    const int ns = oracle_schedule_closed(c, sps, n_sps, R, gamma, lengths, &th_sync, NULL);
+    if (ns < 0) { free(cand); return -1; }
+    *n_star = ns;
+    const int nb = budget < 0 ? ns : (budget < n ? budget : n);
+    double tau = (double)R;
+    for (int ri = 0; ri < R; ++ri) lengths[ri] = 0;
+    for (int i = 0; i < nb; ++i) {
+        lengths[cand[i].r] += 1;
+        tau += (double)cand[i].a;
+    }
+    *theta = tau * sps_at(sps, n_sps, (long)R + nb);
+    free(cand);
+    return nb;
+}
+
 /* Threshold filter (blog section 4.3, the confidence-threshold sweep; the
  * explainer's section 04 contrasts it with the scheduler): every request
  * verifies its longest prefix whose confidence clears one fixed threshold.

@@ -126,6 +126,14 @@ int oracle_schedule_loop(const float* c, const double* sps, int n_sps, int R, in
 int oracle_schedule_closed(const float* c, const double* sps, int n_sps, int R, int gamma,
                            int32_t* lengths, double* theta, double* min_rel_gap);
 
+/* Production-style scheduler (explainer section 04): budget = the n* of two
+ * steps back (negative: none yet, this step's n* is used); the candidates
+ * in the scheduler's order fill min(budget, count) places; theta = tau *
+ * SPS at that batch; *n_star = this step's synchronous n*.  Returns the
+ * number of places filled. */
+int oracle_schedule_budget(const float* c, const double* sps, int n_sps, int R, int gamma, int budget,
+                           int32_t* lengths, double* theta, int32_t* n_star);
+
 /* Expected calibration error (Guo et al., ICML 2017, section 2) of
  * predictions pred[N] against outcomes y[N] (nonzero = 1) over M
  * equal-width bins of [0, 1]; p = 1 falls in the last bin. */

@@ -637,3 +637,38 @@ def test_sts_first_position_is_a_plain_grid_search():
     y = (al >= 1).astype(np.int32)
     e = [oracle.ece(oracle.sts_apply(c[:, :1], [t])[:, 0], y, 12) for t in grid]
     assert r["g"][0] == int(np.argmin(e)) and abs(r["ece"][0] - min(e)) < 1e-15
+
+
+# ------------------------------------------------------------------ production-style scheduler
+def test_budget_scheduler_fills_the_capacity_in_the_scheduler_order():
+    """Explainer section 04: the capacity comes from two steps back and the
+    current candidates are ranked into it.  c = (0.9, 0.8), (0.5, 0.99) gives
+    a = (0.9, 0.72), (0.5, 0.495): the order is (r0 j1), (r0 j2), (r1 j1),
+    (r1 j2), so capacities 1..4 give lengths (1,0), (2,0), (2,1), (2,2); with a
+    flat SPS = 1, theta = 2 + the sum of the chosen a."""
+    c = np.array([[0.9, 0.8], [0.5, 0.99]], np.float32)
+    a = oracle.prefix_survival(c).astype(np.float64)
+    sps = np.ones(2 * 3 + 1)
+    want = {1: [1, 0], 2: [2, 0], 3: [2, 1], 4: [2, 2], 9: [2, 2]}
+    tops = [a[0, 0], a[0, 1], a[1, 0], a[1, 1]]
+    for b, L in want.items():
+        got, th, n, ns = oracle.schedule_budget(c, sps, b)
+        np.testing.assert_array_equal(got, L)
+        assert n == min(b, 4) and abs(th - (2 + sum(tops[:n]))) < 1e-12
+    got, th, n, _ = oracle.schedule_budget(c, sps, 0)
+    assert np.all(got == 0) and n == 0 and th == 2.0
+
+
+@pytest.mark.parametrize("rho", [0.0, 0.5, 0.9])
+def test_budget_scheduler_reduces_to_the_synchronous_one(rho):
+    """With its own n* as the capacity (or none) the production-style rule is
+    the synchronous scheduler, and the n* it reports is the closed form's."""
+    rng = np.random.default_rng(int(rho * 10))
+    for R, gamma in [(3, 4), (16, 5), (64, 8)]:
+        c = (1 / (1 + np.exp(-rng.normal(1.5, 1.0, (R, gamma))))).astype(np.float32)
+        sps = synth.gen_sps(R, gamma, rho)
+        L0, th0, n0, _ = oracle.schedule_closed(c, sps)
+        for b in (-1, n0):
+            L, th, n, ns = oracle.schedule_budget(c, sps, b)
+            np.testing.assert_array_equal(L, L0)
+            assert n == n0 == ns and abs(th - th0) <= 1e-12 * max(1.0, abs(th0))
