@@ -292,6 +292,25 @@ int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gam
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Production-style scheduler (explainer section 04: the capacity comes from
+ * the predictions of two steps back, and the current candidates are ranked
+ * into it, so a pipelined server never waits on the current step's stopping
+ * rule).  Same inputs and ordering as dspark_schedule, plus
+ *   budget  [1]  int32  (device) the capacity: the n_star that this call (or
+ *                dspark_schedule) wrote two steps earlier; a negative value
+ *                means no history yet and this step's own n* is used.
+ * The candidates fill min(budget, number of candidates with a > 0) places:
+ * verify_len counts each request's places, theta = tau * SPS[R + places],
+ * and n_star receives this step's own synchronous n* (the capacity for two
+ * steps later).  A caller keeps three n_star buffers in rotation and passes
+ * the one of step t - 2 as the budget of step t: everything stays on the
+ * device.  Errors as dspark_schedule; INVALID_ARG for a null budget.
+ */
+int dspark_schedule_async(const float* c, const double* sps, int n_sps, int R, int gamma,
+                          const int32_t* budget, int32_t* verify_len, double* theta, int32_t* n_star,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Threshold filter (blog section 4.3, the confidence-threshold sweep; the
  * explainer's section 04 sets the scheduler against one fixed threshold for
  * every request): request r verifies its longest prefix of positions whose

@@ -73,6 +73,7 @@ def load(build_if_missing: bool = True):
         L.dspark_draft_rnn_conf.argtypes = [P, i32, P, P, P, P, i32, P, i32, i32, i32, i32, i32, u64, P, f32,
                                             P, P, P, P, P, P, P, sz, P]
         L.dspark_schedule.argtypes = [P, P, i32, i32, i32, P, P, P, P, sz, P]
+        L.dspark_schedule_async.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, sz, P]
         L.dspark_schedule_threshold.argtypes = [P, i32, i32, f32, i32, P, P]
         L.dspark_sts_workspace_size.argtypes = [i32, i32, i32, i32]
         L.dspark_sts_workspace_size.restype = sz
@@ -83,7 +84,8 @@ def load(build_if_missing: bool = True):
         L.dspark_profile_kernel_name.argtypes = [i32]
         L.dspark_profile_kernel_name.restype = ctypes.c_char_p
         for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_draft_markov_conf", "dspark_draft_rnn_conf",
-                     "dspark_verify", "dspark_schedule", "dspark_schedule_threshold", "dspark_sts_fit",
+                     "dspark_verify", "dspark_schedule", "dspark_schedule_async", "dspark_schedule_threshold",
+                     "dspark_sts_fit",
                      "dspark_sts_apply",
                      "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
             getattr(L, name).restype = i32
@@ -253,8 +255,10 @@ def verify(P, U, W2, draft, temperature: float, seed: int, verify_len=None, req_
     return out
 
 
-def schedule(c, sps, ws=None, out=None, stream=None):
-    """Confidence scheduler (``dspark_schedule``): verify lengths, Theta*, n*."""
+def schedule(c, sps, ws=None, out=None, stream=None, budget=None):
+    """Confidence scheduler (``dspark_schedule``): verify lengths, Theta*, n*.
+    With ``budget`` (an int32 [1] device tensor: the n_star of two steps back)
+    the production-style rule (``dspark_schedule_async``)."""
     L = load()
     R, gamma = c.shape
     dev = c.device
@@ -264,9 +268,16 @@ def schedule(c, sps, ws=None, out=None, stream=None):
                    n_star=torch.empty((1,), dtype=torch.int32, device=dev))
     if ws is None:
         ws = _workspace(L.dspark_schedule_workspace_size(R, gamma), dev)
-    code = L.dspark_schedule(_p(c), _p(sps), sps.numel(), R, gamma, _p(out["verify_len"]), _p(out["theta"]),
-                             _p(out["n_star"]), _p(ws), ws.numel(), _stream(stream))
-    _check("dspark_schedule", code)
+    if budget is None:
+        code = L.dspark_schedule(_p(c), _p(sps), sps.numel(), R, gamma, _p(out["verify_len"]), _p(out["theta"]),
+                                 _p(out["n_star"]), _p(ws), ws.numel(), _stream(stream))
+        _check("dspark_schedule", code)
+    else:
+        if budget.dtype != torch.int32:
+            raise TypeError("budget must be int32")
+        code = L.dspark_schedule_async(_p(c), _p(sps), sps.numel(), R, gamma, _p(budget), _p(out["verify_len"]),
+                                       _p(out["theta"]), _p(out["n_star"]), _p(ws), ws.numel(), _stream(stream))
+        _check("dspark_schedule_async", code)
     out["ws"] = ws
     return out
 

@@ -213,7 +213,18 @@ int dspark_schedule(const float* c, const double* sps, int n_sps, int R, int gam
     if (!c || !sps || !verify_len || !theta || !n_star) return DSPARK_ERR_INVALID_ARG;
     if (!ws || !aligned256(ws)) return DSPARK_ERR_WORKSPACE;
     if (ws_bytes < sizeof(WsHeader)) return DSPARK_ERR_WORKSPACE;
-    return cuda_status(launch_schedule(c, sps, n_sps, R, gamma, verify_len, theta, n_star, ws,
+    return cuda_status(launch_schedule(c, sps, n_sps, R, gamma, nullptr, verify_len, theta, n_star, ws,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_schedule_async(const float* c, const double* sps, int n_sps, int R, int gamma, const int32_t* budget,
+                          int32_t* verify_len, double* theta, int32_t* n_star, void* ws, size_t ws_bytes,
+                          void* stream) {
+    if (R < 1 || gamma < 1 || gamma > 64 || (long long)R * gamma > 8192 || n_sps < 1) return DSPARK_ERR_SHAPE;
+    if (!c || !sps || !budget || !verify_len || !theta || !n_star) return DSPARK_ERR_INVALID_ARG;
+    if (!ws || !aligned256(ws)) return DSPARK_ERR_WORKSPACE;
+    if (ws_bytes < sizeof(WsHeader)) return DSPARK_ERR_WORKSPACE;
+    return cuda_status(launch_schedule(c, sps, n_sps, R, gamma, budget, verify_len, theta, n_star, ws,
                                        static_cast<cudaStream_t>(stream)));
 }
 

@@ -119,8 +119,8 @@ cudaError_t launch_sts_fit(const float* c, const int32_t* accept_len, int N, int
 cudaError_t launch_sts_apply(const float* c, int N, int gamma, const double* t, float* out, cudaStream_t s);
 cudaError_t launch_schedule_threshold(const float* c, int R, int gamma, float theta, int mode, int32_t* len,
                                       cudaStream_t s);
-cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,
-                            double* theta, int32_t* nstar, void* ws, cudaStream_t s);
+cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, const int32_t* budget,
+                            int32_t* len, double* theta, int32_t* nstar, void* ws, cudaStream_t s);
 
 int num_sms();
 

@@ -127,9 +127,14 @@ __device__ void bitonic_sort_regs(unsigned long long* keys, int Np) {
             if (8 * t + e < Np) keys[kslot(8 * t + e)] = k[e];
 }
 
+// budget (may be null): the capacity decided two steps back (the
+// production-style scheduler of explainer section 04); the candidates fill
+// min(budget, count) places instead of n*, and nstar still receives this
+// step's own n* (the capacity for two steps later).  A negative budget means
+// none yet.
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c, const double* sps, int n_sps,
-                                                                 int R, int gamma, int Np, int32_t* len,
-                                                                 double* theta, int32_t* nstar) {
+                                                                 int R, int gamma, int Np, const int32_t* budget,
+                                                                 int32_t* len, double* theta, int32_t* nstar) {
     pdl_launch_dependents();
     extern __shared__ __align__(16) unsigned char smem[];
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
@@ -263,8 +268,13 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     }
     __syncthreads();
     const int ns = s_nstar == INT_MAX ? nvalid : s_nstar;
+    int nb = ns;
+    if (budget) {
+        const int b = *budget;
+        nb = b < 0 ? ns : (b < nvalid ? b : nvalid);
+    }
     // 5: lengths
-    for (int i = tid; i < ns; i += blockDim.x) {
+    for (int i = tid; i < nb; i += blockDim.x) {
         const int idx = (int)(unsigned)(keys[kslot(i)] & 0xFFFFFFFFull);
         atomicAdd(&cnt[idx / gamma], 1);
     }
@@ -272,8 +282,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* c,
     for (int r = tid; r < R; r += blockDim.x) len[r] = cnt[r];
     if (tid == 0) {
         *nstar = ns;
-        const double tn = (double)R + (ns > 0 ? val[ns - 1] : 0.0);
-        *theta = tn * sps_at(sps, n_sps, (long long)R + ns);
+        const double tn = (double)R + (nb > 0 ? val[nb - 1] : 0.0);
+        *theta = tn * sps_at(sps, n_sps, (long long)R + nb);
     }
 }
 
@@ -288,16 +298,16 @@ size_t schedule_smem_bytes(int R, int gamma) {
     return (size_t)kslot(Np) * 8 + (size_t)Np * 8 + (size_t)R * sizeof(int);
 }
 
-cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, int32_t* len,
-                            double* theta, int32_t* nstar, void* ws, cudaStream_t s) {
+cudaError_t launch_schedule(const float* c, const double* sps, int n_sps, int R, int gamma, const int32_t* budget,
+                            int32_t* len, double* theta, int32_t* nstar, void* ws, cudaStream_t s) {
     (void)ws;
     const int Np = next_pow2(R * gamma < 2 ? 2 : R * gamma);
     const size_t smem = schedule_smem_bytes(R, gamma);
     cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_begin(kPSchedule, s);
-    e = launch_kernel(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, false, c, sps, n_sps, R, gamma, Np, len,
-                      theta, nstar);
+    e = launch_kernel(schedule_kernel, dim3(1), dim3(kSchedThreads), smem, s, false, c, sps, n_sps, R, gamma, Np,
+                      budget, len, theta, nstar);
     prof_end(s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -114,3 +114,12 @@ def test_sts_arguments_rejected_on_the_host():
     assert L.dspark_sts_apply(fake, 0, 8, fake, fake, null) == -3
     assert L.dspark_sts_apply(fake, 10, 65, fake, fake, null) == -3
     assert L.dspark_sts_apply(null, 10, 8, fake, fake, null) == -1
+
+
+def test_schedule_async_arguments_rejected_on_the_host():
+    L = binding.load()
+    null = None
+    fake = ctypes.c_void_p(4096)
+    assert L.dspark_schedule_async(fake, fake, 10, 4, 5, null, fake, fake, fake, fake, 1 << 12, null) == -1
+    assert L.dspark_schedule_async(fake, fake, 10, 1000, 16, fake, fake, fake, fake, fake, 1 << 12, null) == -3
+    assert L.dspark_schedule_async(fake, fake, 10, 4, 5, fake, fake, fake, fake, null, 1 << 12, null) == -8

@@ -173,3 +173,47 @@ def test_host_argument_errors():
     with pytest.raises(binding.DsparkError) as e:
         binding.draft_markov(dev(x["U"]), dev(x["anchor"]), dev(x["W1"]), dev(x["W2"]), 1.0, 0, ws=small_ws)
     assert e.value.code == -8
+
+
+@pytest.mark.parametrize("R,gamma,rho", [(1, 1, 0.0), (5, 16, 0.5), (64, 5, 0.9), (300, 7, 0.1), (512, 16, 0.5)])
+def test_schedule_async_parity(R, gamma, rho):
+    """Production-style scheduler (explainer section 04): capacities of none,
+    0, the step's own n*, a random value and more than the candidate count;
+    lengths and the reported n* exact (unless the oracle's Theta comparison
+    is a near-tie), theta within 1e-12."""
+    rng = np.random.default_rng(R * 7 + gamma)
+    c = (1 / (1 + np.exp(-rng.normal(1.5, 1.0, (R, gamma))))).astype(np.float32)
+    c[0, min(1, gamma - 1)] = 0.0
+    sps = synth.gen_sps(R, gamma, rho)
+    _, _, n0, gap = oracle.schedule_closed(c, sps)
+    if gap < 1e-12:
+        pytest.skip("near-tie of Theta in this draw")
+    for b in (-1, 0, n0, int(rng.integers(0, R * gamma + 1)), R * gamma + 5):
+        bud = dev(np.array([b], np.int32))
+        out = binding.schedule(dev(c), dev(sps), budget=bud)
+        L, th, n, ns = oracle.schedule_budget(c, sps, b)
+        np.testing.assert_array_equal(host(out["verify_len"]), L, err_msg=f"budget {b}")
+        assert int(host(out["n_star"])[0]) == ns == n0
+        np.testing.assert_allclose(host(out["theta"])[0], th, rtol=1e-12)
+
+
+def test_schedule_async_two_steps_back_ring():
+    """Six steps with three n_star buffers in rotation: step t takes the
+    n_star of step t - 2 as its capacity (none for the first two), all on the
+    device, against the oracle following the same protocol."""
+    R, gamma, rho = 64, 5, 0.3
+    rng = np.random.default_rng(11)
+    ring = [dev(np.array([-1], np.int32)) for _ in range(3)]
+    hist = []
+    for t in range(6):
+        c = (1 / (1 + np.exp(-rng.normal(1.0 + 0.2 * t, 1.2, (R, gamma))))).astype(np.float32)
+        sps = synth.gen_sps(R, gamma, rho)
+        budget = ring[(t - 2) % 3] if t >= 2 else dev(np.array([-1], np.int32))
+        out = dict(verify_len=torch.empty((R,), dtype=torch.int32, device="cuda:0"),
+                   theta=torch.empty((1,), dtype=torch.float64, device="cuda:0"), n_star=ring[t % 3])
+        binding.schedule(dev(c), dev(sps), budget=budget, out=out)
+        b = hist[t - 2] if t >= 2 else -1
+        L, th, n, ns = oracle.schedule_budget(c, sps, b)
+        hist.append(ns)
+        np.testing.assert_array_equal(host(out["verify_len"]), L, err_msg=f"step {t}")
+        assert int(host(ring[t % 3])[0]) == ns
