@@ -181,18 +181,19 @@ def job_throughput(positions_per_rank_step: int, world: int, steps: int, max_ms:
     return positions_per_rank_step * world * steps / (max_ms / 1000.0)
 
 
-def algorithmic_bytes(w, n_rej: float, verify_rows: int):
-    """Bytes the cycle must move (each input element once; the residual pass
-    re-reads U_j and P_j of every rejecting request and W2 once)."""
+def algorithmic_bytes(w, n_rej: float, verify_rows: float):
+    """Bytes the cycle must move: U, W2 and the W1 rows once; the target rows
+    verification must read (each request's rows up to its first rejection,
+    or through the bonus row: accept_len + 1 rows); the residual pass's
+    re-read of U_j and P_j of every rejecting request and W2 once."""
     su = 4 if w.u_dtype == synth.F32 else 2
     sp = 4 if w.p_dtype == synth.F32 else 2
     sw = 4 if w.w_dtype == synth.F32 else 2
     draft = w.R * w.gamma * w.V * su + w.r * w.V * sw + w.R * w.gamma * w.r * sw
     verify1 = verify_rows * w.V * sp
     resid = n_rej * w.V * (su + sp) + (w.r * w.V * sw if n_rej > 0 else 0)
-    return dict(draft=draft, verify_pass1=verify1, residual=resid, total=draft + verify1 + resid,
+    return dict(draft=draft, verify_rows=verify1, residual=resid, total=draft + verify1 + resid,
                 sweep_per_launch=(w.R * w.V * su + w.r * w.V * sw / w.gamma + w.R * w.r * sw),
-                pass1_per_launch=verify1,
                 residual_per_launch=resid)
 
 
@@ -511,12 +512,13 @@ def main(argv=None):
     n_rej = float(np.mean([int((o[0] < w.gamma).sum().item()) for o in outs]))
     sweeps = [ms for name, ms in launches if name.startswith("draft_sweep")]
     sweep_by_k = [round(float(np.mean(sweeps[k::w.gamma])), 4) for k in range(w.gamma)] if sweeps else None
-    ab = algorithmic_bytes(w, n_rej, w.R * (w.gamma + 1))
+    rows_read = float(np.mean([int((o[0] + 1).sum().item()) for o in outs]))
+    ab = algorithmic_bytes(w, n_rej, rows_read)
     hbm_peak, bf16_peak, peak_src = _peaks()
     dom = max(table.items(), key=lambda kv: kv[1][1])
     dom_name, (dom_n, dom_ms) = dom[0], dom[1]
     per_launch = {"draft_sweep_tc": ab["sweep_per_launch"], "draft_sweep_generic": ab["sweep_per_launch"],
-                  "verify_pass1": ab["pass1_per_launch"], "verify_residual_tc": ab["residual_per_launch"],
+                  "verify_residual_tc": ab["residual_per_launch"],
                   "verify_residual_generic": ab["residual_per_launch"]}
     dom_bytes = per_launch.get(dom_name)
     roofline = None
@@ -628,7 +630,7 @@ def main(argv=None):
             "roofline": roofline,
             "cycle": {"algorithmic_bytes": int(ab["total"]), "achieved_gbs": round(cycle_gbs, 1) if cycle_gbs else None,
                       "hbm_frac": round(cycle_gbs / hbm_peak, 4) if cycle_gbs else None,
-                      "rejecting_requests_per_step": n_rej},
+                      "rejecting_requests_per_step": n_rej, "target_rows_read_per_step": rows_read},
             "kernels": kernels,
             "draft_sweep_ms_by_position": sweep_by_k,
             "ms_per_step_profiled": round(sum(prof_ms) / len(prof_ms), 4),

@@ -224,7 +224,10 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int r);
  *   n_out      [R]            int32  accept_len + 1
  *   p_tok      [R, gamma]     float  p_k(x_k) for tested positions (may be NULL)
  *   lse_p      [R, gamma + 1] double log-sum-exp of P_k / T for rows read (may be NULL)
- * Rows the request never reads hold NaN in p_tok / lse_p.
+ * Rows the request never reads hold NaN in p_tok / lse_p.  The target rows
+ * are read in windows of rows [0, 2), [2, 5), [5, 11), [11, gamma + 1): a
+ * request reads the windows up to the one that holds its first rejection
+ * (or its bonus row) and no further.
  * Requirements as for drafting, and V <= 2^18 when T > 0 (the sampling tree
  * keeps at most 1024 top-level nodes of 256 words; greedy takes V <= 2^20);
  * larger vocabularies return DSPARK_ERR_SHAPE before anything is enqueued.

@@ -44,25 +44,44 @@ __device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
     return L < 0 ? 0 : (L > A.gamma ? A.gamma : L);
 }
 
+// ------------------------------------------------------------------ waves
+// Verification reads the target rows in waves: a request needs row k
+// (0-based) only while positions 1..k were all accepted, and row L (the
+// bonus row) only when all L were.  Wave w covers rows [lo_w, hi_w) of the
+// requests still live (all of them in wave 1); its pass 1 streams those rows,
+// its acceptance pass decides every live request on them and lists the ones
+// that passed the whole window for the next wave.
+// Windows [0, 2), [2, 5), [5, 11), [11, gamma + 1).
+__host__ __device__ __forceinline__ int wave_lo(int w) { return w <= 1 ? 0 : (w == 2 ? 2 : (w == 3 ? 5 : 11)); }
+__host__ __device__ __forceinline__ int wave_hi(int w, int G1) {
+    const int e = w <= 1 ? 2 : (w == 2 ? 5 : (w == 3 ? 11 : G1));
+    return e < G1 ? e : G1;
+}
+__host__ __device__ __forceinline__ int live_count(const VerifyArgs& A, int w) {
+    return w == 1 ? A.R : A.wcount_alive[w];
+}
+__device__ __forceinline__ int live_request(const VerifyArgs& A, int w, int i) {
+    return w == 1 ? i : A.alive[(size_t)(w & 1) * A.R + i];
+}
+
 // ------------------------------------------------------------------ pass 1
+// Warp tasks over (live request, row of the window, 1024-column chunk).
 template <int PT, bool GREEDY>
-__global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
+__global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
     pdl_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0) {   // the accept pass appends to these
-        *A.rej_count = 0;
-        *A.vflags = 0u;
-    }
+    pdl_wait();   // the list of live requests (waves after the first)
     const int lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (blockDim.x >> 5);
     const int V = A.V, G1 = A.gamma + 1, NCH = A.nch;
-    const long long tasks = (long long)A.R * G1 * NCH;
+    const int lo = wave_lo(w), nrow = wave_hi(w, G1) - lo;
+    const long long tasks = (long long)live_count(A, w) * nrow * NCH;
     const float invT = GREEDY ? 1.f : 1.f / A.T;
     for (long long task = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks;
          task += warps_total) {
         const int ch = (int)(task % NCH);
         const long long rr = task / NCH;
-        const int row = (int)(rr % G1);
-        const int r = (int)(rr / G1);
+        const int row = lo + (int)(rr % nrow);
+        const int r = live_request(A, w, (int)(rr / nrow));
         if (row > verify_len_of(A, r)) continue;            // warp-uniform
         const size_t base = ((size_t)r * G1 + row) * (size_t)V;
         const int c0 = ch * kChunk;
@@ -120,18 +139,20 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A) {
             s = warp_sum(s);
             out = make_float2(mw, s);
         }
-        if (lane == 0) A.vparts[rr * NCH + ch] = out;
+        if (lane == 0) A.vparts[((size_t)r * G1 + row) * NCH + ch] = out;
     }
 }
 
 // ------------------------------------------------------------------ accept
-// One CTA per request.  Warp w reduces rows w, w + 8, ... of pass 1's
-// partials (the log-sum-exp of each P row, or its argmax at T = 0) while the
-// drafted tokens and their target logits P_k[x_k] are fetched, which do not
-// depend on it; then every verified position is tested at once and the first
-// rejection decides (everything after it is discarded).
+// One CTA per live request of wave w.  Warp v reduces the window's rows
+// lo + v, lo + v + 8, ... of pass 1's partials (the log-sum-exp of each P
+// row, or its argmax at T = 0) while the drafted tokens and their target
+// logits P_k[x_k] are fetched, which do not depend on it; then every
+// position of the window is tested at once and the first rejection decides
+// (everything after it is discarded).  A request that passes the whole
+// window goes to the next wave's list, unless the window held its bonus row.
 template <int PT, bool GREEDY>
-__global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
+__global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
     __shared__ double s_lse[65];
     __shared__ int s_arg[65];
     __shared__ int s_x[64];
@@ -139,30 +160,36 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
     __shared__ int s_first;
     pdl_launch_dependents();
     pdl_wait();
+    if ((int)blockIdx.x >= live_count(A, w)) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-    const int r = blockIdx.x;
+    const int r = live_request(A, w, blockIdx.x);
     const int G1 = A.gamma + 1, NCH = A.nch, V = A.V;
     const int L = verify_len_of(A, r);
+    const int lo = wave_lo(w), hi = wave_hi(w, G1);
+    const int rhi = min(hi - 1, L);        // the window's rows this request needs: lo .. rhi
+    const int npos = min(hi, L) - lo;      // positions lo + 1 .. lo + npos are tested
     const float invT = GREEDY ? 1.f : 1.f / A.T;
     int32_t* out = A.out_tokens + (size_t)r * G1;
-    if (tid < G1) {
+    if (w == 1 && tid < G1) {
+        // outputs start empty; lse_p rows computed in this wave are written below
         out[tid] = -1;
-        if (A.lse_p && (GREEDY || tid > L)) A.lse_p[(size_t)r * G1 + tid] = NAN;   // rows 0..L: below
+        if (A.lse_p && (GREEDY || tid > rhi)) A.lse_p[(size_t)r * G1 + tid] = NAN;
         if (A.p_tok && tid < A.gamma) A.p_tok[(size_t)r * A.gamma + tid] = NAN;
     }
     if (tid == 0) s_first = INT_MAX;
-    // drafted token x_k and its raw target logit, thread k - 1 for position k <= L
-    if (tid < L) {
-        int x = A.tokens[(size_t)r * A.gamma + tid];
+    // drafted token x_k and its raw target logit, thread k - lo - 1 for position k
+    if (tid < npos) {
+        const int row = lo + tid;
+        int x = A.tokens[(size_t)r * A.gamma + row];
         if (x < 0 || x >= V) {
             raise_status(A.ws, kStatBadToken);
             x = 0;
         }
-        s_x[tid] = x;
-        if (!GREEDY) s_px[tid] = ld_elem(A.P, PT, ((size_t)r * G1 + tid) * (size_t)V + x);
+        s_x[row] = x;
+        if (!GREEDY) s_px[row] = ld_elem(A.P, PT, ((size_t)r * G1 + row) * (size_t)V + x);
     }
     const float2* parts = A.vparts + (size_t)r * G1 * NCH;
-    for (int row = warp; row <= L; row += blockDim.x >> 5) {
+    for (int row = lo + warp; row <= rhi; row += blockDim.x >> 5) {
         const float2* pr = parts + (size_t)row * NCH;
         if (GREEDY) {
             float best = -INFINITY;
@@ -208,17 +235,17 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
         }
     }
     __syncthreads();
-    // position k <= L (thread k - 1): accept or reject
+    // position k = lo + tid + 1: accept or reject
     double px = 0.0;
-    if (tid < L) {
-        const int k = tid + 1;
+    if (tid < npos) {
+        const int row = lo + tid, k = row + 1;
         bool rej;
         if (GREEDY) {
-            rej = s_x[tid] != s_arg[tid];
+            rej = s_x[row] != s_arg[row];
         } else {
             // p(x) = exp(P_x / T - lse_P), the difference formed in double
-            px = exp_from_double((double)s_px[tid] * (double)invT - s_lse[tid]);
-            const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + tid];
+            px = exp_from_double((double)s_px[row] * (double)invT - s_lse[row]);
+            const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + row];
             const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
             const double u = rng_uniform_d(philox_key(A.seed), req, (uint32_t)k, 1u, 0u);
             rej = !(u < ratio);
@@ -227,22 +254,31 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A) {
     }
     __syncthreads();
     const int j = s_first == INT_MAX ? 0 : s_first;      // first rejected position, 0 if none
-    if (tid < L) {
-        const int k = tid + 1;
-        if (!GREEDY && A.p_tok && (!j || k <= j)) A.p_tok[(size_t)r * A.gamma + tid] = (float)px;
-        if (!j || k < j) out[tid] = s_x[tid];
-        else if (GREEDY && k == j) out[tid] = s_arg[tid];   // the target's own token replaces x_j
+    if (tid < npos) {
+        const int row = lo + tid, k = row + 1;
+        if (!GREEDY && A.p_tok && (!j || k <= j)) A.p_tok[(size_t)r * A.gamma + row] = (float)px;
+        if (!j || k < j) out[row] = s_x[row];
+        else if (GREEDY && k == j) out[row] = s_arg[row];   // the target's own token replaces x_j
     }
     if (tid == 0) {
-        const int acc = j ? j - 1 : L;
-        if (GREEDY) {
-            if (!j) out[L] = s_arg[L];                   // bonus: all L drafts matched
-            A.vstate[r] = make_int2(kModeDone, 0);
+        if (j) {
+            A.vstate[r] = GREEDY ? make_int2(kModeDone, 0) : make_int2(kModeResidual, j);
+            A.accept_len[r] = j - 1;
+            A.n_out[r] = j;
+        } else if (L < hi) {
+            // all L drafts accepted and the bonus row was in this window
+            if (GREEDY) {
+                out[L] = s_arg[L];
+                A.vstate[r] = make_int2(kModeDone, 0);
+            } else {
+                A.vstate[r] = make_int2(kModeBonus, L + 1);
+            }
+            A.accept_len[r] = L;
+            A.n_out[r] = L + 1;
         } else {
-            A.vstate[r] = j ? make_int2(kModeResidual, j) : make_int2(kModeBonus, L + 1);
+            const int slot = atomicAdd(A.wcount_alive + w + 1, 1);
+            A.alive[(size_t)((w + 1) & 1) * A.R + slot] = r;
         }
-        A.accept_len[r] = acc;
-        A.n_out[r] = acc + 1;
     }
     if (GREEDY || !j) return;
     // queue the rejecting request for the residual pass with its code e_j as
@@ -530,6 +566,7 @@ size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
     off = align_up(off + (size_t)R * N2 * 4 * sizeof(float), 256);      // rpart
     off = align_up(off + 256, 256);                                      // counters, flags
     off = align_up(off + (size_t)R * sizeof(int), 256);                 // rej_list
+    off = align_up(off + 2ull * R * sizeof(int), 256);                  // live requests of the waves
     const size_t rpad = (size_t)((R + 127) / 128) * 128;
     off = align_up(off + 3 * rpad * r * sizeof(uint16_t), 256);          // a_res: hi, mid, lo planes
     return off;
@@ -550,11 +587,16 @@ int verify_carve(VerifyArgs& a, size_t ws_bytes) {
     off = align_up(off + (size_t)a.R * sizeof(int2), 256);
     a.rpart = reinterpret_cast<float*>(base + off);
     off = align_up(off + (size_t)a.R * N2 * 4 * sizeof(float), 256);
+    // counters cleared before each verification (one 256-byte block):
+    // rejection count, flags, live requests per wave
     a.rej_count = reinterpret_cast<int*>(base + off);
     a.vflags = reinterpret_cast<uint32_t*>(base + off + 16);
+    a.wcount_alive = reinterpret_cast<int*>(base + off + 32);
     off = align_up(off + 256, 256);
     a.rej_list = reinterpret_cast<int*>(base + off);
     off = align_up(off + (size_t)a.R * sizeof(int), 256);
+    a.alive = reinterpret_cast<int*>(base + off);
+    off = align_up(off + 2ull * a.R * sizeof(int), 256);
     a.a_res = reinterpret_cast<uint16_t*>(base + off);
     return DSPARK_OK;
 }
@@ -563,32 +605,29 @@ template <int PT, int UT, int WT>
 static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     const bool greedy = !(a.T > 0.f);
     const int nsm = num_sms();
-    const long long tasks = (long long)a.R * (a.gamma + 1) * a.nch;
-    long long want = (tasks + 7) / 8;
-    int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
-    if (grid < 1) grid = 1;
-    // pass 1 waits for the caller's work; every later launch overlaps the
-    // previous kernel's tail
-    cudaError_t e;
-    if (greedy) {
+    const int G1 = a.gamma + 1;
+    cudaError_t e = cudaMemsetAsync(a.rej_count, 0, 256, s);
+    if (e != cudaSuccess) return e;
+    // the waves: the first pass 1 waits for the caller's work (and the
+    // cleared counters); every later launch overlaps the previous kernel's tail
+    for (int w = 1; w <= 4 && wave_lo(w) < G1; ++w) {
+        const long long tasks = (long long)a.R * (wave_hi(w, G1) - wave_lo(w)) * a.nch;
+        const long long want = (tasks + 7) / 8;
+        int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
+        if (grid < 1) grid = 1;
         prof_begin(kPVerifyPass1, s);
-        e = launch_kernel(verify_pass1<PT, true>, dim3(grid), dim3(256), 0, s, false, a);
+        e = greedy ? launch_kernel(verify_pass1<PT, true>, dim3(grid), dim3(256), 0, s, w > 1, a, w)
+                   : launch_kernel(verify_pass1<PT, false>, dim3(grid), dim3(256), 0, s, w > 1, a, w);
         prof_end(s);
         if (e != cudaSuccess) return e;
         prof_begin(kPVerifyAccept, s);
-        e = launch_kernel(verify_accept<PT, true>, dim3(a.R), dim3(256), 0, s, true, a);
+        e = greedy ? launch_kernel(verify_accept<PT, true>, dim3(a.R), dim3(256), 0, s, true, a, w)
+                   : launch_kernel(verify_accept<PT, false>, dim3(a.R), dim3(256), 0, s, true, a, w);
         prof_end(s);
-        return e != cudaSuccess ? e : cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    prof_begin(kPVerifyPass1, s);
-    e = launch_kernel(verify_pass1<PT, false>, dim3(grid), dim3(256), 0, s, false, a);
-    prof_end(s);
-    if (e != cudaSuccess) return e;
-    prof_begin(kPVerifyAccept, s);
-    e = launch_kernel(verify_accept<PT, false>, dim3(a.R), dim3(256), 0, s, true, a);
-    prof_end(s);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (greedy) return cudaSuccess;
     a.tc = verify_tc_supported(a) ? 1 : 0;
     if (a.tc) {
         e = launch_verify_tc_residual(a, s);
