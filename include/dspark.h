@@ -225,7 +225,7 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int r);
  *   p_tok      [R, gamma]     float  p_k(x_k) for tested positions (may be NULL)
  *   lse_p      [R, gamma + 1] double log-sum-exp of P_k / T for rows read (may be NULL)
  * Rows the request never reads hold NaN in p_tok / lse_p.  The target rows
- * are read in windows of rows [0, 2), [2, 5), [5, 11), [11, gamma + 1): a
+ * are read in windows of rows [0, 1), [1, 3), [3, 7), [7, gamma + 1): a
  * request reads the windows up to the one that holds its first rejection
  * (or its bonus row) and no further.
  * Requirements as for drafting, and V <= 2^18 when T > 0 (the sampling tree
