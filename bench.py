@@ -539,15 +539,23 @@ def main(argv=None):
             hU = hU.view(torch.bfloat16)
         if x["P"].dtype == np.uint16:
             hP = hP.view(torch.bfloat16)
+        n_e2e = args.e2e_steps
         h_out = torch.empty((w.R, w.gamma + 1), dtype=torch.int32).pin_memory()
-        h_n = torch.empty((w.R,), dtype=torch.int32).pin_memory()
-        # two device input sets: the host-to-device copy of step i + 1 runs on
-        # its own stream while step i computes (double buffering); every step's
-        # inputs are still copied, and every result read back, inside the
-        # timed region, which opens before the first copy
-        bufs = [dict(U=U, P=P, anchor=anchor, c=c),
-                dict(U=torch.empty_like(U), P=torch.empty_like(P), anchor=torch.empty_like(anchor),
-                     c=torch.empty_like(c))]
+        h_n = [torch.empty((w.R,), dtype=torch.int32).pin_memory() for _ in range(n_e2e)]
+        # the target logits stay in pinned host memory and verification reads
+        # them in place (zero copy): only the rows its decisions need cross the
+        # host link; U (all of it is drafted from), the anchors and c are
+        # copied.  The device holds two sets of the copied inputs: the copy of
+        # step i + 1 runs on its own stream while step i computes.  The timed
+        # region opens before the first copy and closes after the last result
+        # is read back.
+        try:
+            Pv = binding.host_view(hP, devc)
+        except Exception:                                   # not mapped: copy P as well
+            Pv = None
+        bufs = [dict(U=U, P=Pv if Pv is not None else P, anchor=anchor, c=c),
+                dict(U=torch.empty_like(U), P=Pv if Pv is not None else torch.empty_like(P),
+                     anchor=torch.empty_like(anchor), c=torch.empty_like(c))]
         cstream = torch.cuda.Stream(device=devc)
         ev_copied = [torch.cuda.Event() for _ in range(2)]
         ev_free = [torch.cuda.Event() for _ in range(2)]
@@ -556,7 +564,8 @@ def main(argv=None):
             b = bufs[bi]
             with torch.cuda.stream(cstream):
                 b["U"].copy_(hU, non_blocking=True)
-                b["P"].copy_(hP, non_blocking=True)
+                if Pv is None:
+                    b["P"].copy_(hP, non_blocking=True)
                 b["anchor"].copy_(hA, non_blocking=True)
                 b["c"].copy_(hC, non_blocking=True)
                 ev_copied[bi].record(cstream)
@@ -567,7 +576,7 @@ def main(argv=None):
             v = binding.verify(b["P"], b["U"], W2, d, w.T, seed, verify_len=None, req_ids=rid, ws=wss[2])
             return d, s_, v
 
-        def pipeline(n, seed0):
+        def pipeline(n, seed0, keep):
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             t0.record(stream)
             cstream.wait_event(t0)
@@ -577,7 +586,7 @@ def main(argv=None):
                 stream.wait_event(ev_copied[bi])
                 d, s_, v = step_on(bufs[bi], seed0 + i)
                 h_out.copy_(v["out_tokens"], non_blocking=True)
-                h_n.copy_(v["n_out"], non_blocking=True)
+                keep[i].copy_(v["n_out"], non_blocking=True)
                 ev_free[bi].record(stream)
                 if i + 1 < n:
                     nb = (i + 1) % 2
@@ -588,20 +597,39 @@ def main(argv=None):
             torch.cuda.synchronize()
             return t0.elapsed_time(t1)
 
-        pipeline(2, 4000)                                   # warm-up
+        pipeline(2, 4000, h_n)                              # warm-up
         flush.zero_()
         torch.cuda.synchronize()
-        n_e2e = args.e2e_steps
-        e2e_ms = [pipeline(n_e2e, 5000) / n_e2e] * n_e2e
-        h2d = int(hU.numel() * hU.element_size() + hP.numel() * hP.element_size() + hA.numel() * 4 + hC.numel() * 4)
-        d2h = int(h_out.numel() * 4 + h_n.numel() * 4)
+        e2e_ms = [pipeline(n_e2e, 5000, h_n) / n_e2e] * n_e2e
+        copied = int(hU.numel() * hU.element_size() + hA.numel() * 4 + hC.numel() * 4)
+        if Pv is None:
+            p_bytes = float(hP.numel() * hP.element_size())
+        else:
+            # target bytes fetched: the rows of every window up to the one that
+            # decided each request, the residual's rejecting rows again, the
+            # sampler's chunk of each sampled row (256 or 1024 values)
+            sp_ = hP.element_size()
+            G1 = w.gamma + 1
+            per = []
+            for hn in h_n:
+                dec = hn.numpy().astype(np.int64) - 1                 # decision row = accept_len
+                hi = np.where(dec < 1, 1, np.where(dec < 3, 3, np.where(dec < 7, 7, G1)))
+                rows = np.minimum(hi, G1).sum()
+                rej = int((dec < w.gamma).sum())
+                per.append((rows + rej) * w.V * sp_ + rej * 256 * sp_ + (w.R - rej) * 1024 * sp_)
+            p_bytes = float(np.mean(per))
+        h2d = int(copied + p_bytes)
+        d2h = int(h_out.numel() * 4 + h_n[0].numel() * 4)
         e2e_tot = max_over_ranks(sum(e2e_ms), world, devc)
         e2e_value = job_throughput(w.R * w.gamma, world, len(e2e_ms), e2e_tot)
         e2e = {"value": round(e2e_value, 1), "unit": "positions/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_tot / len(e2e_ms), 3),
-               "steps": len(e2e_ms), "copies": "pinned host -> device on a second stream, double-buffered: the copy "
-                                               "of step i + 1 overlaps step i; the timed region opens before the "
-                                               "first copy and closes after the last result is read back"}
+               "steps": len(e2e_ms),
+               "inputs": ("U, anchors, c copied from pinned host memory on a second stream, double-buffered (the copy "
+                          "of step i + 1 overlaps step i); P read in place from pinned host memory, only the rows "
+                          "verification needs (h2d_bytes_per_step counts the bytes fetched)" if Pv is not None else
+                          "U, P, anchors, c copied from pinned host memory on a second stream, double-buffered"),
+               "p_zero_copy": Pv is not None}
 
     variants = None
     if rank == 0 and world == 1 and not args.no_variants:

@@ -83,6 +83,16 @@ const char* dspark_version(void);
  */
 int dspark_workspace_status(void* ws, void* stream);
 
+/*
+ * The device-accessible address of a pinned (page-locked) host buffer, so
+ * that kernels read it in place over the host link (zero copy).  The input
+ * arrays of the calls below may be such addresses: verification, for
+ * example, then fetches only the target rows its decisions need.  Returns
+ * DSPARK_ERR_CUDA (and *device = NULL) for memory that is not pinned and
+ * mapped.  Host-side only; nothing is enqueued.
+ */
+int dspark_host_pointer(const void* host, void** device);
+
 /* ------------------------------------------------------------------ draft */
 
 /*

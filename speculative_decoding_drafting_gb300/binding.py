@@ -56,6 +56,8 @@ def load(build_if_missing: bool = True):
         L.dspark_strerror.restype = ctypes.c_char_p
         L.dspark_version.restype = ctypes.c_char_p
         L.dspark_workspace_status.argtypes = [P, P]
+        L.dspark_host_pointer.argtypes = [P, P]
+        L.dspark_host_pointer.restype = i32
         L.dspark_draft_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.dspark_draft_workspace_size.restype = sz
         L.dspark_draft_markov.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, u64, P, f32,
@@ -91,6 +93,40 @@ def load(build_if_missing: bool = True):
             getattr(L, name).restype = i32
         _lib = L
         return _lib
+
+
+class DeviceView:
+    """A device-accessible address with a shape and a dtype, passed where the
+    calls take a CUDA tensor: for example a pinned host buffer read in place
+    (``host_view``)."""
+
+    is_cuda = True
+
+    def __init__(self, ptr: int, shape, dtype, device, owner=None):
+        self.ptr, self.shape, self.dtype, self.device, self.owner = int(ptr), tuple(shape), dtype, device, owner
+
+    def data_ptr(self) -> int:
+        return self.ptr
+
+    def is_contiguous(self) -> bool:
+        return True
+
+    def numel(self) -> int:
+        n = 1
+        for d in self.shape:
+            n *= d
+        return n
+
+
+def host_view(t: torch.Tensor, device) -> DeviceView:
+    """A pinned host tensor as a DeviceView its kernels read in place
+    (``dspark_host_pointer``); raises if the memory is not pinned and mapped."""
+    if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+        raise ValueError("host_view takes a contiguous pinned host tensor")
+    out = ctypes.c_void_p()
+    code = load().dspark_host_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(out))
+    _check("dspark_host_pointer", code)
+    return DeviceView(out.value, t.shape, t.dtype, device, owner=t)
 
 
 def _p(t: Optional[torch.Tensor]):

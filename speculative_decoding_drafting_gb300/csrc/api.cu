@@ -68,6 +68,17 @@ const char* dspark_strerror(int status) {
 
 const char* dspark_version(void) { return "dspark-gb300 0.1 (sm_103a)"; }
 
+int dspark_host_pointer(const void* host, void** device) {
+    if (!host || !device) return DSPARK_ERR_INVALID_ARG;
+    *device = nullptr;
+    if (cudaHostGetDevicePointer(device, const_cast<void*>(host), 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        *device = nullptr;
+        return DSPARK_ERR_CUDA;
+    }
+    return DSPARK_OK;
+}
+
 int dspark_workspace_status(void* ws, void* stream) {
     if (!ws) return DSPARK_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -217,3 +217,20 @@ def test_schedule_async_two_steps_back_ring():
         hist.append(ns)
         np.testing.assert_array_equal(host(out["verify_len"]), L, err_msg=f"step {t}")
         assert int(host(ring[t % 3])[0]) == ns
+
+
+def test_verify_reads_host_resident_targets_in_place():
+    """P in pinned host memory, read in place through dspark_host_pointer:
+    every output equal to the run with P on the device."""
+    w = synth.Workload("zc", R=6, gamma=4, V=20488, r=64, T=1.0)
+    x = synth.gen_all(w)
+    dr = oracle_draft(w, x, 21)
+    draft = dict(tokens=dev(dr["tokens"].astype(np.int32)), q_tok=dev(dr["qx"].astype(np.float32)),
+                 lse=dev(dr["lse"].astype(np.float64)), code=dev(dr["code"].astype(np.float32)))
+    hP = torch.from_numpy(np.ascontiguousarray(x["P"])).pin_memory()
+    Pv = binding.host_view(hP, torch.device("cuda:0"))
+    a = binding.verify(dev(x["P"]), dev(x["U"]), dev(x["W2"]), draft, w.T, 21)
+    b = binding.verify(Pv, dev(x["U"]), dev(x["W2"]), draft, w.T, 21)
+    torch.cuda.synchronize()
+    for k in ("out_tokens", "accept_len", "n_out", "p_tok", "lse_p"):
+        np.testing.assert_array_equal(host(a[k]), host(b[k]), err_msg=k)
