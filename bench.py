@@ -553,6 +553,7 @@ def main(argv=None):
             Pv = binding.host_view(hP, devc)
         except Exception:                                   # not mapped: copy P as well
             Pv = None
+        stage = P if Pv is not None else None             # device rows of P, filled by verification's pass 1
         bufs = [dict(U=U, P=Pv if Pv is not None else P, anchor=anchor, c=c),
                 dict(U=torch.empty_like(U), P=Pv if Pv is not None else torch.empty_like(P),
                      anchor=torch.empty_like(anchor), c=torch.empty_like(c))]
@@ -573,7 +574,8 @@ def main(argv=None):
         def step_on(b, seed):
             d = binding.draft_markov(b["U"], b["anchor"], W1, W2, w.T, seed, req_ids=rid, ws=wss[0])
             s_ = binding.schedule(b["c"], sps, ws=wss[1])
-            v = binding.verify(b["P"], b["U"], W2, d, w.T, seed, verify_len=None, req_ids=rid, ws=wss[2])
+            v = binding.verify(b["P"], b["U"], W2, d, w.T, seed, verify_len=None, req_ids=rid, ws=wss[2],
+                               p_stage=stage)
             return d, s_, v
 
         def pipeline(n, seed0, keep):
@@ -606,17 +608,15 @@ def main(argv=None):
             p_bytes = float(hP.numel() * hP.element_size())
         else:
             # target bytes fetched: the rows of every window up to the one that
-            # decided each request, the residual's rejecting rows again, the
-            # sampler's chunk of each sampled row (256 or 1024 values)
+            # decided each request (the later passes read the device copy pass 1
+            # made of them)
             sp_ = hP.element_size()
             G1 = w.gamma + 1
             per = []
             for hn in h_n:
                 dec = hn.numpy().astype(np.int64) - 1                 # decision row = accept_len
                 hi = np.where(dec < 1, 1, np.where(dec < 3, 3, np.where(dec < 7, 7, G1)))
-                rows = np.minimum(hi, G1).sum()
-                rej = int((dec < w.gamma).sum())
-                per.append((rows + rej) * w.V * sp_ + rej * 256 * sp_ + (w.R - rej) * 1024 * sp_)
+                per.append(np.minimum(hi, G1).sum() * w.V * sp_)
             p_bytes = float(np.mean(per))
         h2d = int(copied + p_bytes)
         d2h = int(h_out.numel() * 4 + h_n[0].numel() * 4)
@@ -627,7 +627,8 @@ def main(argv=None):
                "steps": len(e2e_ms),
                "inputs": ("U, anchors, c copied from pinned host memory on a second stream, double-buffered (the copy "
                           "of step i + 1 overlaps step i); P read in place from pinned host memory, only the rows "
-                          "verification needs (h2d_bytes_per_step counts the bytes fetched)" if Pv is not None else
+                          "verification needs, each once: pass 1 copies them to a device staging buffer for the later "
+                          "passes (h2d_bytes_per_step counts the bytes fetched)" if Pv is not None else
                           "U, P, anchors, c copied from pinned host memory on a second stream, double-buffered"),
                "p_zero_copy": Pv is not None}
 

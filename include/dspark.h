@@ -253,6 +253,24 @@ int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype,
                   void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dspark_verify with a staging buffer for P, for targets read in place from
+ * host memory (dspark_host_pointer): pass 1 copies every target row it reads
+ * into p_stage, a device array of P's shape and dtype, and the passes after it
+ * (acceptance, residual, sampling) read the target rows there, so each needed
+ * byte crosses the host link once.  p_stage may be NULL (the same as
+ * dspark_verify).  Rows verification does not read are left untouched.
+ */
+int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype,
+                         const void* W2, int w_dtype,
+                         const int32_t* tokens, const float* q_tok, const double* lse,
+                         const float* code, const int32_t* verify_len,
+                         int R, int gamma, int V, int r,
+                         uint64_t seed, const uint32_t* req_ids, float temperature,
+                         int32_t* out_tokens, int32_t* accept_len, int32_t* n_out,
+                         float* p_tok, double* lse_p, void* p_stage,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
  * dspark_verify_noalloc -- dspark_verify for callers that cannot allocate
  * device memory (no counterpart on the pages: it changes where scratch lives,
  * not what is computed).  Some callers are handed only their input and output

@@ -68,6 +68,8 @@ def load(build_if_missing: bool = True):
         L.dspark_verify_workspace_size.restype = sz
         L.dspark_verify.argtypes = [P, i32, P, i32, P, i32, P, P, P, P, P, i32, i32, i32, i32, u64, P, f32,
                                     P, P, P, P, P, P, sz, P]
+        L.dspark_verify_staged.argtypes = [P, i32, P, i32, P, i32, P, P, P, P, P, i32, i32, i32, i32, u64, P, f32,
+                                           P, P, P, P, P, P, P, sz, P]
         L.dspark_schedule_workspace_size.argtypes = [i32, i32]
         L.dspark_schedule_workspace_size.restype = sz
         L.dspark_draft_markov_conf.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, u64, P, f32,
@@ -86,7 +88,8 @@ def load(build_if_missing: bool = True):
         L.dspark_profile_kernel_name.argtypes = [i32]
         L.dspark_profile_kernel_name.restype = ctypes.c_char_p
         for name in ("dspark_draft_markov", "dspark_draft_rnn", "dspark_draft_markov_conf", "dspark_draft_rnn_conf",
-                     "dspark_verify", "dspark_schedule", "dspark_schedule_async", "dspark_schedule_threshold",
+                     "dspark_verify", "dspark_verify_staged", "dspark_schedule", "dspark_schedule_async",
+                     "dspark_schedule_threshold",
                      "dspark_sts_fit",
                      "dspark_sts_apply",
                      "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
@@ -265,8 +268,10 @@ def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids
 
 
 def verify(P, U, W2, draft, temperature: float, seed: int, verify_len=None, req_ids=None, ws=None, out=None,
-           stream=None):
-    """Rejection-sampling verification (``dspark_verify``); ``draft`` is a draft output dict."""
+           stream=None, p_stage=None):
+    """Rejection-sampling verification (``dspark_verify``); ``draft`` is a draft output dict.
+    ``p_stage`` (a device tensor of P's shape and dtype) receives the target
+    rows pass 1 reads, for the later passes (``dspark_verify_staged``)."""
     L = load()
     R, G1, V = P.shape
     gamma = G1 - 1
@@ -281,11 +286,12 @@ def verify(P, U, W2, draft, temperature: float, seed: int, verify_len=None, req_
     nbytes = L.dspark_verify_workspace_size(R, gamma, V, r)
     if ws is None:
         ws = _workspace(nbytes, dev)
-    code = L.dspark_verify(_p(P), _dt(P), _p(U), _dt(U), _p(W2), _dt(W2), _p(draft["tokens"]),
-                           _p(draft["q_tok"]), _p(draft["lse"]), _p(draft["code"]), _p(verify_len),
-                           R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
-                           _p(out["out_tokens"]), _p(out["accept_len"]), _p(out["n_out"]),
-                           _p(out.get("p_tok")), _p(out.get("lse_p")), _p(ws), ws.numel(), _stream(stream))
+    code = L.dspark_verify_staged(_p(P), _dt(P), _p(U), _dt(U), _p(W2), _dt(W2), _p(draft["tokens"]),
+                                  _p(draft["q_tok"]), _p(draft["lse"]), _p(draft["code"]), _p(verify_len),
+                                  R, gamma, V, r, int(seed) & 0xFFFFFFFFFFFFFFFF, _p(req_ids), float(temperature),
+                                  _p(out["out_tokens"]), _p(out["accept_len"]), _p(out["n_out"]),
+                                  _p(out.get("p_tok")), _p(out.get("lse_p")), _p(p_stage), _p(ws), ws.numel(),
+                                  _stream(stream))
     _check("dspark_verify", code)
     out["ws"] = ws
     return out

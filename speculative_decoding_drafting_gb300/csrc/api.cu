@@ -187,11 +187,12 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int r) {
     return verify_workspace_bytes(R, gamma, V, r);
 }
 
-int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype, const void* W2, int w_dtype,
-                  const int32_t* tokens, const float* q_tok, const double* lse, const float* code,
-                  const int32_t* verify_len, int R, int gamma, int V, int r, uint64_t seed,
-                  const uint32_t* req_ids, float temperature, int32_t* out_tokens, int32_t* accept_len,
-                  int32_t* n_out, float* p_tok, double* lse_p, void* ws, size_t ws_bytes, void* stream) {
+int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype, const void* W2, int w_dtype,
+                         const int32_t* tokens, const float* q_tok, const double* lse, const float* code,
+                         const int32_t* verify_len, int R, int gamma, int V, int r, uint64_t seed,
+                         const uint32_t* req_ids, float temperature, int32_t* out_tokens, int32_t* accept_len,
+                         int32_t* n_out, float* p_tok, double* lse_p, void* p_stage, void* ws, size_t ws_bytes,
+                         void* stream) {
     if (!dtype_ok(p_dtype)) return DSPARK_ERR_UNSUPPORTED_DTYPE;
     int st = check_common(R, gamma, V, r, temperature, u_dtype, w_dtype);
     if (st) return st;
@@ -208,9 +209,21 @@ int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype, const 
     a.R = R; a.gamma = gamma; a.V = V; a.r = r; a.seed = seed; a.req_ids = req_ids; a.T = temperature;
     a.out_tokens = out_tokens; a.accept_len = accept_len; a.n_out = n_out; a.p_tok = p_tok; a.lse_p = lse_p;
     a.ws = ws;
+    a.P_stage = p_stage;
+    a.Pv = p_stage ? p_stage : P;
     st = verify_carve(a, ws_bytes);
     if (st) return st;
     return cuda_status(launch_verify(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype, const void* W2, int w_dtype,
+                  const int32_t* tokens, const float* q_tok, const double* lse, const float* code,
+                  const int32_t* verify_len, int R, int gamma, int V, int r, uint64_t seed,
+                  const uint32_t* req_ids, float temperature, int32_t* out_tokens, int32_t* accept_len,
+                  int32_t* n_out, float* p_tok, double* lse_p, void* ws, size_t ws_bytes, void* stream) {
+    return dspark_verify_staged(P, p_dtype, U, u_dtype, W2, w_dtype, tokens, q_tok, lse, code, verify_len, R, gamma,
+                                V, r, seed, req_ids, temperature, out_tokens, accept_len, n_out, p_tok, lse_p,
+                                nullptr, ws, ws_bytes, stream);
 }
 
 size_t dspark_schedule_workspace_size(int R, int gamma) {

@@ -206,6 +206,23 @@ __device__ __forceinline__ float4 load4_stream<DSPARK_BF16>(const void* base, si
                        bf16_bits_to_float(v.y & 0xFFFFu), bf16_bits_to_float(v.y >> 16));
 }
 
+// Store 4 values at element i of an array of type DT (bf16 values that came
+// from bf16 storage are stored back exactly).
+template <int DT>
+__device__ __forceinline__ void store4(void* base, size_t i, float4 v);
+template <>
+__device__ __forceinline__ void store4<DSPARK_F32>(void* base, size_t i, float4 v) {
+    *reinterpret_cast<float4*>(static_cast<float*>(base) + i) = v;
+}
+template <>
+__device__ __forceinline__ void store4<DSPARK_BF16>(void* base, size_t i, float4 v) {
+    const uint32_t a = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+    const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(base) + i) = make_uint2(a, b);
+}
+
 // 8 consecutive elements starting at i (a multiple of 8 for bf16, of 4 for
 // f32); `avail` = how many of them exist (elements past it read as 0).
 template <int DT>

@@ -62,6 +62,8 @@ struct DraftArgs {
 struct VerifyArgs {
     const void* P;
     int p_dtype;
+    void* P_stage;      // optional device copy of P that pass 1 fills with the rows it reads
+    const void* Pv;     // where the passes after pass 1 read P: P_stage, or P itself
     const void* U;
     int u_dtype;
     const void* W2;

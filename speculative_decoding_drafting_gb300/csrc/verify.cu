@@ -68,7 +68,9 @@ __device__ __forceinline__ int live_request(const VerifyArgs& A, int w, int i) {
 
 // ------------------------------------------------------------------ pass 1
 // Warp tasks over (live request, row of the window, 1024-column chunk).
-template <int PT, bool GREEDY>
+// STAGE: also copy each row read into A.P_stage (P is host memory, and the
+// later passes read the rows from there instead of across the link again).
+template <int PT, bool GREEDY, bool STAGE>
 __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
     pdl_launch_dependents();
     pdl_wait();   // the list of live requests (waves after the first)
@@ -98,6 +100,15 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
             x[4 * i + 1] = v.y;
             x[4 * i + 2] = v.z;
             x[4 * i + 3] = v.w;
+        }
+        if (STAGE) {
+            // stored after all eight loads are issued: the staging buffer
+            // might alias P as far as the compiler knows
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (ok[i])
+                    store4<PT>(A.P_stage, base + c0 + 4 * lane + 128 * i,
+                               make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
         }
         float2 out;
         if (GREEDY) {
@@ -188,7 +199,7 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
             x = 0;
         }
         s_x[row] = x;
-        if (!GREEDY) s_px[row] = ld_elem(A.P, PT, ((size_t)r * G1 + row) * (size_t)V + x);
+        if (!GREEDY) s_px[row] = ld_elem(A.Pv, PT, ((size_t)r * G1 + row) * (size_t)V + x);
     }
     const float2* parts = A.vparts + (size_t)r * G1 * NCH;
     for (int row = lo + warp; row <= rhi; row += blockDim.x >> 5) {
@@ -352,7 +363,7 @@ __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
             const float lq_hi = (float)lq, lq_lo = (float)(lq - (double)lq_hi);
             const float lp_hi = (float)lp, lp_lo = (float)(lp - (double)lp_hi);
             const float4 u4 = load4<UT>(A.U, ((size_t)r * A.gamma + (j - 1)) * V + c);
-            const float4 p4 = load4<PT>(A.P, ((size_t)r * G1 + (j - 1)) * V + c);
+            const float4 p4 = load4<PT>(A.Pv, ((size_t)r * G1 + (j - 1)) * V + c);
             const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
             const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
@@ -492,7 +503,7 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     for (int t = 0; t < 4; ++t) {
         const int i = tid + t * 256;
         const int v = (chunk << clog) + i;
-        pvals[t] = (i < nleaf && v < V) ? ld_elem(A.P, PT, ((size_t)r * G1 + (pos - 1)) * V + v) : 0.f;
+        pvals[t] = (i < nleaf && v < V) ? ld_elem(A.Pv, PT, ((size_t)r * G1 + (pos - 1)) * V + v) : 0.f;
     }
     if (!use_p && tid < nleaf && (chunk << clog) + tid < V)
         uval = ld_elem(A.U, UT, ((size_t)r * A.gamma + (pos - 1)) * V + (chunk << clog) + tid);
@@ -618,8 +629,12 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
         int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
         if (grid < 1) grid = 1;
         prof_begin(kPVerifyPass1, s);
-        e = greedy ? launch_kernel(verify_pass1<PT, true>, dim3(grid), dim3(256), 0, s, w > 1, a, w)
-                   : launch_kernel(verify_pass1<PT, false>, dim3(grid), dim3(256), 0, s, w > 1, a, w);
+        if (a.P_stage)
+            e = greedy ? launch_kernel(verify_pass1<PT, true, true>, dim3(grid), dim3(256), 0, s, w > 1, a, w)
+                       : launch_kernel(verify_pass1<PT, false, true>, dim3(grid), dim3(256), 0, s, w > 1, a, w);
+        else
+            e = greedy ? launch_kernel(verify_pass1<PT, true, false>, dim3(grid), dim3(256), 0, s, w > 1, a, w)
+                       : launch_kernel(verify_pass1<PT, false, false>, dim3(grid), dim3(256), 0, s, w > 1, a, w);
         prof_end(s);
         if (e != cudaSuccess) return e;
         prof_begin(kPVerifyAccept, s);

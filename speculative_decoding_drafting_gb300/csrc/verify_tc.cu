@@ -484,7 +484,7 @@ cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     p.a_res = a.a_res;
     p.a_plane = ((a.R + kBM - 1) / kBM) * kBM * a.r;
     p.U = a.U;
-    p.P = a.P;
+    p.P = a.Pv;
     p.rej_count = a.rej_count;
     p.rej_list = a.rej_list;
     p.vstate = a.vstate;

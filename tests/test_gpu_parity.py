@@ -234,3 +234,26 @@ def test_verify_reads_host_resident_targets_in_place():
     torch.cuda.synchronize()
     for k in ("out_tokens", "accept_len", "n_out", "p_tok", "lse_p"):
         np.testing.assert_array_equal(host(a[k]), host(b[k]), err_msg=k)
+
+
+def test_verify_staged_host_targets():
+    """P read in place from pinned host memory with a device staging buffer:
+    every output equal to the run with P on the device, and the staged rows
+    equal to P where verification read them."""
+    w = synth.Workload("zcs", R=6, gamma=4, V=20488, r=64, T=1.0)
+    x = synth.gen_all(w)
+    dr = oracle_draft(w, x, 23)
+    draft = dict(tokens=dev(dr["tokens"].astype(np.int32)), q_tok=dev(dr["qx"].astype(np.float32)),
+                 lse=dev(dr["lse"].astype(np.float64)), code=dev(dr["code"].astype(np.float32)))
+    hP = torch.from_numpy(np.ascontiguousarray(x["P"])).pin_memory()
+    Pv = binding.host_view(hP, torch.device("cuda:0"))
+    stage = torch.full(hP.shape, float("nan"), dtype=torch.float32, device="cuda:0")
+    a = binding.verify(dev(x["P"]), dev(x["U"]), dev(x["W2"]), draft, w.T, 23)
+    b = binding.verify(Pv, dev(x["U"]), dev(x["W2"]), draft, w.T, 23, p_stage=stage)
+    torch.cuda.synchronize()
+    for k in ("out_tokens", "accept_len", "n_out", "p_tok", "lse_p"):
+        np.testing.assert_array_equal(host(a[k]), host(b[k]), err_msg=k)
+    st = host(stage)
+    for r in range(w.R):
+        d = int(host(b["accept_len"])[r])
+        np.testing.assert_array_equal(st[r, d], x["P"][r, d])     # the decision row was staged
