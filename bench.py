@@ -607,16 +607,11 @@ def main(argv=None):
         if Pv is None:
             p_bytes = float(hP.numel() * hP.element_size())
         else:
-            # target bytes fetched: the rows of every window up to the one that
-            # decided each request (the later passes read the device copy pass 1
-            # made of them)
+            # target bytes fetched: with a staging buffer verification reads one
+            # row per wave, so exactly rows 0 .. accept_len of each request
+            # (n_out rows); the later passes read the device copy pass 1 made
             sp_ = hP.element_size()
-            G1 = w.gamma + 1
-            per = []
-            for hn in h_n:
-                dec = hn.numpy().astype(np.int64) - 1                 # decision row = accept_len
-                hi = np.where(dec < 1, 1, np.where(dec < 3, 3, np.where(dec < 7, 7, G1)))
-                per.append(np.minimum(hi, G1).sum() * w.V * sp_)
+            per = [int(hn.numpy().astype(np.int64).sum()) * w.V * sp_ for hn in h_n]
             p_bytes = float(np.mean(per))
         h2d = int(copied + p_bytes)
         d2h = int(h_out.numel() * 4 + h_n[0].numel() * 4)
@@ -627,8 +622,8 @@ def main(argv=None):
                "steps": len(e2e_ms),
                "inputs": ("U, anchors, c copied from pinned host memory on a second stream, double-buffered (the copy "
                           "of step i + 1 overlaps step i); P read in place from pinned host memory, only the rows "
-                          "verification needs, each once: pass 1 copies them to a device staging buffer for the later "
-                          "passes (h2d_bytes_per_step counts the bytes fetched)" if Pv is not None else
+                          "verification needs (one row per wave), each once: pass 1 copies them to a device staging "
+                          "buffer for the later passes (h2d_bytes_per_step counts the bytes fetched)" if Pv is not None else
                           "U, P, anchors, c copied from pinned host memory on a second stream, double-buffered"),
                "p_zero_copy": Pv is not None}
 

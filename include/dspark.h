@@ -257,8 +257,12 @@ int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype,
  * host memory (dspark_host_pointer): pass 1 copies every target row it reads
  * into p_stage, a device array of P's shape and dtype, and the passes after it
  * (acceptance, residual, sampling) read the target rows there, so each needed
- * byte crosses the host link once.  p_stage may be NULL (the same as
- * dspark_verify).  Rows verification does not read are left untouched.
+ * byte crosses the host link once.  With p_stage the windows are one row each
+ * ([k, k + 1)), so a request reads exactly rows 0 .. accept_len: p_tok holds
+ * positions 1 .. min(accept_len + 1, l_r) and lse_p rows 0 .. accept_len, NaN
+ * elsewhere; the tokens and lengths are those of dspark_verify.  p_stage may be
+ * NULL (the same as dspark_verify).  Rows verification does not read are left
+ * untouched.
  */
 int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype,
                          const void* W2, int w_dtype,

@@ -63,6 +63,7 @@ struct VerifyArgs {
     const void* P;
     int p_dtype;
     void* P_stage;      // optional device copy of P that pass 1 fills with the rows it reads
+    int unit_waves;     // 1: one target row per verification wave (set with P_stage)
     const void* Pv;     // where the passes after pass 1 read P: P_stage, or P itself
     const void* U;
     int u_dtype;

@@ -51,13 +51,24 @@ __device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
 // requests still live (all of them in wave 1); its pass 1 streams those rows,
 // its acceptance pass decides every live request on them and lists the ones
 // that passed the whole window for the next wave.
-// Windows [0, 1), [1, 3), [3, 7), [7, gamma + 1) (of the edge sets timed on
-// the 256-request, gamma = 5 workload, the fastest: fewer rows read than
-// wider first windows, fewer launches than a window per row).
-__host__ __device__ __forceinline__ int wave_lo(int w) { return w <= 1 ? 0 : (w == 2 ? 1 : (w == 3 ? 3 : 7)); }
-__host__ __device__ __forceinline__ int wave_hi(int w, int G1) {
-    const int e = w <= 1 ? 1 : (w == 2 ? 3 : (w == 3 ? 7 : G1));
+// Windows [0, 1), [1, 3), [3, 7), [7, gamma + 1) for P in device memory (of
+// the edge sets timed on the 256-request, gamma = 5 workload, the fastest:
+// fewer rows read than wider first windows, fewer launches than a window per
+// row).  With P in host memory every row read crosses the host link, which
+// bounds the call, so there each wave is one row: [w - 1, w), and only the
+// rows the decisions need are read.
+__host__ __device__ __forceinline__ int wave_lo(int w, bool unit) {
+    if (unit) return w - 1;
+    return w <= 1 ? 0 : (w == 2 ? 1 : (w == 3 ? 3 : 7));
+}
+__host__ __device__ __forceinline__ int wave_hi(int w, int G1, bool unit) {
+    const int e = unit ? w : (w <= 1 ? 1 : (w == 2 ? 3 : (w == 3 ? 7 : G1)));
     return e < G1 ? e : G1;
+}
+__host__ __device__ __forceinline__ int wave_count(int G1, bool unit) {
+    int n = 0;
+    while (n < (unit ? G1 : 4) && wave_lo(n + 1, unit) < G1) ++n;
+    return n;
 }
 __host__ __device__ __forceinline__ int live_count(const VerifyArgs& A, int w) {
     return w == 1 ? A.R : A.wcount_alive[w];
@@ -77,7 +88,7 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
     const int lane = threadIdx.x & 31;
     const int warps_total = gridDim.x * (blockDim.x >> 5);
     const int V = A.V, G1 = A.gamma + 1, NCH = A.nch;
-    const int lo = wave_lo(w), nrow = wave_hi(w, G1) - lo;
+    const int lo = wave_lo(w, A.unit_waves), nrow = wave_hi(w, G1, A.unit_waves) - lo;
     const long long tasks = (long long)live_count(A, w) * nrow * NCH;
     const float invT = GREEDY ? 1.f : 1.f / A.T;
     for (long long task = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks;
@@ -178,7 +189,7 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
     const int r = live_request(A, w, blockIdx.x);
     const int G1 = A.gamma + 1, NCH = A.nch, V = A.V;
     const int L = verify_len_of(A, r);
-    const int lo = wave_lo(w), hi = wave_hi(w, G1);
+    const int lo = wave_lo(w, A.unit_waves), hi = wave_hi(w, G1, A.unit_waves);
     const int rhi = min(hi - 1, L);        // the window's rows this request needs: lo .. rhi
     const int npos = min(hi, L) - lo;      // positions lo + 1 .. lo + npos are tested
     const float invT = GREEDY ? 1.f : 1.f / A.T;
@@ -568,6 +579,9 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
 
 // ------------------------------------------------------------------ host
 static int nch_of(int V) { return (V + kChunk - 1) / kChunk; }
+// rej_count (+0), vflags (+16), live requests per wave (+32: gamma + 2 ints)
+constexpr size_t kCounterBytes = 512;
+static_assert(32 + 4 * (64 + 2) <= kCounterBytes, "wave counters");
 static int nch256_of(int V) { return (V + kRChunk - 1) / kRChunk; }
 
 size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
@@ -577,7 +591,7 @@ size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
     off = align_up(off + (size_t)R * G1 * sizeof(double), 256);         // lse of P rows
     off = align_up(off + (size_t)R * sizeof(int2), 256);                // vstate
     off = align_up(off + (size_t)R * N2 * 4 * sizeof(float), 256);      // rpart
-    off = align_up(off + 256, 256);                                      // counters, flags
+    off = align_up(off + kCounterBytes, 256);                            // counters, flags
     off = align_up(off + (size_t)R * sizeof(int), 256);                 // rej_list
     off = align_up(off + 2ull * R * sizeof(int), 256);                  // live requests of the waves
     const size_t rpad = (size_t)((R + 127) / 128) * 128;
@@ -600,12 +614,12 @@ int verify_carve(VerifyArgs& a, size_t ws_bytes) {
     off = align_up(off + (size_t)a.R * sizeof(int2), 256);
     a.rpart = reinterpret_cast<float*>(base + off);
     off = align_up(off + (size_t)a.R * N2 * 4 * sizeof(float), 256);
-    // counters cleared before each verification (one 256-byte block):
-    // rejection count, flags, live requests per wave
+    // counters cleared before each verification (one block): rejection
+    // count, flags, live requests per wave (up to gamma + 2 <= 66 entries)
     a.rej_count = reinterpret_cast<int*>(base + off);
     a.vflags = reinterpret_cast<uint32_t*>(base + off + 16);
     a.wcount_alive = reinterpret_cast<int*>(base + off + 32);
-    off = align_up(off + 256, 256);
+    off = align_up(off + kCounterBytes, 256);
     a.rej_list = reinterpret_cast<int*>(base + off);
     off = align_up(off + (size_t)a.R * sizeof(int), 256);
     a.alive = reinterpret_cast<int*>(base + off);
@@ -619,12 +633,15 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     const bool greedy = !(a.T > 0.f);
     const int nsm = num_sms();
     const int G1 = a.gamma + 1;
-    cudaError_t e = cudaMemsetAsync(a.rej_count, 0, 256, s);
+    cudaError_t e = cudaMemsetAsync(a.rej_count, 0, kCounterBytes, s);
     if (e != cudaSuccess) return e;
+    a.unit_waves = a.P_stage ? 1 : 0;
+    const bool unit = a.unit_waves != 0;
     // the waves: the first pass 1 waits for the caller's work (and the
     // cleared counters); every later launch overlaps the previous kernel's tail
-    for (int w = 1; w <= 4 && wave_lo(w) < G1; ++w) {
-        const long long tasks = (long long)a.R * (wave_hi(w, G1) - wave_lo(w)) * a.nch;
+    const int nw = wave_count(G1, unit);
+    for (int w = 1; w <= nw; ++w) {
+        const long long tasks = (long long)a.R * (wave_hi(w, G1, unit) - wave_lo(w, unit)) * a.nch;
         const long long want = (tasks + 7) / 8;
         int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
         if (grid < 1) grid = 1;

@@ -236,11 +236,14 @@ def test_verify_reads_host_resident_targets_in_place():
         np.testing.assert_array_equal(host(a[k]), host(b[k]), err_msg=k)
 
 
-def test_verify_staged_host_targets():
-    """P read in place from pinned host memory with a device staging buffer:
-    every output equal to the run with P on the device, and the staged rows
-    equal to P where verification read them."""
-    w = synth.Workload("zcs", R=6, gamma=4, V=20488, r=64, T=1.0)
+@pytest.mark.parametrize("gamma,T,V", [(4, 1.0, 20488), (16, 0.0, 8200), (64, 1.0, 4104)])
+def test_verify_staged_host_targets(gamma, T, V):
+    """P read in place from pinned host memory with a device staging buffer
+    (one target row per wave, up to gamma + 1 waves): tokens and lengths
+    equal to the run with P on the device, p_tok / lse_p equal where the
+    decision read them and NaN elsewhere, and the staged rows equal to P
+    where verification read them."""
+    w = synth.Workload("zcs", R=6, gamma=gamma, V=V, r=64, T=T)
     x = synth.gen_all(w)
     dr = oracle_draft(w, x, 23)
     draft = dict(tokens=dev(dr["tokens"].astype(np.int32)), q_tok=dev(dr["qx"].astype(np.float32)),
@@ -251,8 +254,17 @@ def test_verify_staged_host_targets():
     a = binding.verify(dev(x["P"]), dev(x["U"]), dev(x["W2"]), draft, w.T, 23)
     b = binding.verify(Pv, dev(x["U"]), dev(x["W2"]), draft, w.T, 23, p_stage=stage)
     torch.cuda.synchronize()
-    for k in ("out_tokens", "accept_len", "n_out", "p_tok", "lse_p"):
+    for k in ("out_tokens", "accept_len", "n_out"):
         np.testing.assert_array_equal(host(a[k]), host(b[k]), err_msg=k)
+    # one row per wave: exactly the rows and positions the decision used
+    acc = host(b["accept_len"])
+    for r in range(w.R):
+        d = int(acc[r])
+        np.testing.assert_array_equal(host(b["lse_p"])[r, :d + 1], host(a["lse_p"])[r, :d + 1])
+        assert np.isnan(host(b["lse_p"])[r, d + 1:]).all()
+        npos = min(d + 1, w.gamma)
+        np.testing.assert_array_equal(host(b["p_tok"])[r, :npos], host(a["p_tok"])[r, :npos])
+        assert np.isnan(host(b["p_tok"])[r, npos:]).all()
     st = host(stage)
     for r in range(w.R):
         d = int(host(b["accept_len"])[r])
