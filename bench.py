@@ -66,7 +66,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples go to DSPARK_CLOCKS_DIR (default: the temp directory)
+        import tempfile
+        d = os.environ.get("DSPARK_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:

@@ -9,7 +9,7 @@ import torch
 import oracle
 from speculative_decoding_drafting_gb300 import binding, synth
 
-# the benchmark spec tolerances
+# parity tolerances for the floating-point outputs and the flagging margins
 REL_TOL = 1e-4          # q(x), p(x), logsumexp
 GUMBEL_FLAG = 1e-4      # Gumbel-max (or greedy argmax) margin below which a draft token is flagged
 UNIFORM_FLAG = 1e-6     # a uniform this close to its threshold is flagged
