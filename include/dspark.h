@@ -30,6 +30,10 @@
  *  - Work is enqueued asynchronously on the caller's stream `stream`
  *    (a cudaStream_t passed as void*; NULL = legacy default stream).
  *  - dtype arguments take DSPARK_F32 or DSPARK_BF16 (bf16 = IEEE bfloat16).
+ *  - U, P (and dspark_verify_staged's staging buffer), W2 and Wgco are read
+ *    with 16-byte loads and tensor-map copies: they must start on a 16-byte
+ *    boundary, else the call returns DSPARK_ERR_INVALID_ARG (cudaMalloc and
+ *    PyTorch allocations always do; an offset view may not).
  *  - The return value is DSPARK_OK or a negative DSPARK_ERR_* code.  Host
  *    checks (null pointers, sizes, dtypes, workspace size) fail before any
  *    work is enqueued.  Conditions that only the device can see (a token id

@@ -25,6 +25,9 @@ int num_sms() {
 }
 
 static bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+// U, P (and its staging copy), W2 and Wgco are read with 16-byte loads and
+// tensor-map copies: they must start on a 16-byte boundary
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool dtype_ok(int dt) { return dt == DSPARK_F32 || dt == DSPARK_BF16; }
 
 static int check_vocab(int V, int dt) {
@@ -130,6 +133,7 @@ static int draft_entry(DraftArgs& a, bool rnn, size_t ws_bytes, void* stream) {
     if (rnn && (!a.Wgco || !a.H || a.d < 1 || a.d > 16384)) return rnn && (a.d < 1 || a.d > 16384)
                                                                       ? DSPARK_ERR_SHAPE
                                                                       : DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(a.U) || !aligned16(a.W2) || (rnn && !aligned16(a.Wgco))) return DSPARK_ERR_INVALID_ARG;
     if (!a.ws || !aligned256(a.ws)) return DSPARK_ERR_WORKSPACE;
     st = draft_carve(a, ws_bytes);
     if (st) return st;
@@ -201,6 +205,8 @@ int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype,
     if (temperature > 0.f && V > (1 << 18)) return DSPARK_ERR_SHAPE;   // the sampling tree's top level
     if (!P || !tokens || !out_tokens || !accept_len || !n_out) return DSPARK_ERR_INVALID_ARG;
     if (temperature > 0.f && (!U || !W2 || !q_tok || !lse || !code)) return DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(P) || (p_stage && !aligned16(p_stage))) return DSPARK_ERR_INVALID_ARG;
+    if (temperature > 0.f && (!aligned16(U) || !aligned16(W2))) return DSPARK_ERR_INVALID_ARG;
     if (!ws || !aligned256(ws)) return DSPARK_ERR_WORKSPACE;
     VerifyArgs a;
     std::memset(&a, 0, sizeof a);

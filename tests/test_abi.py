@@ -123,3 +123,29 @@ def test_schedule_async_arguments_rejected_on_the_host():
     assert L.dspark_schedule_async(fake, fake, 10, 4, 5, null, fake, fake, fake, fake, 1 << 12, null) == -1
     assert L.dspark_schedule_async(fake, fake, 10, 1000, 16, fake, fake, fake, fake, fake, 1 << 12, null) == -3
     assert L.dspark_schedule_async(fake, fake, 10, 4, 5, fake, fake, fake, fake, null, 1 << 12, null) == -8
+
+
+def test_misaligned_streamed_arrays_rejected_on_the_host():
+    """U, P, the staging buffer, W2 and Wgco feed 16-byte loads and tensor-map
+    copies: a pointer off a 16-byte boundary fails before anything runs."""
+    L = binding.load()
+    null = None
+    ok = ctypes.c_void_p(1 << 20)            # 16- and 256-byte aligned; never dereferenced
+    off = ctypes.c_void_p((1 << 20) + 4)
+
+    def verify(P, U, W2, T, stage=None):
+        return L.dspark_verify_staged(P, 0, U, 0, W2, 1, ok, ok, ok, ok, null, 4, 5, 4096, 32, 0, null, T,
+                                      ok, ok, ok, null, null, stage, ok, 1 << 30, null)
+
+    assert verify(off, ok, ok, 1.0) == -1                      # P
+    assert verify(ok, ok, ok, 1.0, stage=off) == -1            # staging buffer
+    assert verify(ok, off, ok, 1.0) == -1                      # U (sampled verification reads it)
+    assert verify(ok, ok, off, 1.0) == -1                      # W2
+    assert verify(off, null, null, 0.0) == -1                  # greedy: P only
+
+    def markov(U, W2):
+        return L.dspark_draft_markov(U, 0, ok, ok, W2, 1, 4, 5, 4096, 32, 0, null, 1.0,
+                                     ok, ok, ok, ok, ok, 1 << 30, null)
+
+    assert markov(off, ok) == -1
+    assert markov(ok, off) == -1
