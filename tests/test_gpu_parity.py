@@ -236,21 +236,24 @@ def test_verify_reads_host_resident_targets_in_place():
         np.testing.assert_array_equal(host(a[k]), host(b[k]), err_msg=k)
 
 
-@pytest.mark.parametrize("gamma,T,V", [(4, 1.0, 20488), (16, 0.0, 8200), (64, 1.0, 4104)])
-def test_verify_staged_host_targets(gamma, T, V):
+@pytest.mark.parametrize("gamma,T,V,pdt", [(4, 1.0, 20488, synth.F32), (16, 0.0, 8200, synth.F32),
+                                            (64, 1.0, 4104, synth.F32), (5, 0.8, 8200, synth.BF16)])
+def test_verify_staged_host_targets(gamma, T, V, pdt):
     """P read in place from pinned host memory with a device staging buffer
     (one target row per wave, up to gamma + 1 waves): tokens and lengths
     equal to the run with P on the device, p_tok / lse_p equal where the
     decision read them and NaN elsewhere, and the staged rows equal to P
     where verification read them."""
-    w = synth.Workload("zcs", R=6, gamma=gamma, V=V, r=64, T=T)
+    w = synth.Workload("zcs", R=6, gamma=gamma, V=V, r=64, T=T, p_dtype=pdt)
     x = synth.gen_all(w)
     dr = oracle_draft(w, x, 23)
     draft = dict(tokens=dev(dr["tokens"].astype(np.int32)), q_tok=dev(dr["qx"].astype(np.float32)),
                  lse=dev(dr["lse"].astype(np.float64)), code=dev(dr["code"].astype(np.float32)))
     hP = torch.from_numpy(np.ascontiguousarray(x["P"])).pin_memory()
+    if x["P"].dtype == np.uint16:
+        hP = hP.view(torch.bfloat16)
     Pv = binding.host_view(hP, torch.device("cuda:0"))
-    stage = torch.full(hP.shape, float("nan"), dtype=torch.float32, device="cuda:0")
+    stage = torch.full(hP.shape, float("nan"), dtype=hP.dtype, device="cuda:0")
     a = binding.verify(dev(x["P"]), dev(x["U"]), dev(x["W2"]), draft, w.T, 23)
     b = binding.verify(Pv, dev(x["U"]), dev(x["W2"]), draft, w.T, 23, p_stage=stage)
     torch.cuda.synchronize()
