@@ -254,7 +254,7 @@ __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
     const bool own = j < kRChunk && v < V;
     float u = 0.f;
     if (own) u = Elem<UT>::get(static_cast<const typename Elem<UT>::T*>(A.U), ((size_t)r * A.gamma + (kprev - 1)) * V + v);
-    __shared__ float s_b[NW][kRChunk];
+    __shared__ __align__(16) float s_b[NW][kRChunk];
     {
         constexpr int kBatch = WT == DSPARK_BF16 ? 16 : 8;
         const int c0 = c * kRChunk + 8 * lane;
@@ -274,8 +274,13 @@ __device__ int finish_sample(const DraftArgs& A, int r, int kprev) {
                 for (int jj = 0; jj < 8; ++jj) b[jj] = fmaf(ei, w[t].get(jj), b[jj]);
             }
         }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) s_b[warp][8 * lane + jj] = b[jj];
+        {
+            // two 16-byte stores per lane: eight scalar stores at a stride of
+            // eight floats would put eight lanes on each of four banks
+            float4* dst = reinterpret_cast<float4*>(&s_b[warp][8 * lane]);
+            dst[0] = make_float4(b[0], b[1], b[2], b[3]);
+            dst[1] = make_float4(b[4], b[5], b[6], b[7]);
+        }
     }
     __syncthreads();
     const float invT = 1.f / A.T;
