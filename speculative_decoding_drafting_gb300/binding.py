@@ -150,6 +150,18 @@ def _dt(t: torch.Tensor) -> int:
     raise TypeError(f"storage dtype must be float32 or bfloat16, got {t.dtype}")
 
 
+def _shape(name: str, t, shape, dtype=None):
+    """The C ABI takes bare pointers and cannot see sizes: a tensor of the
+    wrong shape would be read or written past its end on the device, so the
+    binding checks every shape (and the dtype where it is fixed) first."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -210,6 +222,20 @@ def schedule_workspace_bytes(R, gamma) -> int:
     return int(load().dspark_schedule_workspace_size(R, gamma))
 
 
+def _draft_shapes(R, gamma, V, r, anchor, W1, W2, req_ids):
+    _shape("anchor", anchor, (R,), torch.int32)
+    _shape("W1", W1, (V, r))
+    _shape("W2", W2, (r, V))
+    _shape("req_ids", req_ids, (R,))
+
+
+def _draft_out_shapes(out, R, gamma, r):
+    _shape("tokens", out["tokens"], (R, gamma), torch.int32)
+    _shape("q_tok", out["q_tok"], (R, gamma), torch.float32)
+    _shape("lse", out["lse"], (R, gamma), torch.float64)
+    _shape("code", out["code"], (R, gamma, r), torch.float32)
+
+
 def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None, ws=None, out=None, stream=None,
                  conf_w=None, conf_H=None, conf_t=None):
     """Markov-head drafting (``dspark_draft_markov``).  Returns a dict of outputs.
@@ -219,11 +245,13 @@ def draft_markov(U, anchor, W1, W2, temperature: float, seed: int, req_ids=None,
     R, gamma, V = U.shape
     r = W1.shape[1]
     dev = U.device
+    _draft_shapes(R, gamma, V, r, anchor, W1, W2, req_ids)
     if out is None:
         out = dict(tokens=torch.empty((R, gamma), dtype=torch.int32, device=dev),
                    q_tok=torch.empty((R, gamma), dtype=torch.float32, device=dev),
                    lse=torch.empty((R, gamma), dtype=torch.float64, device=dev),
                    code=torch.empty((R, gamma, r), dtype=torch.float32, device=dev))
+    _draft_out_shapes(out, R, gamma, r)
     nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, 0)
     if ws is None:
         ws = _workspace(nbytes, dev)
@@ -248,12 +276,17 @@ def draft_rnn(U, anchor, W1, W2, Wgco, H, temperature: float, seed: int, req_ids
     dev = U.device
     if H.dtype != torch.bfloat16:
         raise TypeError("H must be bfloat16")
+    _draft_shapes(R, gamma, V, r, anchor, W1, W2, req_ids)
+    _shape("Wgco", Wgco, (2 * r + d, 3 * r))
+    _shape("H", H, (R, gamma, d))
     if out is None:
         out = dict(tokens=torch.empty((R, gamma), dtype=torch.int32, device=dev),
                    q_tok=torch.empty((R, gamma), dtype=torch.float32, device=dev),
                    lse=torch.empty((R, gamma), dtype=torch.float64, device=dev),
                    code=torch.empty((R, gamma, r), dtype=torch.float32, device=dev),
                    state=torch.empty((R, r), dtype=torch.float32, device=dev))
+    _draft_out_shapes(out, R, gamma, r)
+    _shape("state", out.get("state"), (R, r), torch.float32)
     nbytes = L.dspark_draft_workspace_size(R, gamma, V, r, d)
     if ws is None:
         ws = _workspace(nbytes, dev)
@@ -277,12 +310,28 @@ def verify(P, U, W2, draft, temperature: float, seed: int, verify_len=None, req_
     gamma = G1 - 1
     r = W2.shape[0]
     dev = P.device
+    _shape("W2", W2, (r, V))
+    if float(temperature) > 0.0:
+        _shape("U", U, (R, gamma, V))
+    _shape("draft tokens", draft["tokens"], (R, gamma), torch.int32)
+    _shape("draft q_tok", draft.get("q_tok"), (R, gamma), torch.float32)
+    _shape("draft lse", draft.get("lse"), (R, gamma), torch.float64)
+    _shape("draft code", draft.get("code"), (R, gamma, r), torch.float32)
+    _shape("verify_len", verify_len, (R,), torch.int32)
+    _shape("req_ids", req_ids, (R,))
+    if p_stage is not None:
+        _shape("p_stage", p_stage, (R, G1, V), P.dtype)
     if out is None:
         out = dict(out_tokens=torch.empty((R, G1), dtype=torch.int32, device=dev),
                    accept_len=torch.empty((R,), dtype=torch.int32, device=dev),
                    n_out=torch.empty((R,), dtype=torch.int32, device=dev),
                    p_tok=torch.empty((R, gamma), dtype=torch.float32, device=dev),
                    lse_p=torch.empty((R, G1), dtype=torch.float64, device=dev))
+    _shape("out_tokens", out["out_tokens"], (R, G1), torch.int32)
+    _shape("accept_len", out["accept_len"], (R,), torch.int32)
+    _shape("n_out", out["n_out"], (R,), torch.int32)
+    _shape("p_tok", out.get("p_tok"), (R, gamma), torch.float32)
+    _shape("lse_p", out.get("lse_p"), (R, G1), torch.float64)
     nbytes = L.dspark_verify_workspace_size(R, gamma, V, r)
     if ws is None:
         ws = _workspace(nbytes, dev)

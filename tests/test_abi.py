@@ -149,3 +149,36 @@ def test_misaligned_streamed_arrays_rejected_on_the_host():
 
     assert markov(off, ok) == -1
     assert markov(ok, off) == -1
+
+
+def test_binding_checks_shapes_before_any_launch():
+    """The C ABI cannot see sizes, so the binding rejects a tensor of the
+    wrong shape or dtype before passing any pointer (CPU tensors suffice:
+    the check comes first)."""
+    import torch
+    R, gamma, V, r = 3, 4, 64, 8
+    P = torch.zeros((R, gamma + 1, V))
+    U = torch.zeros((R, gamma, V))
+    W2 = torch.zeros((r, V), dtype=torch.bfloat16)
+    draft = dict(tokens=torch.zeros((R, gamma), dtype=torch.int32),
+                 q_tok=torch.zeros((R, gamma)), lse=torch.zeros((R, gamma), dtype=torch.float64),
+                 code=torch.zeros((R, gamma, r)))
+    with pytest.raises(ValueError, match="p_stage"):
+        binding.verify(P, U, W2, draft, 1.0, 0, p_stage=torch.zeros((R, gamma, V)))
+    with pytest.raises(TypeError, match="p_stage"):
+        binding.verify(P, U, W2, draft, 1.0, 0, p_stage=torch.zeros((R, gamma + 1, V), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="U"):
+        binding.verify(P, U[:, :2], W2, draft, 1.0, 0)
+    with pytest.raises(ValueError, match="draft code"):
+        binding.verify(P, U, W2, dict(draft, code=torch.zeros((R, gamma, r + 1))), 1.0, 0)
+    with pytest.raises(ValueError, match="verify_len"):
+        binding.verify(P, U, W2, draft, 1.0, 0, verify_len=torch.zeros((R + 1,), dtype=torch.int32))
+    W1 = torch.zeros((V, r), dtype=torch.bfloat16)
+    anchor = torch.zeros((R,), dtype=torch.int32)
+    with pytest.raises(ValueError, match="W2"):
+        binding.draft_markov(U, anchor, W1, W2[:, :V - 8], 1.0, 0)
+    with pytest.raises(ValueError, match="anchor"):
+        binding.draft_markov(U, anchor[:2], W1, W2, 1.0, 0)
+    # correct shapes reach the pointer marshalling, which wants CUDA tensors
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.verify(P, U, W2, draft, 1.0, 0, p_stage=torch.zeros((R, gamma + 1, V)))
