@@ -322,45 +322,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
             tc_fence_after();
             const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
-#pragma unroll 1
+            // the thread's 32 columns of the tile: one tensor-memory load and
+            // all of its U values before anything waits on them
+            float y32[32];
+            __syncwarp();
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 32), y32);
+            if (UT == DSPARK_F32) {
+                const uint8_t* rowp = ust + wg * 16384 + rit * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 f = *reinterpret_cast<const float4*>(rowp + ((c ^ (rit & 7)) << 4));
+                    y32[4 * c + 0] += f.x;
+                    y32[4 * c + 1] += f.y;
+                    y32[4 * c + 2] += f.z;
+                    y32[4 * c + 3] += f.w;
+                }
+            } else {
+                const uint8_t* rowp = ust + (wg >> 1) * 16384 + rit * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 f = *reinterpret_cast<const uint4*>(rowp + ((((wg & 1) * 4 + c) ^ (rit & 7)) << 4));
+                    const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        y32[8 * c + 2 * e + 0] += bf16_bits_to_float(w4[e] & 0xFFFFu);
+                        y32[8 * c + 2 * e + 1] += bf16_bits_to_float(w4[e] >> 16);
+                    }
+                }
+            }
+            // the tile's data is in registers: hand the buffers back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&S.acc_empty[buf]);
+                mbar_arrive(&S.u_empty[us]);
+            }
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int v0 = tile * kBN + wg * 32 + h * 16;
-                float y[16];
-                __syncwarp();
-                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 32 + h * 16), y);
-                if (UT == DSPARK_F32) {
-                    const uint8_t* rowp = ust + wg * 16384 + rit * 128;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float4 f = *reinterpret_cast<const float4*>(rowp + (((4 * h + c) ^ (rit & 7)) << 4));
-                        y[4 * c + 0] += f.x;
-                        y[4 * c + 1] += f.y;
-                        y[4 * c + 2] += f.z;
-                        y[4 * c + 3] += f.w;
-                    }
-                } else {
-                    const uint8_t* rowp = ust + (wg >> 1) * 16384 + rit * 128;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const uint4 f =
-                            *reinterpret_cast<const uint4*>(rowp + ((((wg & 1) * 4 + 2 * h + c) ^ (rit & 7)) << 4));
-                        const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            y[8 * c + 2 * e + 0] += bf16_bits_to_float(w4[e] & 0xFFFFu);
-                            y[8 * c + 2 * e + 1] += bf16_bits_to_float(w4[e] >> 16);
-                        }
-                    }
-                }
-                if (h == 1) {
-                    // the tile's data is in registers: hand the buffers back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&S.acc_empty[buf]);
-                        mbar_arrive(&S.u_empty[us]);
-                    }
-                }
+                float* y = y32 + 16 * h;
                 if (!(row_ok && v0 + 16 <= p.V)) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
