@@ -182,3 +182,18 @@ def test_binding_checks_shapes_before_any_launch():
     # correct shapes reach the pointer marshalling, which wants CUDA tensors
     with pytest.raises(ValueError, match="CUDA"):
         binding.verify(P, U, W2, draft, 1.0, 0, p_stage=torch.zeros((R, gamma + 1, V)))
+
+
+def test_status_codes_agree_between_header_library_and_binding():
+    """Every DSPARK_ERR_* value in the header has a dspark_strerror text and
+    the binding's message table covers exactly the same codes."""
+    with open(os.path.join(ROOT, "include", "dspark.h")) as f:
+        text = f.read()
+    codes = {name: int(v) for name, v in re.findall(r"\b(DSPARK_(?:OK|ERR_[A-Z_]+))\s*=\s*(-?\d+)", text)}
+    assert codes.get("DSPARK_OK") == 0 and len(codes) >= 8
+    L = binding.load()
+    for name, v in codes.items():
+        msg = L.dspark_strerror(v)
+        assert msg and msg != b"unknown status", name
+        assert binding.STATUS.get(v), name
+    assert set(binding.STATUS) == set(codes.values())
