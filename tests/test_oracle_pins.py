@@ -336,6 +336,86 @@ def test_acceptance_rate_is_one_minus_tv():
 
 
 # ------------------------------------------------------------------ tree sampler
+def _residual_pin_case():
+    """Position 1 is forced to accept (P_0 = U_0 + e_1 W2, so p_1 = q_1), W2 is
+    far from zero and T = 0.7, so the residual at position 2 needs q_2 rebuilt
+    from the second code row, the second lse and (U + B) / T together."""
+    V, r, T = 6, 3, 0.7
+    rng = np.random.default_rng(13)
+    W1 = rng.normal(0.0, 1.0, (V, r)).astype(np.float32)
+    W2 = rng.normal(0.0, 1.0, (r, V)).astype(np.float32)
+    anchor = 0
+    U = rng.normal(0.0, 1.0, (2, V)).astype(np.float32)
+    P = np.empty((3, V), np.float32)
+    P[0] = (U[0].astype(np.float64) + W1[anchor].astype(np.float64) @ W2.astype(np.float64)).astype(np.float32)
+    P[1] = rng.normal(0.0, 1.5, V).astype(np.float32)
+    P[2] = rng.normal(0.0, 1.5, V).astype(np.float32)
+    return V, r, T, W1, W2, anchor, U, P
+
+
+def _position2_law(V, T, W1, W2, anchor, U, P, rebuild):
+    """Law of the token emitted at position 2 when position 1 is accepted,
+    by exact enumeration over x_1 ~ q_1 (= p_1) and x_2 ~ q_2(. | x_1), with
+    the residual formed from rebuild(x_1) in place of q_2."""
+    f64 = lambda a: a.astype(np.float64)  # noqa: E731
+    q1 = special.softmax((f64(U[0]) + f64(W1[anchor]) @ f64(W2)) / T)
+    p2 = special.softmax(f64(P[1]) / T)
+    law = np.zeros(V)
+    for x1 in range(V):
+        q2 = special.softmax((f64(U[1]) + f64(W1[x1]) @ f64(W2)) / T)
+        acc = np.minimum(p2, q2)
+        w = np.maximum(p2 - rebuild(x1, q2), 0.0)
+        law += q1[x1] * (acc + (1.0 - acc.sum()) * w / w.sum())
+    return law, p2
+
+
+def test_residual_rebuild_gives_the_target_law_at_position_two():
+    """Explainer section 05: after a rejection at position j the token comes
+    from r(v) = max(p_j - q_j, 0) / Z, with q_j rebuilt from the Markov code
+    e_j = W1[x_{j-1}] (blog section 3.2): q_j(v) = exp((U_j + e_j W2)[v] / T - lse_j).
+    Exact enumeration gives the target law p_2 = softmax(P_1 / T) for the
+    emitted token; the oracle, run on 10^5 request ids, must reproduce it
+    (chi-square).  The three plausible slips -- the previous code row, the
+    previous position's lse, T dividing U alone -- each move the law far
+    enough that the chi-square at this sample size would reject them."""
+    V, r, T, W1, W2, anchor, U, P = _residual_pin_case()
+    f64 = lambda a: a.astype(np.float64)  # noqa: E731
+    law, p2 = _position2_law(V, T, W1, W2, anchor, U, P, lambda x1, q2: q2)
+    np.testing.assert_allclose(law, p2, rtol=0, atol=1e-12)
+
+    # the oracle on N independent request ids with identical inputs
+    N, seed = 100_000, 424242
+    Ur = np.broadcast_to(U, (N, 2, V)).copy()
+    Pr = np.broadcast_to(P, (N, 3, V)).copy()
+    ids = np.arange(N, dtype=np.uint32)
+    d = oracle.draft_markov(Ur, np.full(N, anchor, np.int32), W1, W2, T, seed, req_ids=ids)
+    o = oracle.verify(Pr, Ur, W2, d["tokens"], d["qx"], d["lse"], d["code"], T, seed, req_ids=ids)
+    reached = o["accept_len"] >= 1
+    assert reached.mean() > 0.999                      # p_1 = q_1: position 1 accepted
+    rej2 = (o["accept_len"] == 1).mean()
+    assert 0.2 < rej2 < 0.9                            # the residual path is taken often (about 0.31)
+    counts = np.bincount(o["out_tokens"][reached, 1], minlength=V)
+    n = int(reached.sum())
+    assert stats.chisquare(counts, n * p2).pvalue > 1e-3
+
+    # power against the slips: the law each would produce, as a chi-square
+    # noncentrality at this n (a value of 100 rejects at 1e-3 almost surely)
+    lse1 = special.logsumexp((f64(U[0]) + f64(W1[anchor]) @ f64(W2)) / T)
+    slips = {
+        "previous code row": lambda x1, q2: np.exp(
+            (f64(U[1]) + f64(W1[anchor]) @ f64(W2)) / T
+            - special.logsumexp((f64(U[1]) + f64(W1[x1]) @ f64(W2)) / T)),
+        "previous lse": lambda x1, q2: np.exp((f64(U[1]) + f64(W1[x1]) @ f64(W2)) / T - lse1),
+        "T on U alone": lambda x1, q2: np.exp(
+            f64(U[1]) / T + f64(W1[x1]) @ f64(W2)
+            - special.logsumexp((f64(U[1]) + f64(W1[x1]) @ f64(W2)) / T)),
+    }
+    for name, reb in slips.items():
+        bad, _ = _position2_law(V, T, W1, W2, anchor, U, P, reb)
+        lam = n * float(((bad - p2) ** 2 / p2).sum())
+        assert lam > 100.0, (name, lam)
+
+
 def test_tree_sampler_one_hot_and_half_masses():
     for V in (1, 2, 5, 16, 1000):
         for hot in {0, V // 2, V - 1}:
