@@ -41,14 +41,24 @@
  *    skips the bad access, records the condition in a status word at the
  *    start of the workspace and finishes; dspark_workspace_status() reads
  *    and clears it.
+ *  - U, W2 and Wgco must be device memory of the current device (the
+ *    tensor-core kernels read them through tensor maps and share W2 tiles
+ *    among the CTAs of a thread-block cluster, which is defined for this
+ *    GPU's own memory only); a peer device's buffer, mapped host memory or
+ *    managed memory returns DSPARK_ERR_INVALID_ARG before anything is
+ *    enqueued.  P (the target logits) may be pinned host memory mapped for
+ *    the device (dspark_host_pointer).
  *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key
  *    (seed low 32 bits, seed high 32 bits) and counter
  *    (v / 4, request id, position, stream); index v takes output word v mod 4
  *    and becomes u = (w + 1/2) * 2^-32 in (0, 1).  Streams:
- *    0 = draft Gumbel noise (v = vocabulary index, position k = 1..gamma),
+ *    0 = draft Gumbel noise of a column (v = vocabulary index, position k = 1..gamma),
  *    1 = acceptance uniform (v = 0, position k),
- *    2 = residual / bonus draw (v = tree level, position = the position sampled).
+ *    2 = residual / bonus draw (v = tree level, position = the position sampled),
+ *    3 = draft Gumbel noise of a 256-column chunk (v = chunk index, position k).
  *    The request id is req_ids[i] (device array) or i when req_ids is NULL.
+ *    dspark_philox4x32_10 below evaluates the same block function on the
+ *    device, for known-answer checks.
  *  - Nothing is thrown across the ABI.
  */
 #ifndef DSPARK_H
@@ -121,9 +131,17 @@ size_t dspark_draft_workspace_size(int R, int gamma, int V, int r, int d);
  *   lse     [R, gamma]     double    log sum_v exp((U_k + B_k)[v] / T) (0 at T = 0)
  *   code    [R, gamma, r]  float     e_k = W1[x_{k-1}], the rank-r code that
  *                                    gives B_k = e_k W2 (consumed by verify)
- * Sampling: x_k = argmax_v (U_k + B_k)[v] / T + G_v with Gumbel noise
- * G_v = -ln(-ln u_v) from stream 0; ties go to the lowest v.
- * B_k and q_k are never written to memory.
+ * Sampling (T > 0), with z = (U_k + B_k) / T and Gumbel noise G = -ln(-ln u):
+ * Gumbel-max in two levels, an exact sampler of softmax(z).  First a chunk c
+ * of 256 consecutive columns (the last one may be shorter):
+ *   c = argmax_c  ln(sum_{v in c} exp z_v) + G_c,  u_c from stream 3, index c;
+ * then the column inside it:
+ *   x_k = argmax_{v in c}  z_v + G_v,            u_v from stream 0, index v.
+ * Ties go to the lowest index at both levels.  (A chunk is chosen with
+ * probability equal to its share of the mass, the column with its share of
+ * the chunk, so x_k ~ softmax(z); the realisation differs from a single
+ * Gumbel-max over all V columns.)  T = 0 takes argmax_v (U_k + B_k)[v], the
+ * lowest v on ties.  B_k and q_k are never written to memory.
  * Requirements: R >= 1, 1 <= gamma <= 64, V >= 2 with V % 8 == 0 for bf16 and
  * V % 4 == 0 for f32 storage, V <= 2^20, 1 <= r <= 1024, T >= 0 and finite.
  */
@@ -298,6 +316,9 @@ int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype,
  *    work overlaps on the GPU race: order them (one stream, or events).
  *  - Each call clears the array's status word; device-side conditions
  *    (token ids outside [0, V)) are not reported by this variant.
+ *  - `stream` must belong to the current device (the array's address is
+ *    that device's); a stream of another device returns
+ *    DSPARK_ERR_INVALID_ARG.
  */
 int dspark_verify_noalloc(const void* P, int p_dtype, const void* U, int u_dtype,
                           const void* W2, int w_dtype,
@@ -407,6 +428,20 @@ int dspark_sts_fit(const float* c, const int32_t* accept_len, int N, int gamma,
  * double, all device.  No workspace.
  */
 int dspark_sts_apply(const float* c, int N, int gamma, const double* t, float* out, void* stream);
+
+/* ---------------------------------------------------------------- random */
+
+/*
+ * The device's Philox4x32-10 block function (Salmon et al., SC'11, the
+ * generator every random decision above draws from), for known-answer
+ * checks of the copy the kernels use.  For i < n:
+ *   out[4i .. 4i+3] = Philox4x32-10(counter ctr[4i .. 4i+3], key key[2i .. 2i+1])
+ * ctr [n, 4], key [n, 2] and out [n, 4] are uint32 device arrays
+ * (caller-owned; ctr and out 16-byte aligned, key 8-byte aligned); the work
+ * is enqueued on `stream`.  Errors: SHAPE for n < 1, INVALID_ARG for a null
+ * or misaligned pointer, CUDA if the launch fails.
+ */
+int dspark_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out, int n, void* stream);
 
 /* -------------------------------------------------------------- profiling */
 

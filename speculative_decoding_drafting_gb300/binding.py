@@ -83,6 +83,7 @@ def load(build_if_missing: bool = True):
         L.dspark_sts_workspace_size.restype = sz
         L.dspark_sts_fit.argtypes = [P, P, i32, i32, P, i32, i32, P, P, P, P, P, sz, P]
         L.dspark_sts_apply.argtypes = [P, i32, i32, P, P, P]
+        L.dspark_philox4x32_10.argtypes = [P, P, P, i32, P]
         L.dspark_profile_enable.argtypes = [i32]
         L.dspark_profile_collect.argtypes = [P, P, i32]
         L.dspark_profile_kernel_name.argtypes = [i32]
@@ -91,7 +92,7 @@ def load(build_if_missing: bool = True):
                      "dspark_verify", "dspark_verify_staged", "dspark_schedule", "dspark_schedule_async",
                      "dspark_schedule_threshold",
                      "dspark_sts_fit",
-                     "dspark_sts_apply",
+                     "dspark_sts_apply", "dspark_philox4x32_10",
                      "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
             getattr(L, name).restype = i32
         _lib = L
@@ -417,6 +418,22 @@ def sts_apply(c, t, out=None, stream=None):
         out = torch.empty_like(c)
     code = L.dspark_sts_apply(_p(c), N, gamma, _p(t), _p(out), _stream(stream))
     _check("dspark_sts_apply", code)
+    return out
+
+
+def philox4x32_10(ctr, key, out=None, stream=None):
+    """The device's Philox4x32-10 block function on n counters ``ctr`` [n, 4]
+    and keys ``key`` [n, 2] (uint32 values in int32 CUDA tensors, bit for
+    bit); returns out [n, 4] (``dspark_philox4x32_10``)."""
+    L = load()
+    n = ctr.shape[0]
+    _shape("ctr", ctr, (n, 4), torch.int32)
+    _shape("key", key, (n, 2), torch.int32)
+    if out is None:
+        out = torch.empty((n, 4), dtype=torch.int32, device=ctr.device)
+    _shape("out", out, (n, 4), torch.int32)
+    code = L.dspark_philox4x32_10(_p(ctr), _p(key), _p(out), n, _stream(stream))
+    _check("dspark_philox4x32_10", code)
     return out
 
 

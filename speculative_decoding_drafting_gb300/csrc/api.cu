@@ -2,6 +2,7 @@
 // kernel dispatch.  See include/dspark.h for the contract of each entry point.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -11,17 +12,36 @@
 
 namespace dspark {
 
+// SM count of the current device, looked up once per device (a process may
+// drive several GPUs; each call sizes its grids for the device it runs on).
 int num_sms() {
-    static int cached = 0;
-    if (cached == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-            cached = n;
-        else
-            return 148;
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+    if (dev < kMaxDevices) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
-    return cached;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+    if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// True for device memory of the current device.  The arrays the kernels
+// address through tensor maps (U, W2, Wgco) must be: the tensor-core kernels
+// share W2 tiles among the CTAs of a thread-block cluster by multicast, which
+// is only defined for this GPU's own memory, so a peer device's buffer, a
+// mapped host buffer or managed memory is refused before anything is enqueued.
+static bool on_current_device(const void* p) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
 }
 
 static bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -134,6 +154,8 @@ static int draft_entry(DraftArgs& a, bool rnn, size_t ws_bytes, void* stream) {
                                                                       ? DSPARK_ERR_SHAPE
                                                                       : DSPARK_ERR_INVALID_ARG;
     if (!aligned16(a.U) || !aligned16(a.W2) || (rnn && !aligned16(a.Wgco))) return DSPARK_ERR_INVALID_ARG;
+    if (!on_current_device(a.U) || !on_current_device(a.W2) || (rnn && !on_current_device(a.Wgco)))
+        return DSPARK_ERR_INVALID_ARG;
     if (!a.ws || !aligned256(a.ws)) return DSPARK_ERR_WORKSPACE;
     st = draft_carve(a, ws_bytes);
     if (st) return st;
@@ -207,6 +229,7 @@ int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype,
     if (temperature > 0.f && (!U || !W2 || !q_tok || !lse || !code)) return DSPARK_ERR_INVALID_ARG;
     if (!aligned16(P) || (p_stage && !aligned16(p_stage))) return DSPARK_ERR_INVALID_ARG;
     if (temperature > 0.f && (!aligned16(U) || !aligned16(W2))) return DSPARK_ERR_INVALID_ARG;
+    if (temperature > 0.f && (!on_current_device(U) || !on_current_device(W2))) return DSPARK_ERR_INVALID_ARG;
     if (!ws || !aligned256(ws)) return DSPARK_ERR_WORKSPACE;
     VerifyArgs a;
     std::memset(&a, 0, sizeof a);

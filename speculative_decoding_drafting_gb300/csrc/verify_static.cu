@@ -16,7 +16,9 @@
 // All calls share the one array and each leaves its contents behind: calls
 // whose work overlaps on the GPU (different streams, or different host
 // threads without ordering) race on it and must be serialised by the caller.
-// The status word at the start of the array is cleared by every call.
+// The status word at the start of the array is cleared by every call.  The
+// stream must belong to the current device (the array's address is the
+// current device's); a stream of another device is refused.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -63,10 +65,18 @@ extern "C" int dspark_verify_noalloc(const void* P, int p_dtype, const void* U, 
                                      double* lse_p, void* stream) {
     if (R < 1 || gamma < 1 || gamma > 64 || V < 2 || V > (1 << 20) || r < 1 || r > 1024) return DSPARK_ERR_SHAPE;
     if (verify_workspace_bytes(R, gamma, V, r) > kNoallocScratchBytes) return DSPARK_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the scratch address belongs to the current device: a stream of another
+    // device would hand its kernels memory they cannot address
+    int dev = 0, sdev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DSPARK_ERR_CUDA;
+    }
+    if (sdev != dev) return DSPARK_ERR_INVALID_ARG;
     void* ws = nullptr;
     int st = noalloc_scratch(&ws);
     if (st) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return dspark_verify(P, p_dtype, U, u_dtype, W2, w_dtype, tokens, q_tok, lse, code, verify_len, R, gamma, V, r,
                          seed, req_ids, temperature, out_tokens, accept_len, n_out, p_tok, lse_p, ws,

@@ -151,6 +151,22 @@ def test_misaligned_streamed_arrays_rejected_on_the_host():
     assert markov(ok, off) == -1
 
 
+def test_foreign_memory_refused_on_the_host():
+    """U and W2 must be device memory of the current device (tensor maps,
+    and W2 tiles shared by multicast within a cluster): an address that is
+    not (here: no allocation at all, and on a machine without a GPU no
+    current device) fails with INVALID_ARG before any kernel is enqueued."""
+    L = binding.load()
+    null = None
+    ok = ctypes.c_void_p(1 << 20)            # 16- and 256-byte aligned; never dereferenced
+    st = L.dspark_draft_markov(ok, 0, ok, ok, ok, 1, 4, 5, 4096, 32, 0, null, 1.0,
+                               ok, ok, ok, ok, ok, 1 << 30, null)
+    assert st == -1
+    st = L.dspark_verify_staged(ok, 0, ok, 0, ok, 1, ok, ok, ok, ok, null, 4, 5, 4096, 32, 0, null, 1.0,
+                                ok, ok, ok, null, null, null, ok, 1 << 30, null)
+    assert st == -1
+
+
 def test_binding_checks_shapes_before_any_launch():
     """The C ABI cannot see sizes, so the binding rejects a tensor of the
     wrong shape or dtype before passing any pointer (CPU tensors suffice:
