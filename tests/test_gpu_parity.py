@@ -103,6 +103,20 @@ def test_verify_many_requests_statistics():
     g = gpu_verify_on(w, x, dr, 8)
     o = oracle_verify_on(w, x, dr, 8)
     compare_verify(g, o, np.ones(w.R, bool), tag="stats")
+    # Position 1 is accepted with probability sum_v min(p_1(v), q_1(v)) = 1 - TV
+    # (explainer section 05): p_1 = softmax(P_0 / T), q_1 = softmax((U_0 + e_1 W2) / T)
+    # with e_1 the draft's first code.  The requests are independent, so the
+    # count of accepted first positions has mean sum_r alpha_r and variance
+    # sum_r alpha_r (1 - alpha_r): a z-test on the GPU's acceptances.
+    from scipy.special import softmax
+    z = (x["U"][:, 0, :].astype(np.float64) + dr["code"][:, 0, :] @ x["W2"].astype(np.float64)) / w.T
+    q1 = softmax(z, axis=1)
+    p1 = softmax(x["P"][:, 0, :].astype(np.float64) / w.T, axis=1)
+    alpha = np.minimum(p1, q1).sum(axis=1)
+    assert 0.2 < alpha.mean() < 0.95
+    acc = (g["accept_len"] >= 1).sum()
+    zscore = (acc - alpha.sum()) / np.sqrt((alpha * (1 - alpha)).sum())
+    assert abs(zscore) < 4.0, (acc, alpha.sum(), zscore)
 
 
 @pytest.mark.parametrize("R,gamma,rho", [(1, 1, 0.0), (3, 5, 0.5), (8, 4, 0.0), (5, 16, 0.5), (64, 5, 0.9),
