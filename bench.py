@@ -188,10 +188,14 @@ def algorithmic_bytes(w, n_rej: float, verify_rows: float):
     """Bytes the cycle must move: U, W2 and the W1 rows once; the target rows
     verification must read (each request's rows up to its first rejection,
     or through the bonus row: accept_len + 1 rows); the residual pass's
-    re-read of U_j and P_j of every rejecting request and W2 once."""
+    re-read of U_j and P_j of every rejecting request and W2 once.  Greedy
+    verification (T = 0) has no residual: a mismatch emits the target row's
+    argmax, which the row's own read gives."""
     su = 4 if w.u_dtype == synth.F32 else 2
     sp = 4 if w.p_dtype == synth.F32 else 2
     sw = 4 if w.w_dtype == synth.F32 else 2
+    if not w.T > 0:
+        n_rej = 0
     draft = w.R * w.gamma * w.V * su + w.r * w.V * sw + w.R * w.gamma * w.r * sw
     verify1 = verify_rows * w.V * sp
     resid = n_rej * w.V * (su + sp) + (w.r * w.V * sw if n_rej > 0 else 0)
@@ -200,25 +204,81 @@ def algorithmic_bytes(w, n_rej: float, verify_rows: float):
                 residual_per_launch=resid)
 
 
-def cpu_oracle_sample(w, x, target_s: float = 10.0):
+GUMBEL_FLAG = 1e-4     # a draft (Gumbel-max or greedy) margin below this is a flagged decision
+UNIFORM_FLAG = 1e-6    # so is a uniform this close to its acceptance or tree threshold
+
+
+def count_flags(od: dict, ov: dict, g_tokens: np.ndarray, g_out: np.ndarray, g_acc: np.ndarray, acc: dict):
+    """Flag accounting of one cycle: the oracle's draft od and verification ov
+    against the GPU's tokens, output tokens and accept lengths on the same
+    seed and request ids.  A decision is flagged where the oracle's own
+    margin lies inside a band the kernels' rounding could cross; only there
+    may the two disagree.  Adds to acc: positions compared, flagged decisions,
+    flagged and unflagged disagreements."""
+    R, gamma = od["tokens"].shape
+    for i in range(R):
+        diff = np.nonzero(g_tokens[i] != od["tokens"][i])[0]
+        kc = int(diff[0]) + 1 if diff.size else gamma          # compared up to the first disagreement
+        acc["positions"] += kc
+        acc["flagged"] += int((od["margin"][i, :kc] < GUMBEL_FLAG).sum())
+        if diff.size:
+            k = int(diff[0])
+            acc["flagged_disagreements" if od["margin"][i, k] < GUMBEL_FLAG else "unflagged_disagreements"] += 1
+            continue
+        vflag = bool(ov["min_gap"][i] < UNIFORM_FLAG)
+        acc["flagged"] += int(vflag)
+        if (g_out[i] != ov["out_tokens"][i]).any() or g_acc[i] != ov["accept_len"][i]:
+            acc["flagged_disagreements" if vflag else "unflagged_disagreements"] += 1
+
+
+def cpu_oracle_sample(w, x, target_s: float = 10.0, gpu_cycle=None):
     """Time the CPU oracle (draft + schedule + verify) on the workload itself:
     whole cycles over all R requests, repeated with fresh seeds until about
-    target_s of CPU work; returns positions/s."""
+    target_s of CPU work; returns positions/s.  With gpu_cycle (seed ->
+    numpy tokens, out_tokens, accept_len of the GPU cycle with request ids
+    0..R-1, run outside the oracle's timing) the same cycles also give the
+    flag accounting of the GPU path against the oracle."""
     import oracle
     cores = oracle.default_threads()
     idx = np.arange(w.R).astype(np.uint32)
     t_tot, cycles = 0.0, 0
+    acc = dict(positions=0, flagged=0, flagged_disagreements=0, unflagged_disagreements=0)
     while t_tot < target_s and cycles < 8:
+        seed = 7 + cycles
         t0 = time.perf_counter()
-        d = oracle.draft_markov(x["U"], x["anchor"], x["W1"], x["W2"], w.T, 7 + cycles, req_ids=idx)
+        d = oracle.draft_markov(x["U"], x["anchor"], x["W1"], x["W2"], w.T, seed, req_ids=idx)
         oracle.schedule_loop(x["c"], x["sps"])
-        oracle.verify(x["P"], x["U"], x["W2"], d["tokens"], d["qx"], d["lse"], d["code"], w.T, 7 + cycles,
-                      req_ids=idx)
+        v = oracle.verify(x["P"], x["U"], x["W2"], d["tokens"], d["qx"], d["lse"], d["code"], w.T, seed,
+                          req_ids=idx)
         t_tot += time.perf_counter() - t0
         cycles += 1
-    return dict(value=cycles * w.R * w.gamma / t_tot, unit="positions/s", cores=cores, kind="oracle",
-                sample=f"{cycles} full cycle(s) of the workload (all {w.R} requests x {w.gamma} positions, "
-                       f"V={w.V}): draft+schedule+verify, {t_tot:.2f} s on {cores} threads")
+        if gpu_cycle is not None:
+            count_flags(d, v, *gpu_cycle(seed), acc)
+    cpu = dict(value=cycles * w.R * w.gamma / t_tot, unit="positions/s", cores=cores, kind="oracle",
+               sample=f"{cycles} full cycle(s) of the workload (all {w.R} requests x {w.gamma} positions, "
+                      f"V={w.V}): draft+schedule+verify, {t_tot:.2f} s on {cores} threads")
+    flags = None
+    if gpu_cycle is not None:
+        n = max(1, acc["positions"])
+        flags = dict(acc, flagged_rate=acc["flagged"] / n,
+                     disagreement_rate=(acc["flagged_disagreements"] + acc["unflagged_disagreements"]) / n,
+                     bands={"gumbel_margin": GUMBEL_FLAG, "uniform_gap": UNIFORM_FLAG},
+                     sample=f"the CPU baseline's {cycles} cycle(s), GPU cycles on the same seeds and request ids")
+    return cpu, flags
+
+
+MULTI_GPU_REFUSAL = ("the GPU arm runs on one GPU: the draft sweep and the residual pass share W2 tiles among the "
+                     "CTAs of a thread-block cluster by TMA multicast, which is defined for this GPU's own memory "
+                     "only; requests shard as independent replicas, not measured on several GPUs")
+
+
+def refuse_multi_gpu(rank: int, world: int) -> int:
+    """Under torchrun with more than one rank the GPU arm does no work: rank 0
+    prints one line saying why, every rank exits 0."""
+    if rank == 0:
+        print(json.dumps({"metric": "draft+verify positions/s", "unit": "positions/s", "n_gpus": world,
+                          "value": None, "unavailable": MULTI_GPU_REFUSAL}), flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -256,6 +316,64 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def measure_config(name: str, scheduled: bool, steps: int, devc, flush):
+    """One more workload's whole cycle (Markov draft, scheduler, verification)
+    at its own sizes, timed as the headline is (L2 flushed between cycles,
+    CUDA events on the launch stream): positions per second, the cycle's
+    algorithmic bytes and their fraction of the measured HBM peak.  With
+    `scheduled` the verify lengths come from the scheduler's output (for the
+    long block at rho = 0.9 it chooses l = 0 everywhere: one token per
+    request, drawn from the first target row); otherwise every position is
+    verified.  Inputs are drawn on the device (synth.gen_device)."""
+    import torch
+    from speculative_decoding_drafting_gb300 import binding
+    w = synth.WORKLOADS[name]
+    x = synth.gen_device(w, devc, seed=1)
+    stream = torch.cuda.current_stream()
+    wss = [None, None, None]
+
+    def cycle(seed):
+        d = binding.draft_markov(x["U"], x["anchor"], x["W1"], x["W2"], w.T, seed, ws=wss[0])
+        s = binding.schedule(x["c"], x["sps"], ws=wss[1])
+        v = binding.verify(x["P"], x["U"], x["W2"], d, w.T, seed, verify_len=s["verify_len"] if scheduled else None,
+                           ws=wss[2])
+        wss[:] = [d["ws"], s["ws"], v["ws"]]
+        return d, s, v
+
+    for i in range(3):
+        cycle(10 + i)
+    ms, rej, rows, vl = [], [], [], []
+    for i in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        d, s, v = cycle(100 + i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+        lens = s["verify_len"] if scheduled else torch.full((w.R,), w.gamma, dtype=torch.int32, device=devc)
+        acc = v["accept_len"]
+        rej.append(int((acc < lens).sum().item()))
+        rows.append(int((acc + 1).sum().item()))
+        vl.append(float(lens.float().mean().item()))
+    per = float(np.median(ms))
+    ab = algorithmic_bytes(w, float(np.mean(rej)), float(np.mean(rows)))
+    hbm_peak, _, peak_src = _peaks()
+    gbs = ab["total"] / (per / 1000.0) / 1e9
+    st = {synth.F32: "f32", synth.BF16: "bf16"}
+    del x
+    torch.cuda.empty_cache()
+    return {"workload": (f"{w.name}: R={w.R} gamma={w.gamma} V={w.V} r={w.r} T={w.T} U {st[w.u_dtype]} "
+                         f"P {st[w.p_dtype]} W {st[w.w_dtype]}"),
+            "verify": ("scheduler (rho = %.1f)" % w.rho) if scheduled else "all gamma positions",
+            "metric": "draft+verify positions/s", "value": round(w.R * w.gamma / (per / 1000.0), 1),
+            "ms_per_cycle": round(per, 4), "mean_verify_len": round(float(np.mean(vl)), 3),
+            "rejecting_requests": float(np.mean(rej)), "target_rows_read": float(np.mean(rows)),
+            "algorithmic_bytes": int(ab["total"]), "achieved_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+            "inputs": "drawn on the device (same distributions as the numpy generator)"}
 
 
 def measure_rnn_draft(steps: int, warmup: int, devc, flush):
@@ -430,14 +548,14 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
 
+    rank, world, local = _dist_env()
+    if world > 1:
+        return refuse_multi_gpu(rank, world)
+
     import torch
-    import torch.distributed as dist
 
     from speculative_decoding_drafting_gb300 import binding
 
-    rank, world, local = _dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     devc = torch.device("cuda", local)
     binding.load()
@@ -469,8 +587,6 @@ def main(argv=None):
     for i in range(args.warmup):
         step(10 + i, wss)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -632,14 +748,23 @@ def main(argv=None):
 
     variants = None
     if rank == 0 and world == 1 and not args.no_variants:
-        variants = {"rnn_draft": measure_rnn_draft(max(3, args.steps // 2), 3, devc, flush)}
+        variants = {"dspark5": measure_config("dspark5", False, max(5, args.steps // 2), devc, flush),
+                    "greedy": measure_config("greedy", False, max(5, args.steps // 2), devc, flush),
+                    "longblock_verify_all": measure_config("longblock", False, max(5, args.steps // 2), devc, flush),
+                    "longblock_scheduled": measure_config("longblock", True, max(5, args.steps // 2), devc, flush),
+                    "rnn_draft": measure_rnn_draft(max(3, args.steps // 2), 3, devc, flush)}
         variants.update(measure_confidence_and_threshold(w, U, anchor, W1, W2, c, max(5, args.steps // 2), devc,
                                                          flush))
         variants["sts_fit"] = measure_sts(max(5, args.steps // 2), devc)
 
-    cpu = None
+    cpu = flags = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(w, x)
+        def gpu_cycle(seed):
+            d_, s_, v_ = step(seed, wss)
+            torch.cuda.synchronize()
+            return (d_["tokens"].cpu().numpy(), v_["out_tokens"].cpu().numpy(), v_["accept_len"].cpu().numpy())
+
+        cpu, flags = cpu_oracle_sample(w, x, gpu_cycle=gpu_cycle)
 
     if rank == 0:
         kernels = {k: {"launches": n, "ms_total": round(ms, 3), "share": round(ms / max(1e-9, sum(
@@ -666,12 +791,10 @@ def main(argv=None):
             "wall_s_timed": round(t_wall, 3),
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "flags": flags,
             "variants": variants,
         }
         print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
     return 0
 
 

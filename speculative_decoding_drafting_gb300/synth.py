@@ -254,3 +254,35 @@ def gen_all(w: Workload, rows=None) -> Dict[str, np.ndarray]:
         d["H"] = gen_H(w, idx)
         d["Wgco"] = gen_Wgco(w)
     return d
+
+
+def gen_device(w: Workload, device, seed: int = 0) -> Dict[str, "object"]:
+    """The same recipe as gen_all, drawn on the device from a seeded torch
+    generator (torch tensors; bf16 by round-to-nearest-even).  The values
+    differ from gen_all's (another generator) but the distributions are the
+    same; the benchmark uses this for its timing legs at sizes whose numpy
+    draw would take minutes (the long block's 2.6 billion normals)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 17)
+    sd = {F32: torch.float32, BF16: torch.bfloat16}
+
+    def normal(shape, sigma):
+        return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * sigma
+
+    U = normal((w.R, w.gamma, w.V), w.sigma_u)
+    P = torch.empty((w.R, w.gamma + 1, w.V), dtype=sd[w.p_dtype], device=device)
+    P[:, : w.gamma] = (U + normal((w.R, w.gamma, w.V), w.sigma_pnoise)).to(sd[w.p_dtype])
+    P[:, w.gamma] = (U[:, w.gamma - 1] + normal((w.R, w.V), w.sigma_pnoise)).to(sd[w.p_dtype])
+    d = {
+        "anchor": torch.randint(0, w.V, (w.R,), generator=g, device=device, dtype=torch.int32),
+        "U": U.to(sd[w.u_dtype]),
+        "P": P,
+        "W1": normal((w.V, w.r), w.sigma_w).to(sd[w.w_dtype]),
+        "W2": normal((w.r, w.V), w.sigma_w).to(sd[w.w_dtype]),
+        "c": torch.sigmoid(torch.randn((w.R, w.gamma), generator=g, device=device, dtype=torch.float64)
+                           * w.c_sigma + w.c_mu).to(torch.float32),
+        "sps": torch.from_numpy(gen_sps(w.R, w.gamma, w.rho)).to(device),
+    }
+    del U
+    return d

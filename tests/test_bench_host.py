@@ -5,6 +5,7 @@ import os
 import re
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -87,3 +88,52 @@ def test_source_digest_covers_the_kernel_and_every_header(tmp_path, monkeypatch)
         assert bench.source_digest("k.cu") != d0, f.name
         f.write_text(old)
     assert bench.source_digest("k.cu") == d0
+
+
+def test_flag_accounting_of_the_cpu_leg():
+    """count_flags: positions are compared up to a request's first draft
+    disagreement; a disagreement counts as flagged only where the oracle's
+    margin (draft) or uniform gap (verification) lies inside its band."""
+    R, gamma = 4, 3
+    od = dict(tokens=np.arange(R * gamma, dtype=np.int32).reshape(R, gamma), margin=np.ones((R, gamma)))
+    od["margin"][1, 1] = 5e-5                      # request 1, position 2: inside the Gumbel band
+    ov = dict(out_tokens=np.zeros((R, gamma + 1), np.int32), accept_len=np.full(R, 2, np.int32),
+              min_gap=np.ones(R))
+    ov["min_gap"][2] = 1e-7                        # request 2: a verification decision inside the band
+    g_tok = od["tokens"].copy()
+    g_tok[1, 1] += 1                               # flagged draft disagreement (position 2 of 3)
+    g_tok[3, 0] += 1                               # unflagged draft disagreement at position 1
+    g_out = ov["out_tokens"].copy()
+    g_out[2, 0] = 9                                # flagged verification disagreement
+    g_acc = ov["accept_len"].copy()
+    acc = dict(positions=0, flagged=0, flagged_disagreements=0, unflagged_disagreements=0)
+    bench.count_flags(od, ov, g_tok, g_out, g_acc, acc)
+    assert acc["positions"] == 3 + 2 + 3 + 1
+    assert acc["flagged"] == 1 + 1                 # the draft margin and the verification gap
+    assert acc["flagged_disagreements"] == 2 and acc["unflagged_disagreements"] == 1
+
+
+def test_greedy_cycle_has_no_residual_bytes():
+    """At T = 0 a mismatch emits the target row's argmax: no U_j / P_j re-read."""
+    w = synth.WORKLOADS["greedy"]
+    ab = bench.algorithmic_bytes(w, 200.0, 600.0)
+    assert ab["residual"] == 0
+    assert ab["total"] == ab["draft"] + 600.0 * w.V * 4
+
+
+def test_device_generator_follows_the_recipe():
+    """synth.gen_device draws the gen_all recipe on a torch generator: shapes,
+    storage dtypes, the bonus row built from the last U row, and sigmas."""
+    import torch
+    w = synth.Workload("dev", R=8, gamma=3, V=4096, r=16, T=1.0, u_dtype=synth.BF16, p_dtype=synth.F32)
+    x = synth.gen_device(w, "cpu", seed=3)
+    assert x["U"].shape == (8, 3, 4096) and x["U"].dtype == torch.bfloat16
+    assert x["P"].shape == (8, 4, 4096) and x["P"].dtype == torch.float32
+    assert x["W1"].shape == (4096, 16) and x["W2"].shape == (16, 4096) and x["W2"].dtype == torch.bfloat16
+    assert int(x["anchor"].min()) >= 0 and int(x["anchor"].max()) < 4096
+    noise = x["P"][:, :3].float() - x["U"].float()
+    assert abs(float(noise.std()) - w.sigma_pnoise) < 0.05
+    assert abs(float(x["U"].float().std()) - w.sigma_u) < 0.05
+    assert x["sps"].shape == (8 * 4 + 1,)
+    y = synth.gen_device(w, "cpu", seed=3)
+    assert torch.equal(x["U"], y["U"]) and torch.equal(x["P"], y["P"])

@@ -68,3 +68,18 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     args = types.SimpleNamespace(workload="headline", steps=1, warmup=3)
     assert bench.run_reference(args) == 0
+
+
+def test_gpu_arm_refuses_several_ranks(monkeypatch, capsys):
+    """The GPU arm runs on one GPU only (its kernels share W2 tiles within a
+    cluster by multicast over this GPU's memory): under torchrun with two ranks
+    rank 0 prints one line saying so and every rank exits 0 without work."""
+    import json
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main(["--gpus", "2"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["n_gpus"] == 2 and line["value"] is None and "one GPU" in line["unavailable"]
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--gpus", "2"]) == 0
+    assert capsys.readouterr().out.strip() == ""
