@@ -1,4 +1,4 @@
-// draft_tc.cu -- tensor-core V sweep of one draft step (sm_103a, tcgen05 + TMA).
+// draft_tc.cu -- tensor-core V sweep of one draft step (sm_103a, tcgen05, TMA for W2, cp.async for U).
 //
 // For step k the Markov head's bias is B_k = e_k W2 with e_k = W1[x_{k-1}]
 // ("DSpark: DeepSeek 线上跑的投机解码" blog, section 3.2 MarkovHead; DSpark
@@ -6,12 +6,15 @@
 // requests (an M-group) and a slice of whole 256-column chunks, walked as
 // 128-column tiles:
 //
-//   warp 0  U producer: the U_k tile (128 rows x 128 columns, streamed with
-//           evict-first) into a ring of two stages
+//   warp 0  U producer: the U_k tile (128 rows x 128 columns) into a ring of
+//           stages, by cp.async: one warp instruction moves a row's 512
+//           contiguous bytes (f32; two rows of 256 at bf16) into a padded
+//           shared row, so DRAM sees 512-byte runs of each row and the
+//           epilogue's row-per-thread reads are free of bank conflicts
 //   warp 1  MMA issuer: r/16 tcgen05.mma (M=128, N=128, K=16, bf16 -> f32)
 //           per tile into one of two TMEM accumulators
 //   warp 2  W2 producer: per tile and 64-row K block the W2 stage
-//           (64 x 128 bf16, evict-last) into a ring of six stages
+//           (64 x 128 bf16, evict-last) into a ring of five stages
 //   warps 3-18  first the A operand: the codes e_k of the M-group go to
 //           tensor memory (lane = request row), next to the accumulators,
 //           which leaves shared memory to the U and W2 rings;
@@ -43,18 +46,30 @@ namespace {
 
 constexpr int kBM = 128;           // requests per CTA (one M-group)
 constexpr int kBN = 128;           // vocabulary columns per tile
-constexpr int kNB = 6;             // W2 stages, each 128 columns x 64 rows of r (16 KB)
-constexpr int kNU = 2;             // U stages
+constexpr int kNB = 5;             // W2 stages, each 128 columns x 64 rows of r (16 KB)
+constexpr int kNUMax = 4;          // U stages (at most; see UStage)
 constexpr int kNACC = 2;           // TMEM accumulators (at most; one when A needs the room)
 constexpr int kEpiWG = 4;          // epilogue warpgroups; each owns 32 of a tile's 128 columns
 constexpr int kEpiWarps = 4 * kEpiWG;
 constexpr int kEpiWarp0 = 3;       // warps 0..2: U producer, MMA issuer, W2 producer
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
-constexpr int kUStageBytes = kBM * kBN * 4;   // 64 KB (f32); bf16 uses half
 constexpr int kBStageBytes = 16384;
 
+// U stage of one tile: 128 rows of 128 columns, each row padded by 16 bytes
+// (row r starts 16 r bytes later within the 128-byte bank window than an
+// unpadded row would, so 8 consecutive rows hit 8 different 16-byte slots).
+template <int UT>
+struct UStage {
+    static constexpr int kRowBytes = UT == DSPARK_F32 ? 512 : 256;
+    static constexpr int kPitch = kRowBytes + 16;
+    static constexpr int kBytes = kBM * kPitch;          // 67,584 (f32) or 34,816 (bf16)
+    static constexpr int kN = UT == DSPARK_F32 ? 2 : 4;  // stages: 132 or 136 KB
+};
+
 struct TcParams {
+    const void* U;           // base logits [R, gamma, V] (u_dtype)
+    int gamma;
     const uint16_t* ebf;     // codes e_k, [R][r] bf16 bits
     DraftPartial* parts;     // greedy: this step's partial buffer [R][n_slices]
     float2* cmass;           // sampling: [R][nchunk][4] chunk masses
@@ -82,22 +97,24 @@ struct Smem {
     int* abort_flag;
 };
 
-__host__ __device__ constexpr size_t smem_bytes_for(int /*r*/) {
-    return 1024 + (size_t)kNB * kBStageBytes + (size_t)kNU * kUStageBytes + 256;
+template <int UT>
+__host__ __device__ constexpr size_t smem_bytes_for() {
+    return 1024 + (size_t)kNB * kBStageBytes + (size_t)UStage<UT>::kN * UStage<UT>::kBytes + 256;
 }
 
+template <int UT>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.B = base;
     s.U = s.B + (size_t)kNB * kBStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s.U + (size_t)kNU * kUStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s.U + (size_t)UStage<UT>::kN * UStage<UT>::kBytes);
     s.a_full = bars;
     s.b_full = bars + 1;
     s.b_empty = s.b_full + kNB;
     s.u_full = s.b_empty + kNB;
-    s.u_empty = s.u_full + kNU;
-    s.acc_full = s.u_empty + kNU;
+    s.u_empty = s.u_full + kNUMax;
+    s.acc_full = s.u_empty + kNUMax;
     s.acc_empty = s.acc_full + kNACC;
     s.tmem_holder = reinterpret_cast<uint32_t*>(s.acc_empty + kNACC);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
@@ -158,10 +175,10 @@ __device__ __forceinline__ void issue_mma(const Smem& S, const TcParams& p, uint
 // multicast masks below are compile-time constants
 template <int UT, bool GREEDY, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
-    draft_sweep_tc(const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmU, TcParams p) {
+    draft_sweep_tc(const __grid_constant__ CUtensorMap tmB, TcParams p) {
+    using US = UStage<UT>;
     extern __shared__ uint8_t smem_raw[];
-    const Smem S = carve(smem_raw);
+    const Smem S = carve<UT>(smem_raw);
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x, mg = blockIdx.y;
@@ -178,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.b_full[i], 1);
             mbar_init(&S.b_empty[i], (uint32_t)CS);   // one release per CTA of the cluster
         }
-        for (int i = 0; i < kNU; ++i) {
-            mbar_init(&S.u_full[i], 1);
+        for (int i = 0; i < US::kN; ++i) {
+            mbar_init(&S.u_full[i], 32);                // one cp.async arrival per producer lane
             mbar_init(&S.u_empty[i], kEpiWarps);
         }
         for (int i = 0; i < kNACC; ++i) {
@@ -189,7 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *S.abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmB);
-        prefetch_tmap(&tmU);
     }
     if (warp == 1) tmem_alloc(S.tmem_holder, kTmemCols);
     tc_fence_before();
@@ -199,30 +215,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acol = (uint32_t)(p.nacc * kBN);   // A: columns [acol, acol + nsplit r/2)
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- U producer: runs up to kNU tiles ahead
-            const uint64_t pol_first = policy_evict_first();
-            const uint32_t ubytes = UT == DSPARK_F32 ? (uint32_t)kUStageBytes : (uint32_t)(kUStageBytes / 2);
-            int issued = 0;
-            for (int t = 0; t < nt; ++t) {
-                const int v0 = (t_begin + t) * kBN;
-                const int us = t % kNU;
-                const uint32_t uph = (uint32_t)(t / kNU) & 1u;
-                if (!mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag)) break;
-                mbar_expect_tx(&S.u_full[us], ubytes);
-                uint8_t* dst = S.U + (size_t)us * kUStageBytes;
-                // boxes of 128 rows x 128 bytes: four (f32) or two (bf16) per tile
-                constexpr int nbox = UT == DSPARK_F32 ? 4 : 2;
-                constexpr int bcols = UT == DSPARK_F32 ? 32 : 64;
-#pragma unroll
-                for (int b = 0; b < nbox; ++b)
-                    tma_load_3d(dst + b * 16384, &tmU, &S.u_full[us], v0 + b * bcols, p.k - 1, mg * kBM, pol_first);
-                issued = t + 1;
+        // ---------------- U producer (all 32 lanes): runs up to US::kN tiles ahead.
+        // f32: lane l copies bytes [16 l, 16 l + 16) of one row's 512-byte
+        // segment per instruction; bf16: lanes 0-15 an even row, 16-31 the
+        // next one.  Rows past R and columns past V are zero-filled (never read).
+        constexpr int es = UT == DSPARK_F32 ? 4 : 2;
+        constexpr int rows_per_ins = UT == DSPARK_F32 ? 1 : 2;
+        const int sub = UT == DSPARK_F32 ? 0 : (lane >> 4);
+        const int piece = UT == DSPARK_F32 ? lane : (lane & 15);
+        const char* ubase = static_cast<const char*>(p.U);
+        const size_t row_bytes = (size_t)p.gamma * p.V * es;           // from one request's rows to the next
+        const int nrows = min(kBM, p.R - mg * kBM);                    // rows of this M-group
+        // this lane's first row (row k - 1 of request mg 128 + sub) at column 0
+        const char* lane_row0 = ubase + (size_t)(mg * kBM + sub) * row_bytes + (size_t)(p.k - 1) * p.V * es;
+        const uint64_t pol_first = policy_evict_first();   // U is read once: keep L2 for W2
+        for (int t = 0; t < nt; ++t) {
+            const int us = t % US::kN;
+            const uint32_t uph = (uint32_t)(t / US::kN) & 1u;
+            const bool ok = mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const int v = (t_begin + t) * kBN + piece * (16 / es);     // first column of this lane's piece
+            const bool col_ok = v < p.V;                               // V % (16 / es) == 0: whole pieces
+            uint8_t* dst = S.U + (size_t)us * US::kBytes + sub * US::kPitch + piece * 16;
+            const char* src = lane_row0 + (size_t)v * es;
+#pragma unroll 8
+            for (int i = 0; i < kBM / rows_per_ins; ++i) {
+                const bool in = col_ok && i * rows_per_ins + sub < nrows;
+                cp_async16_zf(dst + i * (rows_per_ins * US::kPitch), in ? src : ubase, in ? 16u : 0u, pol_first);
+                src += rows_per_ins * row_bytes;
             }
-            if (*abort_flag)   // wind down: let the copies this thread issued land
-                for (int t = (issued > kNU ? issued - kNU : 0); t < issued; ++t)
-                    mbar_wait_for(&S.u_full[t % kNU], (uint32_t)(t / kNU) & 1u, kWaitLimitCycles);
+            cp_async_arrive(&S.u_full[us]);
         }
+        cp_async_wait_all();   // no copy of this warp is in flight when the CTA winds down
     } else if (warp == 2) {
         if (lane == 0) {
             // ---------------- W2 producer
@@ -315,33 +339,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tile = t_begin + t;
             const int buf = p.nacc == 2 ? (t & 1) : 0;
             const uint32_t aph = (uint32_t)(p.nacc == 2 ? (t >> 1) : t) & 1u;
-            const int us = t % kNU;
-            const uint32_t uph = (uint32_t)(t / kNU) & 1u;
+            const int us = t % US::kN;
+            const uint32_t uph = (uint32_t)(t / US::kN) & 1u;
             bool ready = mbar_wait(&S.acc_full[buf], aph, abort_flag);
             ready = ready && mbar_wait(&S.u_full[us], uph, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) break;     // the warp stays converged
             tc_fence_after();
-            const uint8_t* ust = S.U + (size_t)us * kUStageBytes;
+            const uint8_t* ust = S.U + (size_t)us * US::kBytes;
             // the thread's 32 columns of the tile: one tensor-memory load and
             // all of its U values before anything waits on them
             float y32[32];
             __syncwarp();
             tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kBN + wg * 32), y32);
             if (UT == DSPARK_F32) {
-                const uint8_t* rowp = ust + wg * 16384 + rit * 128;
+                const uint8_t* rowp = ust + (size_t)rit * US::kPitch + wg * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const float4 f = *reinterpret_cast<const float4*>(rowp + ((c ^ (rit & 7)) << 4));
+                    const float4 f = *reinterpret_cast<const float4*>(rowp + c * 16);
                     y32[4 * c + 0] += f.x;
                     y32[4 * c + 1] += f.y;
                     y32[4 * c + 2] += f.z;
                     y32[4 * c + 3] += f.w;
                 }
             } else {
-                const uint8_t* rowp = ust + (wg >> 1) * 16384 + rit * 128;
+                const uint8_t* rowp = ust + (size_t)rit * US::kPitch + wg * 64;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint4 f = *reinterpret_cast<const uint4*>(rowp + ((((wg & 1) * 4 + c) ^ (rit & 7)) << 4));
+                    const uint4 f = *reinterpret_cast<const uint4*>(rowp + c * 16);
                     const uint32_t w4[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -473,13 +497,22 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, cons
 // M-groups (a cluster shares every W2 stage among its CTAs).
 int cluster_size_for(int n_mg) { return n_mg % 4 == 0 ? 4 : (n_mg % 2 == 0 ? 2 : 1); }
 
-// Clusters of `cs` sweep CTAs that fit on the device at once (0 if unknown).
-int active_clusters(int cs, size_t smem) {
-    static int cache[3][8] = {};   // [log2 cs][r / 64 - 1]
-    const int ci = cs == 4 ? 2 : cs - 1, ri = (int)(smem / 16384) & 7;
-    if (cache[ci][ri]) return cache[ci][ri];
-    auto kern = cs == 4 ? draft_sweep_tc<DSPARK_F32, false, 4> : draft_sweep_tc<DSPARK_F32, false, 2>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+// Clusters of `cs` sweep CTAs (U storage UT) that fit on the device at once
+// (0 if unknown), per device.
+template <int UT>
+int active_clusters(int cs) {
+    constexpr int kMaxDev = 64;
+    static int cache[kMaxDev][3] = {};   // [device][log2 cs]
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    const int ci = cs == 4 ? 2 : cs - 1;
+    if (cache[dev][ci]) return cache[dev][ci];
+    const size_t smem = smem_bytes_for<UT>();
+    auto kern = cs == 4 ? draft_sweep_tc<UT, false, 4> : draft_sweep_tc<UT, false, 2>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, cs, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -496,7 +529,7 @@ int active_clusters(int cs, size_t smem) {
         (void)cudaGetLastError();
         return 0;
     }
-    cache[ci][ri] = n;
+    cache[dev][ci] = n;
     return n;
 }
 
@@ -506,6 +539,7 @@ struct TcPlan {
 };
 
 // One wave: as many column slices as co-resident clusters allow.
+template <int UT>
 TcPlan plan_for(const DraftArgs& a) {
     const int n_mg = (a.R + kBM - 1) / kBM;
     const int nchunk = (a.V + 255) / 256;
@@ -513,7 +547,7 @@ TcPlan plan_for(const DraftArgs& a) {
     pl.cs = cluster_size_for(n_mg);
     int ctas = num_sms();
     if (pl.cs > 1) {
-        const int nc = active_clusters(pl.cs, smem_bytes_for(a.r));
+        const int nc = active_clusters<UT>(pl.cs);
         if (nc > 0)
             ctas = nc * pl.cs;
         else
@@ -529,8 +563,8 @@ TcPlan plan_for(const DraftArgs& a) {
 
 template <int UT, bool GREEDY>
 cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
-    CUtensorMap tmB, tmU;
-    const TcPlan pl = plan_for(a);
+    CUtensorMap tmB;
+    const TcPlan pl = plan_for<UT>(a);
     if (pl.nslices * kEpiWG != a.n_slices) return cudaErrorInvalidValue;
     // B: W2 [r rows x V]; a copy is one 64-column swizzle atom of 64 K rows,
     // or the piece of it one CTA of a cluster loads (64 / (cs / 2) rows)
@@ -541,17 +575,9 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
         if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, str, box))
             return cudaErrorInvalidValue;
     }
-    // U: [R, gamma, V] as a 3-d tensor (V, gamma, R); box 128 B x 1 x 128 rows
-    {
-        const size_t es = UT == DSPARK_F32 ? 4 : 2;
-        cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
-        cuuint64_t str[2] = {(cuuint64_t)a.V * es, (cuuint64_t)a.gamma * a.V * es};
-        cuuint32_t box[3] = {UT == DSPARK_F32 ? 32u : 64u, 1u, (cuuint32_t)kBM};
-        if (!make_map(&tmU, UT == DSPARK_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      3, const_cast<void*>(a.U), dims, str, box))
-            return cudaErrorInvalidValue;
-    }
     TcParams p;
+    p.U = a.U;
+    p.gamma = a.gamma;
     p.ebf = a.ebf;
     // RNN codes tanh(out) are f32: three bf16 terms (exact); Markov codes are W1 rows
     p.nsplit = a.rnn ? 3 : 1;
@@ -568,7 +594,7 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.ntiles = (a.V + kBN - 1) / kBN;
     p.nslices = pl.nslices;
     p.c2 = a.T > 0.f ? kLog2e / a.T : 1.f;
-    const size_t smem = smem_bytes_for(a.r);
+    const size_t smem = smem_bytes_for<UT>();
     auto kern = pl.cs == 4 ? draft_sweep_tc<UT, GREEDY, 4>
                 : pl.cs == 2 ? draft_sweep_tc<UT, GREEDY, 2> : draft_sweep_tc<UT, GREEDY, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -588,7 +614,7 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     prof_begin(kPDraftSweepTc, s);
-    e = cudaLaunchKernelEx(&cfg, kern, tmB, tmU, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmB, p);
     prof_end(s);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -608,11 +634,13 @@ bool draft_tc_supported(const DraftArgs& a) {
     if (a.r % 64 != 0 || a.r > 256) return false;
     if (a.V % 8 != 0) return false;
     if ((reinterpret_cast<uintptr_t>(a.U) & 15) || (reinterpret_cast<uintptr_t>(a.W2) & 15)) return false;
-    if (smem_bytes_for(a.r) > 232448) return false;
+    if (smem_bytes_for<DSPARK_F32>() > 232448 || smem_bytes_for<DSPARK_BF16>() > 232448) return false;
     return encode_fn() != nullptr;
 }
 
-int draft_tc_slices(const DraftArgs& a) { return plan_for(a).nslices * kEpiWG; }
+int draft_tc_slices(const DraftArgs& a) {
+    return (a.u_dtype == DSPARK_F32 ? plan_for<DSPARK_F32>(a) : plan_for<DSPARK_BF16>(a)).nslices * kEpiWG;
+}
 
 cudaError_t launch_draft_tc_sweep(DraftArgs& a, int k, cudaStream_t s) {
     const bool greedy = !(a.T > 0.f);

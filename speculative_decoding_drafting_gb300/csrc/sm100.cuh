@@ -134,6 +134,15 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, 
 }
 
 // ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy that reads `src_bytes` (16 or 0) bytes and
+// fills the rest of the 16 with zeros (0: nothing is read, src may be any
+// valid address), with an L2 cache policy (createpolicy).
+__device__ __forceinline__ void cp_async16_zf(void* dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
