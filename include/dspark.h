@@ -98,6 +98,23 @@ const char* dspark_version(void);
 int dspark_workspace_status(void* ws, void* stream);
 
 /*
+ * Bounded waits (no counterpart on the pages).  Every wait of a kernel on
+ * another thread's progress (a pipeline stage, a peer CTA's copy) gives up
+ * after a limit of SM cycles, records DSPARK_ERR_TIMEOUT in the workspace's
+ * status word and winds the kernel down without faulting.  The limit is
+ * 2^32 cycles (2 to 4 s at 2 to 1 GHz) unless set here for the calls that
+ * use workspace `ws` (limit_cycles = 0 restores the default).
+ * test_withhold = 1 is a test hook: the next draft call on `ws` that runs the
+ * tensor-core sweep withholds the first U stage of its first step (no copy is
+ * issued for it), so that the bounded wait on it runs out and the call ends
+ * with DSPARK_ERR_TIMEOUT in the status word; set 0 to turn it off.  The
+ * values live in the workspace header (a fresh zeroed workspace has the
+ * defaults).  Synchronises `stream`.  Errors: INVALID_ARG for a null or
+ * misaligned workspace or another test_withhold, CUDA for a failed copy.
+ */
+int dspark_workspace_set_wait(void* ws, uint64_t limit_cycles, int test_withhold, void* stream);
+
+/*
  * The device-accessible address of a pinned (page-locked) host buffer, so
  * that kernels read it in place over the host link (zero copy).  The input
  * arrays of the calls below may be such addresses: verification, for

@@ -84,6 +84,7 @@ def load(build_if_missing: bool = True):
         L.dspark_sts_fit.argtypes = [P, P, i32, i32, P, i32, i32, P, P, P, P, P, sz, P]
         L.dspark_sts_apply.argtypes = [P, i32, i32, P, P, P]
         L.dspark_philox4x32_10.argtypes = [P, P, P, i32, P]
+        L.dspark_workspace_set_wait.argtypes = [P, u64, i32, P]
         L.dspark_profile_enable.argtypes = [i32]
         L.dspark_profile_collect.argtypes = [P, P, i32]
         L.dspark_profile_kernel_name.argtypes = [i32]
@@ -92,7 +93,7 @@ def load(build_if_missing: bool = True):
                      "dspark_verify", "dspark_verify_staged", "dspark_schedule", "dspark_schedule_async",
                      "dspark_schedule_threshold",
                      "dspark_sts_fit",
-                     "dspark_sts_apply", "dspark_philox4x32_10",
+                     "dspark_sts_apply", "dspark_philox4x32_10", "dspark_workspace_set_wait",
                      "dspark_workspace_status", "dspark_profile_enable", "dspark_profile_collect"):
             getattr(L, name).restype = i32
         _lib = L
@@ -209,6 +210,13 @@ def version() -> str:
 
 def workspace_status(ws: torch.Tensor, stream=None) -> int:
     return load().dspark_workspace_status(_p(ws), _stream(stream))
+
+
+def workspace_set_wait(ws: torch.Tensor, limit_cycles: int = 0, test_withhold: int = 0, stream=None) -> None:
+    """Bounded-wait limit (SM cycles, 0 = the default 2^32) and the test hook
+    of the calls that use workspace ``ws`` (``dspark_workspace_set_wait``)."""
+    code = load().dspark_workspace_set_wait(_p(ws), int(limit_cycles), int(test_withhold), _stream(stream))
+    _check("dspark_workspace_set_wait", code)
 
 
 def draft_workspace_bytes(R, gamma, V, r, d=0) -> int:

@@ -118,6 +118,21 @@ int dspark_workspace_status(void* ws, void* stream) {
     return DSPARK_OK;
 }
 
+int dspark_workspace_set_wait(void* ws, uint64_t limit_cycles, int test_withhold, void* stream) {
+    if (!ws || !aligned256(ws) || (test_withhold != 0 && test_withhold != 1)) return DSPARK_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // header bytes [4, 20): test_withhold (u32), wait_limit (u64), the marker (u32)
+    struct {
+        uint32_t withhold;
+        uint32_t limit_lo, limit_hi;
+        uint32_t marker;
+    } h = {(uint32_t)test_withhold, (uint32_t)limit_cycles, (uint32_t)(limit_cycles >> 32), kWaitMarker};
+    static_assert(sizeof(h) == 16, "four words");
+    if (cudaMemcpyAsync(static_cast<char*>(ws) + 4, &h, sizeof h, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
 size_t dspark_draft_workspace_size(int R, int gamma, int V, int r, int d) {
     if (R < 1 || gamma < 1 || gamma > 64 || V < 2 || V > (1 << 20) || r < 1 || r > 1024 || d < 0) return 0;
     return draft_workspace_bytes(R, gamma, V, r, d);

@@ -22,8 +22,27 @@ enum : uint32_t { kStatBadToken = 1u, kStatTimeout = 2u };
 
 struct WsHeader {
     uint32_t status;
-    uint32_t pad[63];   // keep what follows 256-byte aligned
+    uint32_t test_withhold;   // test hook: 1 = the draft sweep's U producer withholds its first stage
+    uint64_t wait_limit;      // SM cycles a bounded wait may take (0: the default, 2^32)
+    uint32_t wait_marker;     // kWaitMarker when dspark_workspace_set_wait wrote the two fields above
+    uint32_t pad[59];         // keep what follows 256-byte aligned
 };
+static_assert(sizeof(WsHeader) == 256, "the workspace header is 256 bytes");
+// The two fields count only with the marker, so that the arbitrary contents
+// of a workspace nobody set (only its status word must start at zero) leave
+// the defaults in force.
+constexpr uint32_t kWaitMarker = 0x57414954u;
+
+// The bounded-wait limit and the test hook a workspace carries.
+__device__ __forceinline__ uint64_t ws_wait_limit(const void* ws) {
+    const WsHeader* h = static_cast<const WsHeader*>(ws);
+    const uint64_t v = h->wait_marker == kWaitMarker ? h->wait_limit : 0;
+    return v ? v : (1ull << 32);
+}
+__device__ __forceinline__ uint32_t ws_test_withhold(const void* ws) {
+    const WsHeader* h = static_cast<const WsHeader*>(ws);
+    return h->wait_marker == kWaitMarker ? h->test_withhold : 0u;
+}
 
 __device__ __forceinline__ void raise_status(void* ws, uint32_t bits) {
     atomicOr(reinterpret_cast<uint32_t*>(ws), bits);

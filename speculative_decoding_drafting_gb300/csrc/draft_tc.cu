@@ -94,7 +94,7 @@ struct Smem {
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint32_t* tmem_holder;
-    int* abort_flag;
+    WaitState* wst;
 };
 
 template <int UT>
@@ -116,8 +116,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.u_empty = s.u_full + kNUMax;
     s.acc_full = s.u_empty + kNUMax;
     s.acc_empty = s.acc_full + kNACC;
-    s.tmem_holder = reinterpret_cast<uint32_t*>(s.acc_empty + kNACC);
-    s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
+    s.wst = reinterpret_cast<WaitState*>(s.acc_empty + kNACC);
+    s.tmem_holder = reinterpret_cast<uint32_t*>(s.wst + 1);
     return s;
 }
 
@@ -128,7 +128,7 @@ template <int NS, int CS>
 __device__ __forceinline__ void issue_mma(const Smem& S, const TcParams& p, uint32_t tmem, uint32_t acol, int nt,
                                           int kblocks) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
-    volatile int* abort_flag = S.abort_flag;
+    volatile WaitState* abort_flag = S.wst;
     // two accumulators, or one when three A blocks take the room (NS = 3, r > 128)
     const bool two = NS == 1 || p.nacc == 2;
     bool ok = mbar_wait(S.a_full, 0, abort_flag);
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_end = min(2 * (int)((long long)(slice + 1) * p.nchunk / p.nslices), p.ntiles);
     const int nt = t_end - t_begin;
     const int kblocks = p.r / 64;
-    volatile int* abort_flag = S.abort_flag;
+    volatile WaitState* abort_flag = S.wst;
 
     if (threadIdx.x == 0) {
         mbar_init(S.a_full, kEpiWarps);
@@ -203,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.acc_full[i], 1);
             mbar_init(&S.acc_empty[i], kEpiWarps);
         }
-        *S.abort_flag = 0;
+        S.wst->abort = 0;
+        S.wst->limit = ws_wait_limit(p.ws);
         fence_mbar_init();
         prefetch_tmap(&tmB);
     }
@@ -229,11 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this lane's first row (row k - 1 of request mg 128 + sub) at column 0
         const char* lane_row0 = ubase + (size_t)(mg * kBM + sub) * row_bytes + (size_t)(p.k - 1) * p.V * es;
         const uint64_t pol_first = policy_evict_first();   // U is read once: keep L2 for W2
+        // test hook (workspace header): at the first step, issue nothing for
+        // the first tile, so that the epilogue's bounded wait on that stage
+        // runs out with no copy in flight on it
+        const bool withhold = p.k == 1 && ws_test_withhold(p.ws) == 1u;
         for (int t = 0; t < nt; ++t) {
             const int us = t % US::kN;
             const uint32_t uph = (uint32_t)(t / US::kN) & 1u;
             const bool ok = mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
+            if (withhold && t == 0) continue;
             const int v = (t_begin + t) * kBN + piece * (16 / es);     // first column of this lane's piece
             const bool col_ok = v < p.V;                               // V % (16 / es) == 0: whole pieces
             uint8_t* dst = S.U + (size_t)us * US::kBytes + sub * US::kPitch + piece * 16;
@@ -280,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // the last release of every stage (the peers' included) lands
             // here before the CTA may exit
-            for (int g = (issued > kNB ? issued - kNB : 0); g < issued && !*abort_flag; ++g)
+            for (int g = (issued > kNB ? issued - kNB : 0); g < issued && !abort_flag->abort; ++g)
                 mbar_wait(&S.b_empty[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag);
-            if (*abort_flag) {
+            if (abort_flag->abort) {
                 for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
-                    mbar_wait_for(&S.b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitCycles);
+                    mbar_wait_for(&S.b_full[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag->limit);
             }
         }
     } else if (warp == 1) {
@@ -430,12 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!GREEDY && ((tile & 1) || t == nt - 1)) {
                 // end of a 256-column chunk (or of the vocabulary)
-                if (row_ok && !*abort_flag)
+                if (row_ok && !abort_flag->abort)
                     p.cmass[((size_t)row * p.nchunk + (tile >> 1)) * 4 + wg] = make_float2(mref, csum);
                 csum = 0.f;
             }
         }
-        if (GREEDY && row_ok && !*abort_flag) {
+        if (GREEDY && row_ok && !abort_flag->abort) {
             DraftPartial part;
             part.m = -INFINITY;
             part.s = 0.0;
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) {
+    if (abort_flag->abort) {
         // a peer's multicast copies or releases may still be on their way to
         // this CTA's shared memory: give them a millisecond before leaving
         if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);

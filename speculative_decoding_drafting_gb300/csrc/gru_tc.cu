@@ -58,7 +58,7 @@ struct GruSmem {
     uint64_t* empty;
     uint64_t* acc_full;
     uint32_t* tmem_holder;
-    int* abort_flag;
+    WaitState* wst;
 };
 
 __device__ __forceinline__ GruSmem gru_carve(uint8_t* raw) {
@@ -69,8 +69,8 @@ __device__ __forceinline__ GruSmem gru_carve(uint8_t* raw) {
     s.full = bars;
     s.empty = bars + kGStages;
     s.acc_full = bars + 2 * kGStages;
-    s.tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kGStages + 1);
-    s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
+    s.wst = reinterpret_cast<WaitState*>(bars + 2 * kGStages + 1);
+    s.tmem_holder = reinterpret_cast<uint32_t*>(s.wst + 1);
     return s;
 }
 
@@ -85,14 +85,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int j0 = blockIdx.x * kGJ, m0 = blockIdx.y * kGM, part = blockIdx.z;
     const int kb0 = part * p.per_part, kb1 = min(kb0 + p.per_part, p.kblocks);
     const int nkb = kb1 - kb0;
-    volatile int* abort_flag = S.abort_flag;
+    volatile WaitState* abort_flag = S.wst;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kGStages; ++i) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], 1);
         }
         mbar_init(S.acc_full, 1);
-        *abort_flag = 0;
+        S.wst->abort = 0;
+        S.wst->limit = ws_wait_limit(p.ws);
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -130,9 +131,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
                 issued = i + 1;
             }
-            if (*abort_flag)   // wind down: let the copies this thread issued land
+            if (abort_flag->abort)   // wind down: let the copies this thread issued land
                 for (int i = (issued > kGStages ? issued - kGStages : 0); i < issued; ++i)
-                    mbar_wait_for(&S.full[i % kGStages], (uint32_t)(i / kGStages) & 1u, kWaitLimitCycles);
+                    mbar_wait_for(&S.full[i % kGStages], (uint32_t)(i / kGStages) & 1u, abort_flag->limit);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) {
+    if (abort_flag->abort) {
         // tensor-core work may still be in flight: give it a millisecond
         // before the tensor memory is released
         if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);

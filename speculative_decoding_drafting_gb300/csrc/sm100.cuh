@@ -50,21 +50,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitCycles SM cycles (2 to 4 s at 2 to 1 GHz; or at once when
-// another thread of the CTA already gave up) and returns false; the caller
-// then winds down without touching the pipeline.
-constexpr uint64_t kWaitLimitCycles = 1ull << 32;
+// Per-CTA state of the bounded waits, in shared memory: the limit (SM
+// cycles; from the workspace header, 2^32 = 2 to 4 s at 2 to 1 GHz unless a
+// caller set another) and the abort flag that the first thread whose wait ran
+// out raises, so that every later wait of the CTA gives up at once.
+struct WaitState {
+    int abort;
+    int pad;
+    uint64_t limit;
+};
+constexpr uint64_t kWaitLimitCycles = 1ull << 32;   // the default limit
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// after w->limit SM cycles (or at once when another thread of the CTA
+// already gave up) and returns false; the caller then winds down without
+// touching the pipeline.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile WaitState* w) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = sm_cycles();
+    const uint64_t limit = w->limit;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
-            if (*abort_flag) return false;
-            if (sm_cycles() - t0 > kWaitLimitCycles) {
-                *abort_flag = 1;
+            if (w->abort) return false;
+            if (sm_cycles() - t0 > limit) {
+                w->abort = 1;
                 return false;
             }
         }

@@ -90,7 +90,7 @@ struct MmaBars {
 // CTAs of the cluster.
 template <int NS, int CS>
 __device__ __forceinline__ void issue_mma(const MmaBars& mb, const uint8_t* sB, uint32_t tmem, int r, int nt,
-                                          int kblocks, volatile int* abort_flag) {
+                                          int kblocks, volatile WaitState* abort_flag) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, true);
     bool ok = mbar_wait(mb.a_full, 0, abort_flag);
     tc_fence_after();
@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* s_empty = s_full + kNS;
     uint64_t* acc_full = s_empty + kNS;
     uint64_t* acc_empty = acc_full + kNACC;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + kNACC);
-    volatile int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    WaitState* wst = reinterpret_cast<WaitState*>(acc_empty + kNACC);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(wst + 1);
+    volatile WaitState* abort_flag = wst;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c_begin = (int)((long long)slice * p.nch256 / p.nslices);
@@ -187,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], kEpiWarps);
         }
-        *abort_flag = 0;
+        wst->abort = 0;
+        wst->limit = ws_wait_limit(p.ws);
         fence_mbar_init();
         prefetch_tmap(&tmB);
     }
@@ -223,11 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // the last release of every stage (the peers' included) lands
             // here before the CTA may exit
-            for (int g = (issued > kNB ? issued - kNB : 0); g < issued && !*abort_flag; ++g)
+            for (int g = (issued > kNB ? issued - kNB : 0); g < issued && !abort_flag->abort; ++g)
                 mbar_wait(&b_empty[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag);
-            if (*abort_flag) {
+            if (abort_flag->abort) {
                 for (int g = (issued > kNB ? issued - kNB : 0); g < issued; ++g)
-                    mbar_wait_for(&b_full[g % kNB], (uint32_t)(g / kNB) & 1u, kWaitLimitCycles);
+                    mbar_wait_for(&b_full[g % kNB], (uint32_t)(g / kNB) & 1u, abort_flag->limit);
             }
         }
     } else if (warp == 1) {
@@ -404,19 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     csum += (i < ncols && w > 0.f) ? w : 0.f;
                 }
             }
-            if (((tile & 3) == 3 || t == nt - 1) && row_ok && !*abort_flag) {
+            if (((tile & 3) == 3 || t == nt - 1) && row_ok && !abort_flag->abort) {
                 p.rpart[((size_t)r * p.nch256 + (tile >> 2)) * 4 + wg] = csum;
                 csum = 0.f;
             }
         }
         // the arrivals of the last fills (past the final tile) land before the CTA leaves
-        if (fok && !*abort_flag)
+        if (fok && !abort_flag->abort)
             for (int tt = nt; tt < nt + kNS; ++tt)
                 mbar_wait(&s_full[tt % kNS], (uint32_t)(tt / kNS) & 1u, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) {
+    if (abort_flag->abort) {
         // a peer's multicast copies or releases may still be on their way to
         // this CTA's shared memory: give them a millisecond before leaving
         if (threadIdx.x == 0) raise_status(p.ws, kStatTimeout);
