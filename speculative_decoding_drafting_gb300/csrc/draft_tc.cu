@@ -3,8 +3,9 @@
 // For step k the Markov head's bias is B_k = e_k W2 with e_k = W1[x_{k-1}]
 // ("DSpark: DeepSeek 线上跑的投机解码" blog, section 3.2 MarkovHead; DSpark
 // explainer, section 03, q_k = softmax(U_k + B_k)).  One CTA owns 128
-// requests (an M-group) and a slice of whole 256-column chunks, walked as
-// 128-column tiles:
+// requests (an M-group) and a slice of whole 256-column chunks (every
+// nslices-th chunk, upwards at odd steps and downwards at even ones), walked
+// as 128-column tiles:
 //
 //   warp 0  U producer: the U_k tile (128 rows x 128 columns) into a ring of
 //           stages, by cp.async: one warp instruction moves a row's 512
@@ -182,10 +183,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slice = blockIdx.x, mg = blockIdx.y;
-    // slices hold whole 256-column chunks (two tiles each)
-    const int t_begin = 2 * (int)((long long)slice * p.nchunk / p.nslices);
-    const int t_end = min(2 * (int)((long long)(slice + 1) * p.nchunk / p.nslices), p.ntiles);
-    const int nt = t_end - t_begin;
+    // a slice holds the 256-column chunks slice, slice + nslices, ... (two
+    // tiles each; the last chunk of the vocabulary may have one), so that at
+    // any moment the slices of an M-group read neighbouring chunks of each
+    // row.  Odd steps walk them upwards, even steps downwards: the W2 columns
+    // a step touched last, the likeliest to be still in L2, come first in the
+    // next step.  Inside a chunk the tiles go upwards.
+    const int nch_mine = p.nchunk > slice ? (p.nchunk - slice + p.nslices - 1) / p.nslices : 0;
+    const bool part = nch_mine > 0 && slice + (nch_mine - 1) * p.nslices == p.nchunk - 1 && (p.ntiles & 1);
+    const int nt = 2 * nch_mine - (part ? 1 : 0);
+    const bool down = (p.k & 1) == 0;
+    auto tile_of = [&](int t) {
+        const int u = down && part ? t + 1 : t;     // downwards, the one-tile chunk comes first
+        const int j = down ? nch_mine - 1 - (u >> 1) : (u >> 1);
+        const int half = (down && part && t == 0) ? 0 : (u & 1);
+        return 2 * (slice + j * p.nslices) + half;
+    };
     const int kblocks = p.r / 64;
     volatile WaitState* abort_flag = S.wst;
 
@@ -240,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok = mbar_wait(&S.u_empty[us], uph ^ 1u, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             if (withhold && t == 0) continue;
-            const int v = (t_begin + t) * kBN + piece * (16 / es);     // first column of this lane's piece
+            const int v = tile_of(t) * kBN + piece * (16 / es);     // first column of this lane's piece
             const bool col_ok = v < p.V;                               // V % (16 / es) == 0: whole pieces
             uint8_t* dst = S.U + (size_t)us * US::kBytes + sub * US::kPitch + piece * 16;
             const char* src = lane_row0 + (size_t)v * es;
@@ -274,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&S.b_empty[bs], bph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(&S.b_full[bs], (uint32_t)kBStageBytes);
                 uint8_t* st = S.B + (size_t)bs * kBStageBytes;
-                const int v0 = (t_begin + t) * kBN;
+                const int v0 = tile_of(t) * kBN;
                 if (CS == 1) {
                     tma_load_2d(st, &tmB, &S.b_full[bs], v0, kb * 64, pol_last);
                     tma_load_2d(st + 8192, &tmB, &S.b_full[bs], v0 + 64, kb * 64, pol_last);
@@ -342,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float kb = -INFINITY;
         int ib = INT_MAX;
         for (int t = 0; t < nt; ++t) {
-            const int tile = t_begin + t;
+            const int tile = tile_of(t);
             const int buf = p.nacc == 2 ? (t & 1) : 0;
             const uint32_t aph = (uint32_t)(p.nacc == 2 ? (t >> 1) : t) & 1u;
             const int us = t % US::kN;
@@ -399,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (GREEDY) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (y[i] > kb) {          // columns rise along the thread: first max wins ties
+                        if (y[i] > kb || (y[i] == kb && v0 + i < ib)) {   // ties: the lowest column
                             kb = y[i];
                             ib = v0 + i;
                         }
@@ -434,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!GREEDY && ((tile & 1) || t == nt - 1)) {
+            if (!GREEDY && ((tile & 1) || tile == p.ntiles - 1)) {
                 // end of a 256-column chunk (or of the vocabulary)
                 if (row_ok && !abort_flag->abort)
                     p.cmass[((size_t)row * p.nchunk + (tile >> 1)) * 4 + wg] = make_float2(mref, csum);
