@@ -277,9 +277,8 @@ size_t dspark_verify_workspace_size(int R, int gamma, int V, int r);
  * are read in windows of rows [0, 1), [1, 3), [3, 7), [7, gamma + 1): a
  * request reads the windows up to the one that holds its first rejection
  * (or its bonus row) and no further.
- * Requirements as for drafting, and V <= 2^18 when T > 0 (the sampling tree
- * keeps at most 1024 top-level nodes of 256 words; greedy takes V <= 2^20);
- * larger vocabularies return DSPARK_ERR_SHAPE before anything is enqueued.
+ * Requirements as for drafting (V <= 2^20; larger vocabularies return
+ * DSPARK_ERR_SHAPE before anything is enqueued).
  */
 int dspark_verify(const void* P, int p_dtype, const void* U, int u_dtype,
                   const void* W2, int w_dtype,

@@ -239,7 +239,6 @@ int dspark_verify_staged(const void* P, int p_dtype, const void* U, int u_dtype,
     if (st) return st;
     st = check_vocab(V, p_dtype);
     if (st) return st;
-    if (temperature > 0.f && V > (1 << 18)) return DSPARK_ERR_SHAPE;   // the sampling tree's top level
     if (!P || !tokens || !out_tokens || !accept_len || !n_out) return DSPARK_ERR_INVALID_ARG;
     if (temperature > 0.f && (!U || !W2 || !q_tok || !lse || !code)) return DSPARK_ERR_INVALID_ARG;
     if (!aligned16(P) || (p_stage && !aligned16(p_stage))) return DSPARK_ERR_INVALID_ARG;

@@ -94,6 +94,7 @@ struct VerifyArgs {
     int* rej_count;     // number of requests that rejected a draft
     int* wcount_alive;  // [6] requests live at each verification wave (index = wave)
     int* alive;         // [2][R] live requests of the current and the next wave
+    int* live_mark;     // [R] the wave a request is still undecided in (0: decided); written by every acceptance pass
     int* rej_list;      // [R] those requests, in arrival order
     uint16_t* a_res;    // [3][rpad][r] bf16 terms hi, mid, lo of the rejecting requests' codes e_j (compact order; rpad = R rounded up to 128)
     uint32_t* vflags;   // bit 0: some rejecting code is not bf16-exact

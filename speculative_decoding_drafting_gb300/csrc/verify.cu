@@ -168,13 +168,16 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
 }
 
 // ------------------------------------------------------------------ accept
-// One CTA per live request of wave w.  Warp v reduces the window's rows
+// One CTA per request; in wave w only the requests still undecided
+// (live_mark[r] == w, every request in wave 1) go past the wait.  The
+// drafted tokens, their target logits P_k[x_k], q(x_k) and the acceptance
+// uniforms are inputs of the call, so they are fetched before the wait,
+// under the tail of pass 1.  After it, warp v reduces the window's rows
 // lo + v, lo + v + 8, ... of pass 1's partials (the log-sum-exp of each P
-// row, or its argmax at T = 0) while the drafted tokens and their target
-// logits P_k[x_k] are fetched, which do not depend on it; then every
-// position of the window is tested at once and the first rejection decides
-// (everything after it is discarded).  A request that passes the whole
-// window goes to the next wave's list, unless the window held its bonus row.
+// row, or its argmax at T = 0); then every position of the window is tested
+// at once and the first rejection decides (everything after it is
+// discarded).  A request that passes the whole window goes to the next
+// wave's list, unless the window held its bonus row.
 template <int PT, bool GREEDY>
 __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
     __shared__ double s_lse[65];
@@ -183,16 +186,35 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
     __shared__ float s_px[64];
     __shared__ int s_first;
     pdl_launch_dependents();
-    pdl_wait();
-    if ((int)blockIdx.x >= live_count(A, w)) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
-    const int r = live_request(A, w, blockIdx.x);
+    const int r = blockIdx.x;
     const int G1 = A.gamma + 1, NCH = A.nch, V = A.V;
     const int L = verify_len_of(A, r);
     const int lo = wave_lo(w, A.unit_waves), hi = wave_hi(w, G1, A.unit_waves);
     const int rhi = min(hi - 1, L);        // the window's rows this request needs: lo .. rhi
     const int npos = min(hi, L) - lo;      // positions lo + 1 .. lo + npos are tested
     const float invT = GREEDY ? 1.f : 1.f / A.T;
+    const bool staged = A.Pv != A.P;       // P_stage is filled by pass 1: read it after the wait
+    int x = 0;
+    bool bad_x = false;
+    float px_raw = 0.f, qx = 1.f;
+    double u = 0.0;
+    if (tid < npos) {
+        const int row = lo + tid, k = row + 1;
+        x = A.tokens[(size_t)r * A.gamma + row];
+        if (x < 0 || x >= V) {
+            bad_x = true;
+            x = 0;
+        }
+        if (!GREEDY) {
+            if (!staged) px_raw = ld_elem(A.P, PT, ((size_t)r * G1 + row) * (size_t)V + x);
+            qx = A.q_tok[(size_t)r * A.gamma + row];
+            const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
+            u = rng_uniform_d(philox_key(A.seed), req, (uint32_t)k, 1u, 0u);
+        }
+    }
+    pdl_wait();
+    if (w > 1 && A.live_mark[r] != w) return;
     int32_t* out = A.out_tokens + (size_t)r * G1;
     if (w == 1 && tid < G1) {
         // outputs start empty; lse_p rows computed in this wave are written below
@@ -201,16 +223,11 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
         if (A.p_tok && tid < A.gamma) A.p_tok[(size_t)r * A.gamma + tid] = NAN;
     }
     if (tid == 0) s_first = INT_MAX;
-    // drafted token x_k and its raw target logit, thread k - lo - 1 for position k
     if (tid < npos) {
         const int row = lo + tid;
-        int x = A.tokens[(size_t)r * A.gamma + row];
-        if (x < 0 || x >= V) {
-            raise_status(A.ws, kStatBadToken);
-            x = 0;
-        }
+        if (bad_x) raise_status(A.ws, kStatBadToken);
         s_x[row] = x;
-        if (!GREEDY) s_px[row] = ld_elem(A.Pv, PT, ((size_t)r * G1 + row) * (size_t)V + x);
+        if (!GREEDY) s_px[row] = staged ? ld_elem(A.Pv, PT, ((size_t)r * G1 + row) * (size_t)V + x) : px_raw;
     }
     const float2* parts = A.vparts + (size_t)r * G1 * NCH;
     for (int row = lo + warp; row <= rhi; row += blockDim.x >> 5) {
@@ -269,9 +286,7 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
         } else {
             // p(x) = exp(P_x / T - lse_P), the difference formed in double
             px = exp_from_double((double)s_px[row] * (double)invT - s_lse[row]);
-            const double ratio = px / (double)A.q_tok[(size_t)r * A.gamma + row];
-            const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
-            const double u = rng_uniform_d(philox_key(A.seed), req, (uint32_t)k, 1u, 0u);
+            const double ratio = px / (double)qx;
             rej = !(u < ratio);
         }
         if (rej) atomicMin(&s_first, k);
@@ -285,6 +300,7 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
         else if (GREEDY && k == j) out[row] = s_arg[row];   // the target's own token replaces x_j
     }
     if (tid == 0) {
+        A.live_mark[r] = 0;
         if (j) {
             A.vstate[r] = GREEDY ? make_int2(kModeDone, 0) : make_int2(kModeResidual, j);
             A.accept_len[r] = j - 1;
@@ -300,6 +316,7 @@ __global__ void __launch_bounds__(256) verify_accept(VerifyArgs A, int w) {
             A.accept_len[r] = L;
             A.n_out[r] = L + 1;
         } else {
+            A.live_mark[r] = w + 1;
             const int slot = atomicAdd(A.wcount_alive + w + 1, 1);
             A.alive[(size_t)((w + 1) & 1) * A.R + slot] = r;
         }
@@ -400,53 +417,60 @@ __global__ void __launch_bounds__(256) verify_residual_generic(VerifyArgs A) {
 }
 
 // ------------------------------------------------------------------ sample
-// Inverse CDF down the binary sum tree over leaves[0 .. 2^levels): node k of
-// the heap (root 1, children 2k and 2k + 1, leaf i = node 2^levels + i)
-// holds the mass under it; at depth d the walk draws u = u_level[d] and goes
-// left iff u (mL + mR) < mL.  The uniforms do not depend on the path, so the
-// caller draws them in parallel beforehand.  The inner nodes are built by
-// eight warps, each over its own subtree with warp barriers only, then the
-// few nodes above the subtrees by one thread; the chosen leaf goes to *out.
-// Every thread of the (256-thread) block must call it.
-__device__ void tree_descend(const double* leaves, double* tree, int levels, const double* u_level, int* out) {
+// Inverse CDF down the binary sum tree over leaves[0 .. 2^levels), levels
+// <= 10: node k of the heap (root 1, children 2k and 2k + 1, leaf i = node
+// 2^levels + i) at depth d holds the mass under it, and the walk goes right
+// at k unless u_level[d] (mL + mR) < mL.  The uniforms do not depend on the
+// path, so neither do the decisions: each is taken while its node is built.
+// Eight warps build their own subtrees with warp barriers only, thread 0 the
+// few nodes above them, then follows the decision bytes down from the root.
+// *out receives the chosen leaf and *root the leaves' total.  Every thread
+// of the (256-thread) block must call it.
+__device__ void tree_descend(const double* leaves, double* tree, uint8_t* go_right, int levels,
+                             const double* u_level, int* out, double* root) {
     const int n = 1 << levels;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ls = levels >= 3 ? 3 : 0;          // log2 of the number of subtrees
     const int S = 1 << ls;
     auto mass = [&](int k) { return k >= n ? leaves[k - n] : tree[k]; };
+    auto build = [&](int k, int d) {
+        const double mL = mass(2 * k), mR = mass(2 * k + 1);
+        const double m = mL + mR;
+        tree[k] = m;
+        go_right[k] = (u_level[d] * m < mL) ? 0 : 1;
+    };
     if (warp < S) {
         for (int h = levels - 1; h >= ls; --h) {     // depth h: nodes [2^h, 2^(h+1)), 2^(h-ls) per subtree
             const int per = 1 << (h - ls);
             const int k0 = (1 << h) + warp * per;
-            for (int i = lane; i < per; i += 32) {
-                const int k = k0 + i;
-                tree[k] = mass(2 * k) + mass(2 * k + 1);
-            }
+            for (int i = lane; i < per; i += 32) build(k0 + i, h);
             __syncwarp();
         }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int k = S - 1; k >= 1; --k) tree[k] = mass(2 * k) + mass(2 * k + 1);
+        for (int h = ls - 1; h >= 0; --h)
+            for (int k = 1 << h; k < (2 << h); ++k) build(k, h);
         int node = 1;
-        for (int d = 0; d < levels; ++d) {
-            const int lc = 2 * node;
-            const double mL = mass(lc), mR = mass(lc + 1);
-            node = (u_level[d] * (mL + mR) < mL) ? lc : lc + 1;
-        }
+        for (int d = 0; d < levels; ++d) node = 2 * node + go_right[node];
         *out = levels > 0 ? node - n : 0;
+        *root = levels > 0 ? tree[1] : leaves[0];
     }
 }
 
+// Mass of one 256-column residual chunk: the float sum of its four quarter
+// masses (as residual_tc wrote them), in double.
+__device__ __forceinline__ double rchunk_mass(float4 q) { return (double)((q.x + q.y) + (q.z + q.w)); }
+
 template <int PT, int UT, int WT>
 __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
-    __shared__ double cm[1024];        // node masses: chunk masses first, then leaf weights
-    __shared__ double tree[1024];      // inner nodes of the sum tree over cm
+    __shared__ double cm[1024];          // leaves: top-tree leaf masses first, then leaf weights
+    __shared__ double tree[1024];        // inner nodes of the sum tree over cm
+    __shared__ uint8_t go_right[1024];   // the walk's decision at every inner node
     __shared__ float e_sh[1024];
-    __shared__ double sh[8];
-    __shared__ double s_u[32];         // the uniform of every tree level
-    __shared__ int s_chunk, s_leaf;
-    __shared__ int s_use_p;
+    __shared__ double s_u[32];           // the uniform of every tree level
+    __shared__ int s_leaf, s_chunk;
+    __shared__ double s_root;
     pdl_launch_dependents();
     pdl_wait();
     const int r = blockIdx.x;
@@ -459,38 +483,72 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
     const uint32_t req = A.req_ids ? A.req_ids[r] : (uint32_t)r;
     if (tid < L) s_u[tid] = rng_uniform_d(philox_key(A.seed), req, (uint32_t)pos, 2u, (uint32_t)tid);
     const double lp = A.lsep_ws[(size_t)r * G1 + (pos - 1)];
-    if (mode == kModeResidual)
-        for (int i = tid; i < A.r; i += blockDim.x) e_sh[i] = A.code[((size_t)r * A.gamma + (pos - 1)) * A.r + i];
-    // chunk masses: 256-wide residual masses (their total decides whether the
-    // residual is empty), or 1024-wide masses of p
+    // The tree over the 2^L leaves (columns) is walked in pieces: the top
+    // levels over chunk masses, then inside the chosen chunk over exact
+    // leaf weights.  `above` counts the levels walked before the chunk.
     bool use_p = mode != kModeResidual;
+    int clog = kChunkLog2, above = 0;
     if (!use_p) {
-        const int Ltop = L > kRChunkLog2 ? L - kRChunkLog2 : 0;
-        double tot = 0.0;
-        for (int c = tid; c < (1 << Ltop); c += blockDim.x) {
-            double m = 0.0;
-            if (c < A.nch256) {
-                const float4 q4 = *reinterpret_cast<const float4*>(A.rpart + ((size_t)r * A.nch256 + c) * 4);
-                m = (((double)q4.x + (double)q4.y) + (double)q4.z) + (double)q4.w;
+        // residual: masses of the 256-column chunks of max(p_j - q_j, 0); with
+        // more than 1024 chunks (V > 2^18) a top-tree leaf is a group of 2^lg
+        // neighbouring chunks, its mass their pairwise sum
+        for (int i = tid; i < A.r; i += blockDim.x) e_sh[i] = A.code[((size_t)r * A.gamma + (pos - 1)) * A.r + i];
+        clog = kRChunkLog2;
+        const int Lc = L > kRChunkLog2 ? L - kRChunkLog2 : 0;
+        const int Ltop = Lc < 10 ? Lc : 10;
+        const int lg = Lc - Ltop;                      // 0, 1 or 2
+        const int ntop = 1 << Ltop;
+        const float4* rp = reinterpret_cast<const float4*>(A.rpart) + (size_t)r * A.nch256;
+        float4 q[4][4];                                // [leaf of this thread][chunk of the leaf]
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int c = ((tid + 256 * t) << lg) + g;
+                const bool in = tid + 256 * t < ntop && g < (1 << lg) && c < A.nch256;
+                q[t][g] = in ? rp[c] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            cm[c] = m;
-            tot += m;
-        }
-        tot = warp_sum_d(tot);
-        if (lane == 0) sh[warp] = tot;
-        __syncthreads();
-        if (tid == 0) {
-            double t = 0.0;
-            for (int i = 0; i < 8; ++i) t += sh[i];
-            s_use_p = t > 0.0 ? 0 : 1;        // empty residual (rounding only): draw from p_j
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int c = tid + 256 * t;
+            if (c < ntop) {
+                const double m0 = rchunk_mass(q[t][0]), m1 = rchunk_mass(q[t][1]);
+                const double m2 = rchunk_mass(q[t][2]), m3 = rchunk_mass(q[t][3]);
+                cm[c] = lg == 0 ? m0 : (lg == 1 ? m0 + m1 : (m0 + m1) + (m2 + m3));
+            }
         }
         __syncthreads();
-        use_p = s_use_p != 0;
+        tree_descend(cm, tree, go_right, Ltop, s_u, &s_leaf, &s_root);
+        __syncthreads();
+        if (s_root > 0.0) {
+            if (tid == 0) {
+                // the levels inside a group of chunks (none unless V > 2^18)
+                const int base = s_leaf << lg;
+                int sub = 0;
+                if (lg > 0) {
+                    double m[4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+                        m[g] = (g < (1 << lg) && base + g < A.nch256) ? rchunk_mass(rp[base + g]) : 0.0;
+                    if (lg == 1) {
+                        sub = (s_u[Ltop] * (m[0] + m[1]) < m[0]) ? 0 : 1;
+                    } else {
+                        const double a0 = m[0] + m[1], a1 = m[2] + m[3];
+                        const int h = (s_u[Ltop] * (a0 + a1) < a0) ? 0 : 1;
+                        sub = 2 * h + ((s_u[Ltop + 1] * (m[2 * h] + m[2 * h + 1]) < m[2 * h]) ? 0 : 1);
+                    }
+                }
+                s_chunk = base + sub;
+            }
+            above = Lc;
+        } else {
+            use_p = true;                  // empty residual (rounding only): draw from p_j
+        }
     }
-    const int clog = use_p ? kChunkLog2 : kRChunkLog2;
-    const int Ltop = L > clog ? L - clog : 0;
     if (use_p) {
-        for (int c = tid; c < (1 << Ltop); c += blockDim.x) {
+        clog = kChunkLog2;
+        above = L > kChunkLog2 ? L - kChunkLog2 : 0;
+        for (int c = tid; c < (1 << above); c += blockDim.x) {
             double m = 0.0;
             if (c < A.nch) {
                 const float2 p2 = A.vparts[((size_t)r * G1 + (pos - 1)) * A.nch + c];
@@ -498,15 +556,14 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
             }
             cm[c] = m;
         }
+        __syncthreads();
+        tree_descend(cm, tree, go_right, above, s_u, &s_chunk, &s_root);
     }
-    __syncthreads();
-    // top levels over the chunk masses
-    tree_descend(cm, tree, Ltop, s_u, &s_chunk);
     __syncthreads();
     const int chunk = s_chunk;
     // exact leaf weights of the chosen chunk, in double; the P (and U) values
     // of this thread's columns are fetched first
-    const int Lbot = L - Ltop;
+    const int Lbot = L - above;
     const int nleaf = 1 << Lbot;           // <= 256 (residual) or 1024 (p)
     const double invT = 1.0 / (double)A.T;
     float pvals[4], uval = 0.f;
@@ -568,7 +625,7 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
         cm[i] = w;
     }
     __syncthreads();
-    tree_descend(cm, tree, Lbot, s_u + Ltop, &s_leaf);
+    tree_descend(cm, tree, go_right, Lbot, s_u + above, &s_leaf, &s_root);
     __syncthreads();
     if (tid == 0) {
         int y = (chunk << clog) + s_leaf;
@@ -594,6 +651,7 @@ size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
     off = align_up(off + kCounterBytes, 256);                            // counters, flags
     off = align_up(off + (size_t)R * sizeof(int), 256);                 // rej_list
     off = align_up(off + 2ull * R * sizeof(int), 256);                  // live requests of the waves
+    off = align_up(off + (size_t)R * sizeof(int), 256);                 // live_mark
     const size_t rpad = (size_t)((R + 127) / 128) * 128;
     off = align_up(off + 3 * rpad * r * sizeof(uint16_t), 256);          // a_res: hi, mid, lo planes
     return off;
@@ -624,6 +682,8 @@ int verify_carve(VerifyArgs& a, size_t ws_bytes) {
     off = align_up(off + (size_t)a.R * sizeof(int), 256);
     a.alive = reinterpret_cast<int*>(base + off);
     off = align_up(off + 2ull * a.R * sizeof(int), 256);
+    a.live_mark = reinterpret_cast<int*>(base + off);
+    off = align_up(off + (size_t)a.R * sizeof(int), 256);
     a.a_res = reinterpret_cast<uint16_t*>(base + off);
     return DSPARK_OK;
 }

@@ -56,12 +56,13 @@ def test_invalid_arguments_rejected_before_any_device_work():
                                  null, null, null, null, null, 0, null) == -3
     assert L.dspark_verify(null, 0, null, 0, null, 1, null, null, null, null, null, 4, 0, 4096, 32, 0, null,
                            1.0, null, null, null, null, null, null, 0, null) == -3
-    # sampled verification keeps the vocabulary within 2^18 (greedy within 2^20)
-    big = (1 << 18) + 8
-    assert L.dspark_verify(null, 0, null, 0, null, 1, null, null, null, null, null, 4, 5, big, 32, 0, null,
-                           1.0, null, null, null, null, null, null, 0, null) == -3
-    assert L.dspark_verify(null, 0, null, 0, null, 1, null, null, null, null, null, 4, 5, big, 32, 0, null,
-                           0.0, null, null, null, null, null, null, 0, null) == -1
+    # the vocabulary stays within 2^20, sampled or greedy
+    big = (1 << 20) + 8
+    for t in (1.0, 0.0):
+        assert L.dspark_verify(null, 0, null, 0, null, 1, null, null, null, null, null, 4, 5, big, 32, 0, null,
+                               t, null, null, null, null, null, null, 0, null) == -3
+        assert L.dspark_verify(null, 0, null, 0, null, 1, null, null, null, null, null, 4, 5, 1 << 20, 32, 0,
+                               null, t, null, null, null, null, null, null, 0, null) == -1
     assert L.dspark_schedule(null, null, 10, 4, 5, null, null, null, null, 0, null) == -1
     assert L.dspark_schedule(null, null, 10, 1000, 16, null, null, null, null, 0, null) == -3
 

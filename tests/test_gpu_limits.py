@@ -1,5 +1,5 @@
 """GPU parity at the documented size limits (include/dspark.h): gamma = 64,
-V = 2^18 for sampled verification and 2^20 for greedy, r = 1024 (the CUDA-core
+V up to 2^20 (sampled, where the verifier groups residual chunks, and greedy), r = 1024 (the CUDA-core
 sweep), the RNN head at r = 512 (tensor-core GRU, CUDA-core sweep), eight
 128-request M-groups, and a d = 16384 confidence head.  Comparison rules as in
 test_gpu_parity.py."""
@@ -27,6 +27,9 @@ LIMITS = {
     "gamma64": synth.Workload("gamma64", R=3, gamma=64, V=4104, r=64, T=1.0),
     "v2p18_sampled": synth.Workload("v2p18", R=2, gamma=2, V=1 << 18, r=64, T=1.0),
     "v2p20_greedy": synth.Workload("v2p20", R=2, gamma=2, V=1 << 20, r=32, T=0.0, sigma_u=2.0),
+    # more than 1024 residual chunks: the sampler groups them four to a top-tree leaf
+    "v2p20_sampled": synth.Workload("v2p20s", R=4, gamma=2, V=(1 << 20) - 8, r=32, T=1.0, sigma_pnoise=2.0),
+    "v2p19_sampled": synth.Workload("v2p19s", R=4, gamma=2, V=(1 << 19) + 24, r=32, T=1.0, sigma_pnoise=2.0),
     "r1024": synth.Workload("r1024", R=3, gamma=2, V=2056, r=1024, T=1.0, sigma_w=0.01),
     "rnn_r512": synth.Workload("rnn_r512", R=4, gamma=2, V=4104, r=512, T=1.0, head="rnn", d=128, sigma_w=0.01),
     "mg8": synth.Workload("mg8", R=1024, gamma=2, V=1032, r=64, T=1.0),
@@ -53,6 +56,9 @@ def test_limits_draft_and_verify(name):
     ov = oracle_verify_on(w, x, o, seed)
     nv, nvf = compare_verify(gv, ov, np.ones(w.R, bool), tag=name)
     assert nv + nvf == w.R
+    if name.endswith("_sampled"):
+        # the residual draw (not only the bonus draw) is exercised
+        assert (np.asarray(ov["accept_len"]) < w.gamma).any()
 
 
 def test_limits_confidence_head_d16384():
