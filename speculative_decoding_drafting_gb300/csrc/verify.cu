@@ -77,12 +77,22 @@ __device__ __forceinline__ int live_request(const VerifyArgs& A, int w, int i) {
     return w == 1 ? i : A.alive[(size_t)(w & 1) * A.R + i];
 }
 
+// The counter block of the workspace: rej_count (+0), vflags (+16), live
+// requests per wave (+32: gamma + 2 ints).  The first pass-1 launch of a
+// call clears it (block 0, before it lets the acceptance pass launch).
+constexpr size_t kCounterBytes = 512;
+static_assert(32 + 4 * (64 + 2) <= kCounterBytes, "wave counters");
+
 // ------------------------------------------------------------------ pass 1
 // Warp tasks over (live request, row of the window, 1024-column chunk).
 // STAGE: also copy each row read into A.P_stage (P is host memory, and the
 // later passes read the rows from there instead of across the link again).
 template <int PT, bool GREEDY, bool STAGE>
 __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
+    // wave 1 is the call's first kernel, launched after all earlier work:
+    // its block 0 clears the counters before any acceptance pass can start
+    if (w == 1 && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < (int)(kCounterBytes / 4); i += blockDim.x) A.rej_count[i] = 0;
     pdl_launch_dependents();
     pdl_wait();   // the list of live requests (waves after the first)
     const int lane = threadIdx.x & 31;
@@ -636,9 +646,6 @@ __global__ void __launch_bounds__(256) verify_sample(VerifyArgs A) {
 
 // ------------------------------------------------------------------ host
 static int nch_of(int V) { return (V + kChunk - 1) / kChunk; }
-// rej_count (+0), vflags (+16), live requests per wave (+32: gamma + 2 ints)
-constexpr size_t kCounterBytes = 512;
-static_assert(32 + 4 * (64 + 2) <= kCounterBytes, "wave counters");
 static int nch256_of(int V) { return (V + kRChunk - 1) / kRChunk; }
 
 size_t verify_workspace_bytes(int R, int gamma, int V, int r) {
@@ -693,8 +700,7 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     const bool greedy = !(a.T > 0.f);
     const int nsm = num_sms();
     const int G1 = a.gamma + 1;
-    cudaError_t e = cudaMemsetAsync(a.rej_count, 0, kCounterBytes, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     a.unit_waves = a.P_stage ? 1 : 0;
     const bool unit = a.unit_waves != 0;
     // the waves: the first pass 1 waits for the caller's work (and the
