@@ -80,7 +80,7 @@ struct TcParams {
     int R, V, r, k;          // k = 1-based step
     int ntiles, nslices;
     float c2;                // log2(e) / T
-    int nsplit;              // bf16 terms of the code: 1 (bf16-exact codes) or 3 (f32 codes, hi + mid + lo)
+    int nsplit;              // bf16 terms of the code: 1 (bf16-exact codes), 2 or 3 (f32 codes: hi + mid (+ lo))
     int nacc;                // TMEM accumulators: 2, or 1 when the split A needs the room
 };
 
@@ -311,6 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if (p.nsplit == 1)
                 issue_mma<1, CS>(S, p, tmem, acol, nt, kblocks);
+            else if (p.nsplit == 2)
+                issue_mma<2, CS>(S, p, tmem, acol, nt, kblocks);
             else
                 issue_mma<3, CS>(S, p, tmem, acol, nt, kblocks);
         }
@@ -598,8 +600,12 @@ cudaError_t launch_typed(DraftArgs& a, int k, cudaStream_t s) {
     p.U = a.U;
     p.gamma = a.gamma;
     p.ebf = a.ebf;
-    // RNN codes tanh(out) are f32: three bf16 terms (exact); Markov codes are W1 rows
-    p.nsplit = a.rnn ? 3 : 1;
+    // Markov codes are W1 rows (bf16); RNN codes tanh(out) are f32: three
+    // bf16 terms hi + mid + lo (exact) when they fit in tensor memory beside
+    // two accumulators (r <= 128), else hi + mid, which keep 16 significant
+    // bits of every code element (the dropped term is below 2^-16 of it)
+    // and keep the MMA of tile t + 1 overlapping the epilogue of tile t
+    p.nsplit = a.rnn ? ((3 * (a.r / 2) + kNACC * kBN <= (int)kTmemCols) ? 3 : 2) : 1;
     p.nacc = (p.nsplit * (a.r / 2) + kNACC * kBN <= (int)kTmemCols) ? kNACC : 1;
     p.parts = a.parts + (size_t)(k & 1) * a.parts_stride;
     p.cmass = a.cmass;

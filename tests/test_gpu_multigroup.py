@@ -29,6 +29,9 @@ MULTI = {
     # RNN head: f32 codes as three bf16 terms on the tensor cores, clusters of two and four
     "mg2_rnn": synth.Workload("mg2_rnn", R=256, gamma=2, V=4104, r=64, T=1.0, head="rnn", d=96),
     "mg4_rnn": synth.Workload("mg4_rnn", R=512, gamma=2, V=2056, r=128, T=0.8, head="rnn", d=64),
+    # RNN head at r = 256: the sweep's codes as two bf16 terms (three would leave
+    # tensor memory for one accumulator only); every request compared
+    "mg2_rnn256": synth.Workload("mg2_rnn256", R=256, gamma=3, V=4104, r=256, T=1.0, head="rnn", d=96),
 }
 
 
