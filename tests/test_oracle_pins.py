@@ -200,6 +200,31 @@ def test_two_level_gumbel_draft_law_over_many_chunks():
     assert stats.chisquare(np.bincount(chunk, minlength=5), n * cm).pvalue > 1e-3
 
 
+def test_single_chunk_draft_is_textbook_gumbel_max():
+    """With V <= 256 there is one chunk, so its race is decided and the draft
+    is the plain Gumbel-max over the whole vocabulary: x_k = argmax_v z_v + G_v,
+    G_v = -ln(-ln u_v), u_v the stream-0 uniform of (request, position k, v),
+    z = (U_k + W1[x_{k-1}] W2) / T.  Checked token by token, through an
+    independent matmul and the known-answer-pinned generator, with request ids
+    that are not the row numbers."""
+    rng = np.random.default_rng(41)
+    R, gamma, V, r, T, seed = 6, 3, 200, 5, 0.8, (9 << 32) | 1234
+    U = rng.normal(0, 1.5, (R, gamma, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.4, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.4, (r, V)).astype(np.float32)
+    anchor = rng.integers(0, V, R).astype(np.int32)
+    req = (1000 + 37 * np.arange(R)).astype(np.uint32)
+    d = oracle.draft_markov(U, anchor, W1, W2, T, seed, req_ids=req)
+    prev = np.concatenate([anchor[:, None], d["tokens"][:, :-1]], axis=1)
+    z = (U + np.einsum("rki,iv->rkv", W1.astype(np.float64)[prev], W2.astype(np.float64))) / T
+    for i in range(R):
+        for k in range(1, gamma + 1):
+            u = np.array([oracle.rng_uniform(seed, int(req[i]), k, 0, v) for v in range(V)])
+            key = z[i, k - 1] - np.log(-np.log(u))
+            assert d["tokens"][i, k - 1] == int(np.argmax(key))
+    np.testing.assert_allclose(d["lse"], special.logsumexp(z, axis=2), rtol=1e-12)
+
+
 def test_two_level_gumbel_draft_never_leaves_the_only_live_chunk():
     V, R = 1024, 64
     U = np.full((R, 2, V), -1.0e4, np.float32)
