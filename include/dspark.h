@@ -161,6 +161,9 @@ size_t dspark_draft_workspace_size(int R, int gamma, int V, int r, int d);
  * lowest v on ties.  B_k and q_k are never written to memory.
  * Requirements: R >= 1, 1 <= gamma <= 64, V >= 2 with V % 8 == 0 for bf16 and
  * V % 4 == 0 for f32 storage, V <= 2^20, 1 <= r <= 1024, T >= 0 and finite.
+ * A logit of -inf (in U here, in U or P for verification) masks its column:
+ * the column has no mass and is never drawn; every row needs at least one
+ * finite logit.  NaN and +inf logits are not supported.
  */
 int dspark_draft_markov(const void* U, int u_dtype, const int32_t* anchor,
                         const void* W1, const void* W2, int w_dtype,

@@ -32,10 +32,12 @@ cudaError_t launch_verify_tc_residual(VerifyArgs& a, cudaStream_t s);
 
 // exp(a) for a double argument without double-precision transcendentals:
 // exp(a_hi) in float times the first-order correction for a - a_hi
-// (relative error about 1e-7 for |a| < 80).
+// (relative error about 1e-7 for |a| < 80).  exp(-inf) = 0: a masked logit
+// (-inf) has no mass, and neither has an argument that underflows.
 __device__ __forceinline__ double exp_from_double(double a) {
     const float ah = (float)a;
-    return (double)expf(ah) * (1.0 + (a - (double)ah));
+    const float e = expf(ah);
+    return e == 0.f ? 0.0 : (double)e * (1.0 + (a - (double)ah));
 }
 
 __device__ __forceinline__ int verify_len_of(const VerifyArgs& A, int r) {
@@ -164,12 +166,14 @@ __global__ void __launch_bounds__(256) verify_pass1(VerifyArgs A, int w) {
                 for (int q = 0; q < 4; ++q)
                     if (ok[i]) m = fmaxf(m, x[4 * i + q] * invT);
             const float mw = warp_max(m);
+            // a chunk of masked logits only (all -inf) has no mass: (-inf, 0)
+            const float mr = mw == -INFINITY ? 0.f : mw;
             float s = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    if (ok[i]) s += ex2_approx((x[4 * i + q] * invT - mw) * kLog2e);
+                    if (ok[i]) s += ex2_approx((x[4 * i + q] * invT - mr) * kLog2e);
             s = warp_sum(s);
             out = make_float2(mw, s);
         }

@@ -286,3 +286,72 @@ def test_verify_staged_host_targets(gamma, T, V, pdt):
     for r in range(w.R):
         d = int(host(b["accept_len"])[r])
         np.testing.assert_array_equal(st[r, d], x["P"][r, d])     # the decision row was staged
+
+
+MASKED = {
+    "f32_tc": synth.Workload("masked_f32_tc", R=6, gamma=4, V=20488, r=64, T=1.0),
+    "bf16_storage_T08": synth.Workload("masked_bf16_T08", R=5, gamma=3, V=12296, r=128, T=0.8,
+                                       u_dtype=BF16, p_dtype=BF16, sigma_pnoise=1.2),
+    "greedy": synth.Workload("masked_greedy", R=5, gamma=4, V=16392, r=64, T=0.0, sigma_u=2.0, sigma_pnoise=0.7),
+    "f32_generic": synth.Workload("masked_f32_r7", R=3, gamma=2, V=5124, r=7, T=1.3, w_dtype=F32, sigma_w=0.3),
+}
+
+
+def _mask(a: np.ndarray, cols: np.ndarray):
+    """Set columns `cols` of every row of a (f32 or bf16 bits) to -inf."""
+    a[..., cols] = np.uint16(0xFF80) if a.dtype == np.uint16 else np.float32(-np.inf)
+
+
+@pytest.mark.parametrize("name", list(MASKED))
+def test_masked_vocabulary_parity(name):
+    """Masked columns (logits of -inf) carry no mass on either side: closed to
+    both the draft and the target (one whole 2048-column block, which covers
+    two of the target pass's 1024-column chunks and eight of the draft's
+    256-column chunks, and a random fifth of the rest), or open to the draft
+    and closed to the target, so that such drafts are rejected with p = 0.
+    Draft and verification must match the oracle, no column closed to the
+    draft may be drafted, and no token may be emitted from a target row that
+    closes it."""
+    w = MASKED[name]
+    x = synth.gen_all(w)
+    rng = np.random.default_rng(11)
+    both = np.concatenate([np.arange(2048, 4096), rng.choice(np.arange(4096, w.V), (w.V - 4096) // 5, replace=False)])
+    open_cols = np.setdiff1d(np.arange(w.V), both)
+    p_only = rng.choice(open_cols, w.V // 20, replace=False)
+    _mask(x["U"], both)
+    _mask(x["P"], both)
+    _mask(x["P"], p_only)
+    seed = 31
+    g = gpu_draft(w, x, seed)
+    o = oracle_draft(w, x, seed)
+    _, _, m = compare_draft(g, o, tag=name)
+    assert not np.isin(g["tokens"], both).any()
+    same = (g["tokens"] == o["tokens"]).all(axis=1)
+    gv = gpu_verify_on(w, x, g, seed)
+    ov = oracle_verify_on(w, x, o, seed)
+    compare_verify(gv, ov, same, tag=name)
+    # verification of the oracle's drafts, some of them closed to the target:
+    # request i (even) finds its draft at position 1 + i // 2 closed in P
+    dr = oracle_draft(w, x, 5)
+    for i in range(0, w.R, 2):
+        k = min(i // 2, w.gamma - 1)
+        t = int(dr["tokens"][i, k])
+        if x["P"].dtype == np.uint16:
+            x["P"][i, k, t] = np.uint16(0xFF80)
+        else:
+            x["P"][i, k, t] = np.float32(-np.inf)
+    gv = gpu_verify_on(w, x, dr, 5)
+    ov = oracle_verify_on(w, x, dr, 5)
+    n, nflag = compare_verify(gv, ov, np.ones(w.R, bool), tag=name)
+    assert n + nflag == w.R
+    if w.T > 0:
+        # a draft the target has closed is rejected with p(x) = 0 (request 0:
+        # position 1 is the one closed)
+        assert ov["accept_len"][0] == 0 and gv["accept_len"][0] == 0 and gv["p_tok"][0, 0] == 0.0
+    # every emitted token (accepted draft, residual draw, bonus) is open in
+    # the target row it was decided on: output slot j comes from row j
+    Pf = synth.bf16_bits_to_f32(x["P"]) if x["P"].dtype == np.uint16 else x["P"]
+    for i in range(w.R):
+        for j in range(int(gv["n_out"][i])):
+            t = int(gv["out_tokens"][i, j])
+            assert np.isfinite(Pf[i, j, t]), f"{name}: request {i} emitted column {t}, closed in target row {j}"

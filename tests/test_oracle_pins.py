@@ -121,6 +121,44 @@ def test_toy_monte_carlo_output_law_and_acceptance():
     assert np.all(v["n_out"] >= 1)
 
 
+def test_masked_columns_have_no_mass():
+    """Logits of -inf (masked columns) carry no probability: the draft follows
+    softmax over the open columns (a whole chunk masked included), the
+    verification emits the target's law over its open columns, and a draft
+    the target has masked is always rejected."""
+    rng = np.random.default_rng(23)
+    V, n = 700, 200_000
+    u = rng.normal(0, 1.0, V)
+    p = u + rng.normal(0, 0.7, V)
+    u[256:512] = -np.inf                                  # one whole chunk closed to both
+    u[rng.choice(V, 120, replace=False)] = -np.inf
+    p[np.isinf(u)] = -np.inf
+    closed_p = rng.choice(np.nonzero(np.isfinite(u))[0], 40, replace=False)
+    p[closed_p] = -np.inf                                 # open to the draft, closed to the target
+    u = u.astype(np.float32).astype(np.float64)           # the values as stored
+    p = p.astype(np.float32).astype(np.float64)
+    U = np.broadcast_to(u.astype(np.float32), (n, 1, V)).copy()
+    P = np.broadcast_to(np.stack([p, p]).astype(np.float32), (n, 2, V)).copy()
+    W1 = np.zeros((V, 1), np.float32)
+    W2 = np.zeros((1, V), np.float32)
+    d = oracle.draft_markov(U, np.zeros(n, np.int32), W1, W2, 1.0, 123)
+    q = special.softmax(u)
+    assert np.all(np.isfinite(u[d["tokens"][:, 0]]))
+    open_u = np.isfinite(u)
+    cnt = np.bincount(d["tokens"][:, 0], minlength=V)[open_u]
+    assert stats.chisquare(cnt, n * q[open_u]).pvalue > 1e-3
+    np.testing.assert_allclose(d["lse"][:, 0], special.logsumexp(u), rtol=1e-13)
+    v = oracle.verify(P, U, W2, d["tokens"], d["qx"], d["lse"], d["code"], 1.0, 123)
+    first = v["out_tokens"][:, 0]
+    assert np.all(np.isfinite(p[first]))
+    drafted_closed = np.isin(d["tokens"][:, 0], closed_p)
+    assert drafted_closed.any() and np.all(v["accept_len"][drafted_closed] == 0)
+    np.testing.assert_array_equal(v["px"][drafted_closed, 0], 0.0)
+    pt = special.softmax(p)
+    open_p = np.isfinite(p)
+    assert stats.chisquare(np.bincount(first, minlength=V)[open_p], n * pt[open_p]).pvalue > 1e-3
+
+
 def test_q_equals_p_accepts_everything():
     """Explainer section 05: if q = p nothing is ever rejected."""
     rng = np.random.default_rng(5)
