@@ -710,10 +710,14 @@ static cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     // the waves: the first pass 1 waits for the caller's work (and the
     // cleared counters); every later launch overlaps the previous kernel's tail
     const int nw = wave_count(G1, unit);
+    // pass 1 keeps its loads in registers (32 floats a lane), so the number
+    // of resident warps bounds the bytes in flight: five 256-thread CTAs per
+    // SM at 48 registers (four for the staging variant, at 58)
+    const long long per_sm = a.P_stage ? 4 : 5;
     for (int w = 1; w <= nw; ++w) {
         const long long tasks = (long long)a.R * (wave_hi(w, G1, unit) - wave_lo(w, unit)) * a.nch;
         const long long want = (tasks + 7) / 8;
-        int grid = (int)(want < (long long)nsm * 4 ? want : (long long)nsm * 4);
+        int grid = (int)(want < (long long)nsm * per_sm ? want : (long long)nsm * per_sm);
         if (grid < 1) grid = 1;
         prof_begin(kPVerifyPass1, s);
         if (a.P_stage)

@@ -27,6 +27,9 @@ SMALL = {
     "rnn": synth.Workload("rnn", R=4, gamma=3, V=8200, r=64, T=1.0, head="rnn", d=96),
     "f32_r7": synth.Workload("f32_r7", R=3, gamma=2, V=1036, r=7, T=1.3, w_dtype=F32, sigma_w=0.3),
     "tiny": synth.Workload("tiny", R=1, gamma=1, V=8, r=1, T=1.0, w_dtype=F32, sigma_w=0.5),
+    # temperature extremes: near-greedy (z spans about 250 nats) and nearly flat
+    "cold_T005": synth.Workload("cold_T005", R=5, gamma=4, V=12296, r=64, T=0.05),
+    "hot_T8": synth.Workload("hot_T8", R=5, gamma=4, V=12296, r=64, T=8.0, sigma_pnoise=4.0),
 }
 
 
