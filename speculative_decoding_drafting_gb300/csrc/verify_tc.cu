@@ -18,6 +18,7 @@
 // column slice form a cluster that shares every W2 stage by multicast; a
 // cluster member whose M-group has no rejecting requests still runs the W2
 // pipeline so that its peers are served.
+#include <atomic>
 #include <cuda.h>
 
 #include "common.cuh"
@@ -431,14 +432,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Clusters of `cs` residual CTAs that fit on the device at once (0 if unknown).
+// Clusters of two residual CTAs with `smem` bytes of shared memory each that
+// fit on the device at once (0 if unknown), per device.
 template <int UT, int PT>
 int active_clusters(int cs, size_t smem) {
-    static int cache[3] = {0, 0, 0};
-    const int ci = cs == 4 ? 2 : cs - 1;
-    if (cache[ci]) return cache[ci];
-    auto kern = cs == 4 ? residual_tc<UT, PT, 4> : residual_tc<UT, PT, 2>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    constexpr int kMaxDev = 64;
+    static std::atomic<long long> cache[kMaxDev];   // (smem << 20) | count, 0 = not yet known
+    int dev = 0;
+    if (cs != 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    const long long c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0 && (size_t)(c >> 20) == smem) return (int)(c & 0xFFFFF);
+    auto kern = residual_tc<UT, PT, 2>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, cs, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -455,7 +463,7 @@ int active_clusters(int cs, size_t smem) {
         (void)cudaGetLastError();
         return 0;
     }
-    cache[ci] = n;
+    if (n > 0 && n < (1 << 20)) cache[dev].store(((long long)smem << 20) | n, std::memory_order_relaxed);
     return n;
 }
 
@@ -463,9 +471,10 @@ template <int UT, int PT>
 cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     constexpr int esu = UT == DSPARK_F32 ? 4 : 2, esp = PT == DSPARK_F32 ? 4 : 2;
     const size_t smem = smem_bytes(a.r, esu, esp);
-    // M-groups per cluster: the largest of 4, 2, 1 dividing the number of groups
+    // M-groups per cluster: pairs when the number of groups is even (clusters
+    // of four place fewer CTAs at once, as in the draft sweep)
     const int ng = (a.R + kBM - 1) / kBM;
-    int cs = ng % 4 == 0 ? 4 : (ng % 2 == 0 ? 2 : 1);
+    int cs = ng % 2 == 0 ? 2 : 1;
     int ctas = num_sms();
     if (cs > 1) {
         const int nc = active_clusters<UT, PT>(cs, smem);
@@ -506,7 +515,7 @@ cudaError_t launch_typed(VerifyArgs& a, cudaStream_t s) {
     if (ns > a.nch256) ns = a.nch256;
     p.nslices = ns;
     p.c2 = 1.4426950408889634f / a.T;
-    auto kern = cs == 4 ? residual_tc<UT, PT, 4> : cs == 2 ? residual_tc<UT, PT, 2> : residual_tc<UT, PT, 1>;
+    auto kern = cs == 2 ? residual_tc<UT, PT, 2> : residual_tc<UT, PT, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
