@@ -1,10 +1,10 @@
 """GPU parity with several 128-request M-groups, and at the full headline size.
 
 The tensor-core draft sweep gives each 128-request M-group its own CTAs; the
-M-groups that share a column slice run as one thread-block cluster and share
-every W2 stage (two groups per cluster when their number is even, four when it
-is a multiple of four, no cluster otherwise).  These cases cover each cluster
-shape, a ragged last M-group, and the full-size launch the benchmark times
+M-groups that share a column slice run in thread-block clusters of two that
+share every W2 stage (when their number is even; no cluster otherwise, and at
+four M-groups a slice has two clusters).  These cases cover each cluster shape,
+a ragged last M-group, and the full-size launch the benchmark times
 (R = 256, gamma = 5, V = 151936, r = 256), where the oracle checks a sample of
 requests through their request ids.
 """
@@ -22,11 +22,11 @@ MULTI = {
     "mg2": synth.Workload("mg2", R=256, gamma=2, V=6152, r=64, T=1.0),
     # three M-groups (the last one 44 requests) -> no cluster
     "mg3": synth.Workload("mg3", R=300, gamma=2, V=4104, r=128, T=0.9),
-    # four M-groups -> clusters of four (each W2 stage in four 32-row pieces)
+    # four M-groups -> two clusters of two per slice
     "mg4": synth.Workload("mg4", R=512, gamma=2, V=4104, r=64, T=1.0),
     # greedy with two M-groups
     "mg2_greedy": synth.Workload("mg2_greedy", R=256, gamma=2, V=4104, r=64, T=0.0, sigma_u=2.0),
-    # RNN head: f32 codes as three bf16 terms on the tensor cores, clusters of two and four
+    # RNN head: f32 codes as three bf16 terms on the tensor cores, two and four M-groups
     "mg2_rnn": synth.Workload("mg2_rnn", R=256, gamma=2, V=4104, r=64, T=1.0, head="rnn", d=96),
     "mg4_rnn": synth.Workload("mg4_rnn", R=512, gamma=2, V=2056, r=128, T=0.8, head="rnn", d=64),
     # RNN head at r = 256: the sweep's codes as two bf16 terms (three would leave
@@ -62,8 +62,8 @@ def test_draft_parity_multigroup(name):
                                                 ("mg2_rnn", "all"), ("mg4_rnn", "random")])
 def test_verify_parity_multigroup(name, mode):
     """The residual pass runs one CTA per 128 rejecting requests and column
-    slice, clusters of 2 or 4 M-groups sharing W2; with random verify lengths
-    fewer requests reject and the last M-groups of a cluster may be empty."""
+    slice, clusters of two M-groups sharing W2; with random verify lengths
+    fewer requests reject and the last M-group of a cluster may be empty."""
     w = MULTI[name]
     x = synth.gen_all(w)
     dr = oracle_draft(w, x, 8)
