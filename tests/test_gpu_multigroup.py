@@ -77,19 +77,21 @@ def test_verify_parity_multigroup(name, mode):
     flags.check(name)
 
 
-@pytest.mark.parametrize("name", ["headline", "greedy", "rnn", "longblock"])
+@pytest.mark.parametrize("name", ["headline", "dspark5", "greedy", "rnn", "longblock"])
 def test_full_size_sampled(name):
-    """Full-size launches: the benchmark's headline cycle, the greedy one, the
-    RNN head (gamma = 8, d = 2048) and the long block (R = 512, gamma = 16,
-    bf16 storage, T = 0.8).  GPU draft and verify run on every request; the
-    oracle recomputes a sample of requests (every M-group, its edges) from the
-    same bytes and request ids."""
+    """Full-size launches: the benchmark's headline cycle, DSpark-5 at 64
+    requests (one M-group, half of its rows empty), the greedy cycle, the RNN
+    head (gamma = 8, d = 2048) and the long block (R = 512, gamma = 16, bf16
+    storage, T = 0.8).  GPU draft and verify run on every request; the oracle
+    recomputes a sample of requests (every M-group, its edges) from the same
+    bytes and request ids."""
     w = synth.WORKLOADS[name]
     x = synth.gen_all(w)
     seed = 2024
     g = gpu_draft(w, x, seed)
     gv = gpu_verify_on(w, x, g, seed)
-    idx = np.array(sorted({0, 1, 126, 127, 128, 200, w.R // 2 + 5, w.R - 129, w.R - 2, w.R - 1}))
+    idx = np.array(sorted(i for i in {0, 1, 126, 127, 128, 200, w.R // 2 + 5, w.R - 129, w.R - 2, w.R - 1}
+                          if 0 <= i < w.R))
     xs = {k: (v[idx] if k in ("U", "P", "anchor", "H") else v) for k, v in x.items()}
     o = oracle_draft(w, xs, seed, req_ids=idx.astype(np.uint32))
     gs = {k: v[idx] for k, v in g.items()}
