@@ -96,6 +96,31 @@ def test_cycle_end_to_end(name):
     compare_verify(gv, ov, same, tag=name)
 
 
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_q_equal_to_p_accepts_every_draft(T):
+    """Explainer section 05: where the target's distribution equals the
+    draft's, nothing is rejected.  W2 = 0 makes q_k = softmax(U_k / T); the
+    target rows repeat U (the bonus row repeats the last position), so p = q
+    and every block is accepted whole, with its bonus token drawn from
+    softmax(U_gamma / T).  The only admissible exception is a uniform within
+    the flag band of a ratio that rounding puts a hair below 1."""
+    w = synth.Workload("q_eq_p", R=48, gamma=4, V=4104, r=64, T=T)
+    x = synth.gen_all(w)
+    x["W2"] = synth.f32_to_bf16_bits(np.zeros((w.r, w.V), np.float32))
+    x["P"] = np.concatenate([x["U"], x["U"][:, -1:, :]], axis=1)
+    seed = 404
+    g = gpu_draft(w, x, seed)
+    o = oracle_draft(w, x, seed)
+    compare_draft(g, o, tag="q_eq_p")
+    gv = gpu_verify_on(w, x, g, seed)
+    ov = oracle_verify_on(w, x, g, seed)
+    assert np.all(ov["accept_len"] == w.gamma)
+    ok = ov["min_gap"] >= 1e-6
+    assert np.all(gv["accept_len"][ok] == w.gamma) and np.all(gv["n_out"][ok] == w.gamma + 1)
+    np.testing.assert_array_equal(gv["out_tokens"][ok, : w.gamma], g["tokens"][ok])
+    compare_verify(gv, ov, np.ones(w.R, bool), tag="q_eq_p")
+
+
 def test_verify_many_requests_statistics():
     """Many requests of a small vocabulary: parity on each request, and the
     empirical first-position acceptance matches 1 - TV of the oracle's p and q."""
