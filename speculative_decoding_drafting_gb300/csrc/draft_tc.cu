@@ -24,11 +24,11 @@
 //           keeps each chunk's (reference, sum of 2^(y - reference)) pair,
 //           greedy the running argmax of the logits
 //
-// The M-groups that share a column slice form a thread-block cluster: every
-// W2 stage is cut into one piece per CTA, each CTA loads its piece and the
-// copy is multicast to all of them, so W2 leaves HBM once per slice however
-// many M-groups read it.  A stage is reused only after every CTA's MMAs have
-// released it (the release is multicast as well).
+// Pairs of M-groups that share a column slice form a thread-block cluster:
+// every W2 stage is cut into one piece per CTA, each CTA loads its piece and
+// the copy is multicast to both, so a cluster reads each W2 tile once.  A
+// stage is reused only after every CTA's MMAs have released it (the release
+// is multicast as well).
 //
 // B_k and q_k never leave the SM.  Every wait is bounded (mbar_wait); a CTA
 // that gives up records DSPARK_ERR_TIMEOUT in the workspace status word,
@@ -514,8 +514,6 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, void* base, cons
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// M-groups per cluster: the largest of 4, 2, 1 that divides the number of
-// M-groups (a cluster shares every W2 stage among its CTAs).
 // M-groups per cluster: pairs when the number of M-groups is even, else one.
 // Clusters of four placed 36 at a time on a 152-SM GB300 (144 CTAs, against
 // 76 pairs), and the 512-request sweep took 64.6 us per launch with them

@@ -14,10 +14,10 @@
 // shared rows (conflict-free for the row-per-thread reads), while the rank-r
 // product runs as tcgen05.mma (M = 128 requests, N = 64 columns, K = r): the
 // codes (A) sit in tensor memory next to the accumulators, W2 tiles come by
-// TMA through a six-stage ring.  As in the draft sweep, the M-groups of a
-// column slice form a cluster that shares every W2 stage by multicast; a
+// TMA through a six-stage ring.  As in the draft sweep, pairs of M-groups of
+// a column slice form a cluster that shares every W2 stage by multicast; a
 // cluster member whose M-group has no rejecting requests still runs the W2
-// pipeline so that its peers are served.
+// pipeline so that its peer is served.
 #include <atomic>
 #include <cuda.h>
 
